@@ -1,0 +1,147 @@
+"""CPU oracle for the Mamba-2 SSD prefill forward.
+
+TEST INFRASTRUCTURE ONLY: only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import this package. The CUDA library never
+imports it, and it imports nothing from the CUDA library.
+
+The arithmetic lives in ``ssd_oracle.c``: the fp64 token-by-token recurrence
+
+    dt_t = softplus(dt_raw_t + dt_bias_h)
+    h_t  = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t (outer) B_t
+    y_t  = C_t . h_t + D_h * x_t
+
+run independently for every (batch, head) chain, with the head-to-group map
+g = h // (H / G). This module only gathers each chain's slices, converts the
+stored inputs exactly to float64, and calls the C code.
+
+Page citations: the recurrence is the selective linear recurrence of "Mamba
+hardware-aware algorithms" (section on the associative-scan foundations) with
+the discretisation of "Mamba-2 compiler optimisation" section 1.1; the state
+layout [B, H, P, N] is that page's decode-cache layout (section 2.2).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libssd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle's C source with the host compiler (gcc)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-shared", "-fPIC", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            lib.oracle_ssd_chains.argtypes = [i64, i64, i64, i64, d, d, d, d, d, d, d, d, d, d, ctypes.c_int]
+            lib.oracle_ssd_chains.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    """Exact conversion of a stored tensor (torch or numpy; f32/f16/bf16/f64) to float64 numpy."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+
+        return a.detach().to("cpu", torch.float64).contiguous().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def ssd_chains(x, dt_raw, dt_bias, A, B, C, D=None, init=None, nthreads=None):
+    """Run stacked independent chains.
+
+    x [n, L, P], dt_raw [n, L], dt_bias/A/D [n], B/C [n, L, N], init [n, P, N].
+    Returns (y [n, L, P], final [n, P, N]) as float64 arrays.
+    """
+    x, dt_raw, dt_bias, A, B, C = (_f64(v) for v in (x, dt_raw, dt_bias, A, B, C))
+    D, init = _f64(D), _f64(init)
+    n, L, P = x.shape
+    N = B.shape[-1]
+    assert dt_raw.shape == (n, L) and B.shape == (n, L, N) and C.shape == (n, L, N)
+    assert dt_bias.shape == (n,) and A.shape == (n,)
+    assert D is None or D.shape == (n,)
+    assert init is None or init.shape == (n, P, N)
+    y = np.empty((n, L, P), dtype=np.float64)
+    fin = np.empty((n, P, N), dtype=np.float64)
+    rc = _load().oracle_ssd_chains(n, L, P, N, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+                                   _ptr(D), _ptr(init), _ptr(y), _ptr(fin), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_ssd_chains rejected its arguments")
+    return y, fin
+
+
+def ssd_reference(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chains=None, nthreads=None):
+    """Oracle SSD forward on library-layout inputs.
+
+    x [b, L, H, P], dt_raw [b, L, H], dt_bias/A/D [H], B/C [b, L, G, N],
+    init_states [b, H, P, N] (None = zeros). With ``chains`` None every (b, h)
+    chain is run and (y [b, L, H, P], final [b, H, P, N]) is returned; with a
+    list of (b, h) pairs only those run and (y [n, L, P], final [n, P, N]) is
+    returned in the list's order.
+    """
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if H % G:
+        raise ValueError("nheads must be a multiple of ngroups")
+    per = H // G
+    all_chains = chains is None
+    if all_chains:
+        chains = [(bi, h) for bi in range(b) for h in range(H)]
+    bs = np.array([c[0] for c in chains], dtype=np.int64)
+    hs = np.array([c[1] for c in chains], dtype=np.int64)
+    gs = hs // per
+    if len(chains) == 0:
+        return np.empty((0, L, P)), np.empty((0, P, N))
+
+    # gather one chain at a time: keeps the exact conversion and the memory small
+    xs = np.stack([_f64(x[int(bi), :, int(h), :]) for bi, h in zip(bs, hs)])
+    dts = np.stack([_f64(dt_raw[int(bi), :, int(h)]) for bi, h in zip(bs, hs)])
+    Bs = np.stack([_f64(B[int(bi), :, int(g), :]) for bi, g in zip(bs, gs)])
+    Cs = np.stack([_f64(C[int(bi), :, int(g), :]) for bi, g in zip(bs, gs)])
+    bias = _f64(dt_bias)[hs]
+    Ah = _f64(A)[hs]
+    Dh = None if D is None else _f64(D)[hs]
+    init = None if init_states is None else np.stack([_f64(init_states[int(bi), int(h)]) for bi, h in zip(bs, hs)])
+    y, fin = ssd_chains(xs, dts, bias, Ah, Bs, Cs, Dh, init, nthreads=nthreads)
+    if not all_chains:
+        return y, fin
+    y_full = np.empty((b, L, H, P), dtype=np.float64)
+    f_full = np.empty((b, H, P, N), dtype=np.float64)
+    for k, (bi, h) in enumerate(chains):
+        y_full[bi, :, h, :] = y[k]
+        f_full[bi, h] = fin[k]
+    return y_full, f_full
