@@ -1,0 +1,125 @@
+/*
+ * ssd.h - C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked-scan prefill forward.
+ *
+ * One call computes, for every batch b and head h, the selective state-space
+ * recurrence over the whole sequence:
+ *
+ *   dt_t = softplus(dt_raw[b,t,h] + dt_bias[h])
+ *   h_t  = exp(dt_t * A[h]) * h_{t-1} + dt_t * x[b,t,h,:] (outer) B[b,t,g,:]
+ *   y[b,t,h,:] = h_t . C[b,t,g,:] + D[h] * x[b,t,h,:]
+ *   final_states[b,h] = h_{L-1},  h_{-1} = init_states[b,h] (zeros if NULL)
+ *
+ * with g = h / (nheads / ngroups). The recurrence is the one of "Mamba-2
+ * state space model compiler optimisation" (bxzpzcl.cn) section 1.1, computed
+ * the way "Accelerating Mamba2 with Kernel Fusion" (section on the SSD core
+ * operations) splits it: chunk cumsum, BMM, chunk state, state passing and
+ * chunk scan, here fused into one persistent kernel launch.
+ *
+ * Layouts (row-major, last index contiguous, no padding):
+ *   x, y            [batch, seqlen, nheads, headdim]        io dtype
+ *   dt_raw          [batch, seqlen, nheads]                 io dtype
+ *   B, C            [batch, seqlen, ngroups, dstate]        io dtype
+ *   dt_bias, A, D   [nheads]                                fp32
+ *   init_states,
+ *   final_states    [batch, nheads, headdim, dstate]        state dtype
+ *   (the state layout is the decode-cache layout of the compiler-optimisation
+ *   page, section 2.2)
+ *
+ * Ownership: the caller owns every buffer, including the workspace; the
+ * library allocates no device memory and keeps no per-call global state.
+ * All pointers except the workspace and the stream are device pointers.
+ *
+ * Errors: argument errors are detected on the host, return immediately and
+ * launch nothing. The launch itself is asynchronous on `stream`; a device-side
+ * failure (a state-passing wait that ran past its time limit) is recorded in
+ * the workspace and reported by ssd_fwd_check().
+ */
+#ifndef MAMBA_SSD_H
+#define MAMBA_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_API __attribute__((visibility("default")))
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1, /* bad shape, NULL or misaligned pointer, bad enum */
+    SSD_ERR_UNSUPPORTED = 2, /* valid problem, but no kernel instance for it */
+    SSD_ERR_WORKSPACE = 3,   /* workspace NULL, too small or misaligned */
+    SSD_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, copy) */
+    SSD_ERR_TIMEOUT = 5,     /* device: a state-passing wait ran out of time */
+    SSD_ERR_DEVICE = 6       /* device: an internal pipeline wait gave up */
+} ssd_status_t;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype_t;
+
+/* Which kernel runs the problem. AUTO picks the tensor-core kernel where it
+ * has an instance (bf16/fp16 I/O, headdim 64, dstate 128, chunk 128 or 256)
+ * and the fp32 SIMT kernel otherwise. */
+typedef enum { SSD_KERNEL_AUTO = 0, SSD_KERNEL_SIMT = 1, SSD_KERNEL_TC = 2 } ssd_kernel_t;
+
+typedef struct {
+    int64_t batch;      /* >= 0                                              */
+    int64_t seqlen;     /* >= 0; any length, the last chunk may be ragged    */
+    int64_t nheads;     /* >= 1                                              */
+    int64_t headdim;    /* P                                                 */
+    int64_t dstate;     /* N                                                 */
+    int64_t ngroups;    /* G, divides nheads                                 */
+    int64_t chunk_size; /* Q: tokens per state-passing step                  */
+    int32_t io_dtype;   /* ssd_dtype_t of x, dt_raw, B, C, y                 */
+    int32_t state_dtype;/* SSD_F32 or SSD_F16: init/final and passed states  */
+    int32_t kernel;     /* ssd_kernel_t                                      */
+    int32_t reserved;   /* must be 0                                         */
+} ssd_problem_t;
+
+/* Bytes of workspace ssd_fwd needs for `prob` (written to *bytes). The
+ * workspace must be zero-filled once before its first use; after that each
+ * call leaves it ready for the next one (launches on one stream may reuse it
+ * back to back; concurrent launches need separate workspaces). */
+SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes);
+
+/* Launch the fused SSD prefill forward on `stream` (a cudaStream_t, NULL for
+ * the legacy default stream).
+ *  x, dt_raw, B, C, y   required, 16-byte aligned
+ *  dt_bias, A           required
+ *  D                    optional (NULL: no skip term)
+ *  init_states          optional (NULL: zero initial state)
+ *  final_states         optional (NULL: not written)
+ *  workspace            required, 256-byte aligned, >= ssd_fwd_workspace_size
+ * Returns SSD_OK once the launch is queued. */
+SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw,
+                             const float *dt_bias, const float *A, const void *B, const void *C,
+                             const float *D, const void *init_states, void *y, void *final_states,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read the device status recorded in `workspace` by the
+ * calls queued before, clear it, and return it (SSD_OK when none failed). */
+SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);
+
+/* Test hooks, written into the workspace header on `stream`:
+ *  timeout_ns     limit of every device-side wait (0 restores the 2 s default)
+ *  skip_publish   chunk index whose state publish is skipped, so that the next
+ *                 chunk's wait runs out (-1 disables). Host-armed fault
+ *                 injection: no memory fault, no trap, the kernel returns. */
+SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream);
+
+/* Which kernel ssd_fwd would run for `prob` (SSD_KERNEL_SIMT or _TC), or a
+ * negative ssd_status_t if the problem is rejected. */
+SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob);
+
+/* Static text for a status code. */
+SSD_API const char *ssd_status_string(ssd_status_t status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+SSD_API int ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SSD_H */

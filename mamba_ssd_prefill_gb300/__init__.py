@@ -1,0 +1,184 @@
+"""GB300-native Mamba-2 SSD chunked-scan prefill forward.
+
+A thin ctypes binding over the C ABI in ``include/ssd.h`` (``libmamba_ssd.so``,
+built in-tree by ``_build.py``). This module only marshals arguments: it
+checks tensor shapes and dtypes, allocates outputs and the workspace with
+PyTorch (device memory and streams are PyTorch's job here), and passes raw
+pointers. Every step of the computation runs in the library's CUDA kernels;
+there is no CPU path. If the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["ssd_fwd", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
+           "Workspace", "lib", "LIB_PATH", "STATUS"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
+
+_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+_KERNEL = {"auto": 0, "simt": 1, "tc": 2}
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
+          4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_DEVICE"}
+
+
+class SsdProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("io_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+                ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        text = _lib.ssd_status_string(status).decode() if _lib is not None else name
+        super().__init__(f"{what}: {name} ({text})" if what else f"{name} ({text})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """Load libmamba_ssd.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                                   f"g.build()'` (nvcc, sm_103a). There is no CPU fallback.")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, sz, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+            pp = ctypes.POINTER(SsdProblem)
+            L.ssd_fwd_workspace_size.argtypes = [pp, ctypes.POINTER(sz)]
+            L.ssd_fwd_workspace_size.restype = ctypes.c_int
+            L.ssd_fwd.argtypes = [pp] + [vp] * 10 + [vp, sz, vp]
+            L.ssd_fwd.restype = ctypes.c_int
+            L.ssd_fwd_check.argtypes = [vp, vp]
+            L.ssd_fwd_check.restype = ctypes.c_int
+            L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
+            L.ssd_debug_set.restype = ctypes.c_int
+            L.ssd_fwd_kernel_for.argtypes = [pp]
+            L.ssd_fwd_kernel_for.restype = ctypes.c_int
+            L.ssd_status_string.argtypes = [ctypes.c_int]
+            L.ssd_status_string.restype = ctypes.c_char_p
+            L.ssd_version.argtypes = []
+            L.ssd_version.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def make_problem(batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size, io_dtype=torch.bfloat16,
+                 state_dtype=torch.float32, kernel="auto") -> SsdProblem:
+    return SsdProblem(int(batch), int(seqlen), int(nheads), int(headdim), int(dstate), int(ngroups), int(chunk_size),
+                      _DT[io_dtype], _DT[state_dtype], _KERNEL[kernel], 0)
+
+
+def workspace_size(prob: SsdProblem) -> int:
+    n = ctypes.c_size_t(0)
+    st = lib().ssd_fwd_workspace_size(ctypes.byref(prob), ctypes.byref(n))
+    if st:
+        raise SsdError(st, "ssd_fwd_workspace_size")
+    return int(n.value)
+
+
+def kernel_for(prob: SsdProblem) -> str:
+    k = lib().ssd_fwd_kernel_for(ctypes.byref(prob))
+    if k < 0:
+        raise SsdError(-k, "ssd_fwd_kernel_for")
+    return {1: "simt", 2: "tc"}[k]
+
+
+class Workspace:
+    """A zero-initialised device workspace, grown on demand and reused across calls on one stream."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            # the library asks for a zero-filled workspace on first use only
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def ssd_fwd(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chunk_size=128, state_dtype=None, *, y=None,
+            final_states=None, return_final_states=True, workspace=None, kernel="auto", stream=None):
+    """Fused Mamba-2 SSD prefill forward on the GPU.
+
+    x [b, L, H, P], dt_raw [b, L, H], B/C [b, L, G, N] in one I/O dtype (fp32,
+    bf16 or fp16); dt_bias, A, D [H] fp32; init_states [b, H, P, N] in the
+    state dtype (fp32 or fp16). Returns (y [b, L, H, P], final_states or None).
+    """
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_fwd runs on CUDA tensors only (there is no CPU path)")
+    io = x.dtype
+    if state_dtype is None:
+        state_dtype = init_states.dtype if init_states is not None else torch.float32
+    for name, t, shape, dt in (("dt_raw", dt_raw, (b, L, H), io), ("B", B, (b, L, G, N), io), ("C", C, (b, L, G, N), io),
+                               ("dt_bias", dt_bias, (H,), torch.float32), ("A", A, (H,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dt} {shape} on {dev}, got {t.dtype} {tuple(t.shape)}")
+    if D is not None and (tuple(D.shape) != (H,) or D.dtype != torch.float32 or not D.is_contiguous()):
+        raise ValueError("D: expected contiguous fp32 [H]")
+    if init_states is not None and (tuple(init_states.shape) != (b, H, P, N) or init_states.dtype != state_dtype
+                                    or not init_states.is_contiguous()):
+        raise ValueError("init_states: expected contiguous [b, H, P, N] in the state dtype")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    prob = make_problem(b, L, H, P, N, G, chunk_size, io, state_dtype, kernel)
+    nbytes = workspace_size(prob)
+    if y is None:
+        y = torch.empty_like(x)
+    if final_states is None and return_final_states:
+        final_states = torch.empty(b, H, P, N, dtype=state_dtype, device=dev)
+    if workspace is None:
+        key = (dev.index, torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream)
+        workspace = _default_ws.setdefault(key, Workspace(dev))
+    ws = workspace.get(nbytes) if isinstance(workspace, Workspace) else workspace
+    st = lib().ssd_fwd(ctypes.byref(prob), _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                       _ptr(init_states), _ptr(y), _ptr(final_states), _ptr(ws), ws.numel() * ws.element_size(),
+                       _stream_ptr(stream, dev))
+    if st:
+        raise SsdError(st, "ssd_fwd")
+    return y, final_states
+
+
+def check(workspace, stream=None):
+    """Synchronise and raise SsdError if a device-side wait failed in an earlier call."""
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    if ws is None:
+        return
+    st = lib().ssd_fwd_check(_ptr(ws), _stream_ptr(stream, ws.device))
+    if st:
+        raise SsdError(st, "ssd_fwd_check")
+
+
+def debug_set(workspace, timeout_ns=0, skip_publish=-1, stream=None):
+    """Test hook: set the device wait limit and the chunk whose publish is skipped."""
+    ws = workspace.buf if isinstance(workspace, Workspace) else workspace
+    st = lib().ssd_debug_set(_ptr(ws), int(timeout_ns), int(skip_publish), _stream_ptr(stream, ws.device))
+    if st:
+        raise SsdError(st, "ssd_debug_set")

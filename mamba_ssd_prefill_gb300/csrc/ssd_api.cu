@@ -1,0 +1,228 @@
+// The C ABI declared in include/ssd.h: argument checks, workspace layout,
+// kernel selection and launch. Host code only.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "../../include/ssd.h"
+#include "ssd_internal.h"
+
+namespace {
+
+using ssd::Params;
+using ssd::WsHeader;
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];  // 0 = not queried yet (benign race: same value)
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) g_sm_count[dev] = n;
+    return n;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t elem_size(int dt) { return dt == SSD_F32 ? 4 : 2; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Plan {
+    int kernel = 0;          // SSD_KERNEL_SIMT / _TC
+    int64_t nc = 0;          // chunks per sequence
+    int heads_per_unit = 1;  // TC only
+    uint32_t total_units = 0;
+    size_t flags_off = 0, ring_off = 0, bytes = 0;
+};
+
+// Validate the problem and lay out the workspace. No CUDA calls except the
+// SM count used to size the tensor-core work units.
+ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
+    if (!pr || !out) return SSD_ERR_INVALID_ARG;
+    if (pr->reserved != 0) return SSD_ERR_INVALID_ARG;
+    if (pr->batch < 0 || pr->seqlen < 0 || pr->nheads < 1 || pr->headdim < 1 || pr->dstate < 1 ||
+        pr->ngroups < 1 || pr->chunk_size < 1)
+        return SSD_ERR_INVALID_ARG;
+    if (pr->nheads % pr->ngroups) return SSD_ERR_INVALID_ARG;
+    if (pr->io_dtype < SSD_F32 || pr->io_dtype > SSD_F16) return SSD_ERR_INVALID_ARG;
+    if (pr->state_dtype != SSD_F32 && pr->state_dtype != SSD_F16) return SSD_ERR_INVALID_ARG;
+    if (pr->kernel < SSD_KERNEL_AUTO || pr->kernel > SSD_KERNEL_TC) return SSD_ERR_INVALID_ARG;
+    // keep every element index comfortably inside int64
+    const double tok = (double)pr->batch * (double)pr->seqlen;
+    if (tok * (double)pr->nheads * (double)pr->headdim > 4e18 || tok * (double)pr->ngroups * (double)pr->dstate > 4e18 ||
+        (double)pr->batch * pr->nheads * pr->headdim * pr->dstate > 4e18)
+        return SSD_ERR_INVALID_ARG;
+
+    Plan pl;
+    pl.nc = (pr->seqlen + pr->chunk_size - 1) / pr->chunk_size;
+    const bool tc_ok = ssd::tc_supports(pr->headdim, pr->dstate, pr->chunk_size, pr->io_dtype);
+    const bool simt_ok = ssd::simt_smem_bytes(pr->headdim, pr->dstate) <= 227u * 1024u;
+    if (pr->kernel == SSD_KERNEL_TC) {
+        if (!tc_ok) return SSD_ERR_UNSUPPORTED;
+        pl.kernel = SSD_KERNEL_TC;
+    } else if (pr->kernel == SSD_KERNEL_SIMT) {
+        if (!simt_ok) return SSD_ERR_UNSUPPORTED;
+        pl.kernel = SSD_KERNEL_SIMT;
+    } else {
+        if (tc_ok)
+            pl.kernel = SSD_KERNEL_TC;
+        else if (simt_ok)
+            pl.kernel = SSD_KERNEL_SIMT;
+        else
+            return SSD_ERR_UNSUPPORTED;
+    }
+    const int64_t chains = pr->batch * pr->nheads;
+    double units;
+    if (pl.kernel == SSD_KERNEL_TC) {
+        pl.heads_per_unit = ssd::tc_heads_per_unit(pr->batch, pr->nheads, pr->ngroups, pl.nc, std::max(1, sm_count()));
+        units = (double)ssd::tc_total_units(pr->batch, pr->nheads, pr->ngroups, pl.nc, pl.heads_per_unit);
+    } else {
+        units = (double)chains * (double)pl.nc;
+    }
+    if (units >= 4.0e9) return SSD_ERR_UNSUPPORTED;
+    pl.total_units = (uint32_t)units;
+    pl.flags_off = sizeof(WsHeader);
+    pl.ring_off = align_up(pl.flags_off + sizeof(uint32_t) * (size_t)(chains * pl.nc), 256);
+    size_t ring;
+    if (pl.kernel == SSD_KERNEL_TC)
+        ring = ssd::tc_ring_bytes(chains, pr->headdim, pr->dstate, pr->state_dtype);
+    else
+        ring = (size_t)chains * 2 * (size_t)(pr->headdim * pr->dstate) * elem_size(pr->state_dtype);
+    pl.bytes = align_up(pl.ring_off + ring, 256);
+    *out = pl;
+    return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes) {
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    Plan pl;
+    const ssd_status_t st = plan(prob, &pl);
+    if (st != SSD_OK) return st;
+    *bytes = pl.bytes;
+    return SSD_OK;
+}
+
+SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob) {
+    Plan pl;
+    const ssd_status_t st = plan(prob, &pl);
+    return st == SSD_OK ? pl.kernel : -(int)st;
+}
+
+SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw, const float *dt_bias,
+                             const float *A, const void *B, const void *C, const float *D, const void *init_states,
+                             void *y, void *final_states, void *workspace, size_t workspace_bytes, void *stream) {
+    Plan pl;
+    ssd_status_t st = plan(prob, &pl);
+    if (st != SSD_OK) return st;
+    const ssd_problem_t &pr = *prob;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(pr.io_dtype);
+    const size_t ses = elem_size(pr.state_dtype);
+    const bool tokens = pr.batch > 0 && pr.seqlen > 0;
+    if (!dt_bias || !A) return SSD_ERR_INVALID_ARG;
+    if (!aligned(dt_bias, 4) || !aligned(A, 4) || (D && !aligned(D, 4))) return SSD_ERR_INVALID_ARG;
+    if (init_states && !aligned(init_states, 16)) return SSD_ERR_INVALID_ARG;
+    if (final_states && !aligned(final_states, 16)) return SSD_ERR_INVALID_ARG;
+    if (tokens) {
+        if (!x || !dt_raw || !B || !C || !y) return SSD_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) || !aligned(dt_raw, es))
+            return SSD_ERR_INVALID_ARG;
+    }
+    if (pr.batch == 0) return SSD_OK;
+    if (pr.seqlen == 0) {  // nothing to scan: the final state is the initial one
+        if (!final_states) return SSD_OK;
+        const size_t n = (size_t)(pr.batch * pr.nheads * pr.headdim * pr.dstate) * ses;
+        const cudaError_t e = init_states ? cudaMemcpyAsync(final_states, init_states, n, cudaMemcpyDeviceToDevice, s)
+                                          : cudaMemsetAsync(final_states, 0, n, s);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SSD_ERR_WORKSPACE;
+    const int sms = sm_count();
+    if (sms <= 0) return SSD_ERR_CUDA;
+
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.dt_raw = dt_raw;
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.D = D;
+    p.init = init_states;
+    p.y = y;
+    p.final_states = final_states;
+    char *ws = static_cast<char *>(workspace);
+    p.hdr = reinterpret_cast<WsHeader *>(ws);
+    p.flags = reinterpret_cast<uint32_t *>(ws + pl.flags_off);
+    p.ring = ws + pl.ring_off;
+    p.batch = pr.batch;
+    p.L = pr.seqlen;
+    p.H = pr.nheads;
+    p.P = pr.headdim;
+    p.N = pr.dstate;
+    p.G = pr.ngroups;
+    p.Q = pr.chunk_size;
+    p.nc = pl.nc;
+    p.heads_per_group = pr.nheads / pr.ngroups;
+    p.total_units = pl.total_units;
+
+    cudaError_t e;
+    if (pl.kernel == SSD_KERNEL_TC)
+        e = ssd::launch_tc(p, pr.io_dtype, pr.state_dtype, pl.heads_per_unit, sms, s);
+    else
+        e = ssd::launch_simt(p, pr.io_dtype, pr.state_dtype, sms, s);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream) {
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSD_ERR_CUDA;
+    uint32_t status = 0;
+    WsHeader *hdr = static_cast<WsHeader *>(workspace);
+    if (cudaMemcpy(&status, &hdr->status, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess) return SSD_ERR_CUDA;
+    if (status == 0) return SSD_OK;
+    if (cudaMemset(&hdr->status, 0, sizeof(status)) != cudaSuccess) return SSD_ERR_CUDA;
+    if (status == ssd::DEV_TIMEOUT) return SSD_ERR_TIMEOUT;
+    return SSD_ERR_DEVICE;
+}
+
+SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream) {
+    if (!workspace || !aligned(workspace, 256)) return SSD_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SSD_ERR_CUDA;
+    WsHeader *hdr = static_cast<WsHeader *>(workspace);
+    if (cudaMemcpy(&hdr->timeout_ns, &timeout_ns, sizeof(timeout_ns), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    const int64_t stored = skip_publish < 0 ? 0 : skip_publish + 1;  // 0 = off (zero-filled workspace)
+    if (cudaMemcpy(&hdr->skip_publish, &stored, sizeof(stored), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+SSD_API const char *ssd_status_string(ssd_status_t status) {
+    switch (status) {
+        case SSD_OK: return "ok";
+        case SSD_ERR_INVALID_ARG: return "invalid argument";
+        case SSD_ERR_UNSUPPORTED: return "unsupported problem (no kernel instance)";
+        case SSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case SSD_ERR_CUDA: return "CUDA runtime error";
+        case SSD_ERR_TIMEOUT: return "device wait timed out (state passing)";
+        case SSD_ERR_DEVICE: return "device pipeline error";
+    }
+    return "unknown status";
+}
+
+SSD_API int ssd_version(void) { return 10000; }
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+// Shared device-side definitions of the SSD prefill library: workspace header,
+// kernel parameters, scheduling and flag helpers, dtype conversion.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssd {
+
+// ---------------------------------------------------------------------------
+// Workspace. The header sits at offset 0; the per-chain flags and the state
+// ring follow at offsets the host computes (see ssd_api.cu).
+//
+// Epochs make the flags self-clearing: launch k (k = 1, 2, ...) reads
+// epoch = header.epoch + 1, tags every flag it publishes with that value and,
+// in the last CTA to finish, stores it back into header.epoch. A flag is
+// "set" for this launch only when it equals this launch's epoch.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    uint32_t epoch;       // epoch of the last finished launch
+    uint32_t ticket;      // persistent-grid work counter (reset by the last CTA)
+    uint32_t done;        // CTAs finished (reset by the last CTA)
+    uint32_t status;      // first device error of any launch since the last check
+    uint32_t abort;       // == epoch when this launch gave up: waiters bail out
+    uint32_t err_unit;    // unit (ticket) that recorded the error
+    uint32_t err_chunk;   // chunk index of that unit
+    uint32_t err_where;   // which wait gave up (WAIT_* below)
+    uint64_t timeout_ns;  // limit of every device wait, 0 = default
+    int64_t skip_publish; // test hook: 1 + chunk whose publish is skipped (0 = off, the zero-filled state)
+    uint32_t pad[52];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr uint32_t kMaxSpinIters = 1u << 26;           // hard cap besides the clock
+
+enum WaitSite : uint32_t {
+    WAIT_CHAIN = 1,   // state-passing flag of the previous chunk
+    WAIT_PIPE = 2,    // intra-CTA mbarrier (tensor-core kernel)
+};
+
+enum DevStatus : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_PIPE = 6 };
+
+// Parameters common to both kernels. Element strides are implied by the
+// packed layouts documented in ssd.h.
+struct Params {
+    const void *x;
+    const void *dt_raw;
+    const float *dt_bias;
+    const float *A;
+    const void *B;
+    const void *C;
+    const float *D;     // may be null
+    const void *init;   // may be null
+    void *y;
+    void *final_states; // may be null
+    WsHeader *hdr;
+    uint32_t *flags;    // [batch * nheads * nchunks]
+    void *ring;         // state ring, layout per kernel
+    int64_t batch, L, H, P, N, G, Q, nc;
+    int64_t heads_per_group;
+    uint32_t total_units;
+};
+
+// ---------------------------------------------------------------------------
+// Small PTX helpers (hand-written; no library code).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Record the first device error and raise this launch's abort flag.
+__device__ __forceinline__ void report_error(WsHeader *hdr, uint32_t epoch, uint32_t code, uint32_t unit,
+                                             uint32_t chunk, uint32_t where) {
+    if (atomicCAS(&hdr->status, 0u, code) == 0u) {
+        hdr->err_unit = unit;
+        hdr->err_chunk = chunk;
+        hdr->err_where = where;
+    }
+    __threadfence();
+    st_relaxed_gpu(&hdr->abort, epoch);
+}
+
+__device__ __forceinline__ bool aborted(const WsHeader *hdr, uint32_t epoch) {
+    return ld_relaxed_gpu(&hdr->abort) == epoch;
+}
+
+// Bounded wait until *flag == epoch (acquire). Returns false (after recording
+// a timeout) when the limit passes or another CTA aborted the launch.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch, WsHeader *hdr, uint64_t limit_ns,
+                                          uint32_t unit, uint32_t chunk) {
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t sleep_ns = 20;
+    for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
+        if (ld_acquire_gpu(flag) == epoch) return true;
+        if ((it & 7u) == 7u) {
+            if (aborted(hdr, epoch)) return false;
+            if (globaltimer() - t0 > limit_ns) break;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 200) sleep_ns += 20;
+    }
+    report_error(hdr, epoch, DEV_TIMEOUT, unit, chunk, WAIT_CHAIN);
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// Element conversion.
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// softplus(v) = log(1 + e^v); above 20 it equals v to fp32 precision.
+__device__ __forceinline__ float softplus_f32(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+
+}  // namespace ssd

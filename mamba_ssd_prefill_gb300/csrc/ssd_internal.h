@@ -1,0 +1,25 @@
+// Host-side interfaces between the C ABI (ssd_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+// fp32 SIMT kernel (ssd_simt.cu)
+size_t simt_smem_bytes(int64_t P, int64_t N);
+cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
+
+// tcgen05 / TMA kernel (ssd_tc.cu)
+bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype);
+size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype);
+uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int heads_per_unit);
+int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms);
+cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int heads_per_unit, int sms, cudaStream_t stream);
+
+}  // namespace ssd

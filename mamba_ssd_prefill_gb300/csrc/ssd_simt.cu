@@ -1,0 +1,208 @@
+// fp32 SIMT kernel of the fused SSD prefill forward.
+//
+// Used for fp32 I/O (where tensor-core TF32 would not hold the fp32 accuracy
+// bound) and for shapes the tensor-core kernel has no instance for. One work
+// unit is (chunk c, batch b, head h); units are handed out by an atomic ticket
+// in chunk-major order, so a unit only ever waits on a lower ticket that a
+// running CTA already holds (deadlock-free without co-residency).
+//
+// Per unit: wait for the state entering chunk c (flag of chunk c-1, epoch
+// tagged), then walk the chunk in 32-token sub-chunks with the running state
+// in shared memory, doing the five SSD steps of "Accelerating Mamba2 with
+// Kernel Fusion" (chunk cumsum, BMM, chunk state, state passing, chunk scan)
+// at sub-chunk granularity, then publish the state leaving chunk c.
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSub = 32;  // tokens per sub-chunk (one warp-wide cumsum)
+
+template <typename IO, typename ST>
+__global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
+    extern __shared__ float4 smem_f4[];
+    float *smem = reinterpret_cast<float *>(smem_f4);
+    const int P = (int)p.P, N = (int)p.N, NB = N + 1;  // padded B/C rows avoid bank conflicts
+    float *S = smem;              // [N][P] running state
+    float *xs = S + N * P;        // [kSub][P]
+    float *Bs = xs + kSub * P;    // [kSub][N+1]
+    float *Cs = Bs + kSub * NB;   // [kSub][N+1]
+    float *Pm = Cs + kSub * NB;   // [kSub][kSub] masked, decayed C.B^T * dt
+    float *cs = Pm + kSub * kSub; // [kSub] inclusive cumsum of dt*A
+    float *dts = cs + kSub;       // [kSub] dt
+    float *wj = dts + kSub;       // [kSub] exp(cs_last - cs_j) * dt_j
+    float *ecs = wj + kSub;       // [kSub] exp(cs_i)
+    __shared__ uint32_t s_ticket;
+    __shared__ int s_ok;
+
+    const int tid = threadIdx.x;
+    WsHeader *hdr = p.hdr;
+    const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
+    const uint64_t limit = hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs;
+    const int64_t skip = hdr->skip_publish - 1;  // -1: no chunk skipped
+    const int64_t BH = p.batch * p.H;
+    const IO *x = static_cast<const IO *>(p.x);
+    const IO *dtr = static_cast<const IO *>(p.dt_raw);
+    const IO *Bg = static_cast<const IO *>(p.B);
+    const IO *Cg = static_cast<const IO *>(p.C);
+    IO *y = static_cast<IO *>(p.y);
+    const ST *init = static_cast<const ST *>(p.init);
+    ST *fin = static_cast<ST *>(p.final_states);
+    ST *ring = static_cast<ST *>(p.ring);
+
+    for (;;) {
+        if (tid == 0) s_ticket = atomicAdd(&hdr->ticket, 1u);
+        __syncthreads();
+        const uint32_t t = s_ticket;
+        __syncthreads();
+        if (t >= p.total_units) break;
+        const int64_t c = t / BH, rem = t % BH, b = rem / p.H, h = rem % p.H;
+        const int64_t g = h / p.heads_per_group;
+        const int64_t chain = b * p.H + h;
+        const float Ah = p.A[h], bias = p.dt_bias[h], Dh = p.D ? p.D[h] : 0.f;
+
+        // ---- state entering chunk c
+        if (tid == 0) s_ok = aborted(hdr, epoch) ? 0 : (c == 0 ? 1 : (int)wait_flag(&p.flags[chain * p.nc + c - 1],
+                                                                                   epoch, hdr, limit, t, (uint32_t)c));
+        __syncthreads();
+        if (!s_ok) continue;  // launch aborted: drain the remaining tickets
+        if (c == 0) {
+            for (int e = tid; e < N * P; e += kThreads) {
+                const int n = e / P, q = e % P;
+                S[e] = init ? to_f32(init[(chain * P + q) * N + n]) : 0.f;
+            }
+        } else {
+            const ST *slot = ring + (chain * 2 + (c & 1)) * (int64_t)(N * P);
+            for (int e = tid; e < N * P; e += kThreads) S[e] = to_f32(__ldcg(slot + e));
+        }
+        __syncthreads();
+
+        const int64_t c0 = c * p.Q, c1 = (c0 + p.Q < p.L) ? c0 + p.Q : p.L;
+        for (int64_t s0 = c0; s0 < c1; s0 += kSub) {
+            const int T = (int)((c1 - s0) < kSub ? (c1 - s0) : kSub);
+            // step 1: dt = softplus(dt_raw + bias), inclusive cumsum of dt*A (rows >= T: dt = 0)
+            if (tid < 32) {
+                float dtv = 0.f;
+                if (tid < T) dtv = softplus_f32(to_f32(dtr[(b * p.L + s0 + tid) * p.H + h]) + bias);
+                float sc = dtv * Ah;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, sc, o);
+                    if (tid >= o) sc += u;
+                }
+                const float last = __shfl_sync(0xffffffffu, sc, 31);
+                cs[tid] = sc;
+                dts[tid] = dtv;
+                wj[tid] = expf(last - sc) * dtv;
+                ecs[tid] = expf(sc);
+            }
+            for (int e = tid; e < kSub * P; e += kThreads) {
+                const int r = e / P, q = e % P;
+                xs[e] = r < T ? to_f32(x[((b * p.L + s0 + r) * p.H + h) * P + q]) : 0.f;
+            }
+            for (int e = tid; e < kSub * N; e += kThreads) {
+                const int r = e / N, q = e % N;
+                const int64_t off = ((b * p.L + s0 + r) * p.G + g) * N + q;
+                Bs[r * NB + q] = r < T ? to_f32(Bg[off]) : 0.f;
+                Cs[r * NB + q] = r < T ? to_f32(Cg[off]) : 0.f;
+            }
+            __syncthreads();
+            // step 2 (BMM) with the segsum decay mask: Pm[i][j] = (C_i.B_j) exp(cs_i - cs_j) dt_j, j <= i
+            for (int e = tid; e < kSub * kSub; e += kThreads) {
+                const int i = e / kSub, j = e % kSub;
+                float v = 0.f;
+                if (j <= i) {
+                    float d = 0.f;
+                    for (int n = 0; n < N; ++n) d = fmaf(Cs[i * NB + n], Bs[j * NB + n], d);
+                    v = d * expf(cs[i] - cs[j]) * dts[j];
+                }
+                Pm[e] = v;
+            }
+            __syncthreads();
+            // step 5 (chunk scan): y_i = sum_j Pm_ij x_j + exp(cs_i) C_i . S + D x_i
+            for (int e = tid; e < T * P; e += kThreads) {
+                const int i = e / P, q = e % P;
+                float a1 = 0.f, a2 = 0.f;
+                for (int j = 0; j <= i; ++j) a1 = fmaf(Pm[i * kSub + j], xs[j * P + q], a1);
+                for (int n = 0; n < N; ++n) a2 = fmaf(Cs[i * NB + n], S[n * P + q], a2);
+                const float v = a1 + ecs[i] * a2 + Dh * xs[i * P + q];
+                y[((b * p.L + s0 + i) * p.H + h) * P + q] = from_f32<IO>(v);
+            }
+            __syncthreads();
+            // steps 3 + 4 (chunk state, state passing): S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
+            const float decay = ecs[kSub - 1];
+            for (int e = tid; e < N * P; e += kThreads) {
+                const int n = e / P, q = e % P;
+                float acc = 0.f;
+                for (int j = 0; j < T; ++j) acc = fmaf(wj[j] * xs[j * P + q], Bs[j * NB + n], acc);
+                S[e] = fmaf(decay, S[e], acc);
+            }
+            __syncthreads();
+        }
+
+        // ---- publish the state leaving chunk c
+        if (c == p.nc - 1) {
+            if (fin)
+                for (int e = tid; e < N * P; e += kThreads) {
+                    const int q = e / N, n = e % N;
+                    fin[(chain * P + q) * N + n] = from_f32<ST>(S[n * P + q]);
+                }
+        } else if (c != skip) {
+            ST *slot = ring + (chain * 2 + ((c + 1) & 1)) * (int64_t)(N * P);
+            for (int e = tid; e < N * P; e += kThreads) __stcg(slot + e, from_f32<ST>(S[e]));
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release_gpu(&p.flags[chain * p.nc + c], epoch);
+        }
+        __syncthreads();
+    }
+
+    // ---- launch bookkeeping: the last CTA resets the counters and commits the epoch
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t d = atomicAdd(&hdr->done, 1u);
+        if (d == gridDim.x - 1) {
+            hdr->ticket = 0;
+            hdr->done = 0;
+            __threadfence();
+            st_relaxed_gpu(&hdr->epoch, epoch);
+        }
+    }
+}
+
+template <typename IO, typename ST>
+cudaError_t launch_t(const Params &p, int sms, cudaStream_t stream) {
+    const size_t smem = simt_smem_bytes(p.P, p.N);
+    auto k = simt_kernel<IO, ST>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const int64_t grid = std::min<int64_t>((int64_t)p.total_units, (int64_t)sms * per_sm);
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_smem_bytes(int64_t P, int64_t N) {
+    return sizeof(float) * (size_t)(N * P + kSub * P + 2 * kSub * (N + 1) + kSub * kSub + 4 * kSub);
+}
+
+cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream) {
+    if (state_dtype == 0) {
+        if (io_dtype == 0) return launch_t<float, float>(p, sms, stream);
+        if (io_dtype == 1) return launch_t<__nv_bfloat16, float>(p, sms, stream);
+        return launch_t<__half, float>(p, sms, stream);
+    }
+    if (io_dtype == 0) return launch_t<float, __half>(p, sms, stream);
+    if (io_dtype == 1) return launch_t<__nv_bfloat16, __half>(p, sms, stream);
+    return launch_t<__half, __half>(p, sms, stream);
+}
+
+}  // namespace ssd

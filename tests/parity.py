@@ -1,0 +1,57 @@
+"""Parity gates between the CUDA path and the CPU oracle.
+
+Tolerances (the bars the GPU path is held to):
+  fp32 I/O:       max |y - y_ref| <= 1e-3 * RMS(y_ref)           (and the same for final states)
+  bf16/fp16 I/O:  |y - y_ref| <= 1e-2 + r * |y_ref| element-wise, r = 2^-8 (bf16) or 2^-10 (fp16):
+                  absolute 1e-2 on the value, plus one rounding of the stored output to its
+                  16-bit type (a bf16 y of magnitude 16 cannot be within 1e-2 of anything).
+  final states:   the same rule with r for the state dtype (0 for fp32 states) on top of the
+                  I/O rounding term.
+The match percentages at tolerance 0 / 1e-3 / 1e-2 are reported beside the gate,
+in the format of the fused-kernel page's precision table.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+REL = {"f32": 0.0, "bf16": 2.0 ** -8, "f16": 2.0 ** -10}
+
+
+def stats(got, ref):
+    d = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    return {
+        "max_abs": float(d.max()) if d.size else 0.0,
+        "rms_ref": rms,
+        "max_over_rms": float(d.max() / rms) if d.size and rms > 0 else 0.0,
+        "match_0": float(np.mean(d == 0)) if d.size else 1.0,
+        "match_1e-3": float(np.mean(d <= 1e-3)) if d.size else 1.0,
+        "match_1e-2": float(np.mean(d <= 1e-2)) if d.size else 1.0,
+    }
+
+
+def gate_y(got, ref, io: str):
+    """Return (ok, stats) for the output y."""
+    s = stats(got, ref)
+    if got.size == 0:
+        return True, s
+    if io == "f32":
+        ok = s["max_abs"] <= 1e-3 * s["rms_ref"]
+    else:
+        bound = 1e-2 + REL[io] * np.abs(ref)
+        excess = np.abs(got - ref) - bound
+        s["worst_margin"] = float(excess.max())
+        ok = bool(np.all(excess <= 0))
+    return ok, s
+
+
+def gate_final(got, ref, io: str, state: str):
+    s = stats(got, ref)
+    if got.size == 0:
+        return True, s
+    if io == "f32" and state == "f32":
+        ok = s["max_abs"] <= 1e-3 * max(s["rms_ref"], 1e-30)
+    else:
+        bound = 1e-2 + (REL[state] + REL[io]) * np.abs(ref)
+        ok = bool(np.all(np.abs(got - ref) <= bound))
+    return ok, s

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/ssd.h declares, and rejects bad problems before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import mamba_ssd_prefill_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"SSD_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(m.LIB_PATH):
+        from mamba_ssd_prefill_gb300 import _build
+
+        _build.build()
+    return m.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "ssd_fwd" in names and "ssd_fwd_workspace_size" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssd_version() >= 10000
+    for code in range(7):
+        assert lib.ssd_status_string(code)
+
+
+def prob(**kw):
+    d = dict(batch=1, seqlen=1024, nheads=8, headdim=64, dstate=128, ngroups=1, chunk_size=128,
+             io_dtype=torch.bfloat16, state_dtype=torch.float32, kernel="auto")
+    d.update(kw)
+    return m.make_problem(**d)
+
+
+@pytest.mark.parametrize("bad", [dict(nheads=6, ngroups=4), dict(nheads=0), dict(chunk_size=0), dict(seqlen=-1),
+                                 dict(headdim=0), dict(dstate=0)])
+def test_rejects_bad_problem(lib, bad):
+    with pytest.raises(m.SsdError) as e:
+        m.workspace_size(prob(**bad))
+    assert e.value.status == 1
+
+
+def test_rejects_bad_enums(lib):
+    p = prob()
+    p.io_dtype = 7
+    n = ctypes.c_size_t()
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 1
+    p = prob()
+    p.state_dtype = 1  # bf16 states are not offered
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 1
+    p = prob()
+    p.reserved = 3
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 1
+
+
+def test_workspace_size_scales_with_chains(lib):
+    a = m.workspace_size(prob(batch=1))
+    b = m.workspace_size(prob(batch=4))
+    assert b > a > 256
+    assert a % 256 == 0
+
+
+def test_kernel_selection(lib):
+    assert m.kernel_for(prob(io_dtype=torch.float32, dstate=64)) == "simt"
+    assert m.kernel_for(prob(kernel="simt")) == "simt"
+    # shapes the SIMT kernel cannot hold in shared memory are rejected
+    with pytest.raises(m.SsdError) as e:
+        m.kernel_for(prob(headdim=1024, dstate=1024, kernel="simt"))
+    assert e.value.status == 2
+
+
+def test_null_pointers_rejected_before_any_cuda_call(lib):
+    p = prob(seqlen=64)
+    vp = ctypes.c_void_p
+    st = lib.ssd_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None, None, None, None, 0, None)
+    assert st == 1
+    # misaligned x
+    st = lib.ssd_fwd(ctypes.byref(p), vp(8), vp(256), vp(256), vp(256), vp(256), vp(256), None, None, vp(256), None,
+                     vp(256), 1 << 30, None)
+    assert st == 1
+
+
+def test_workspace_rejected_when_small(lib):
+    p = prob(seqlen=64)
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)
+    st = lib.ssd_fwd(ctypes.byref(p), a, a, a, a, a, a, None, None, a, None, a, 16, None)
+    assert st == 3
+    st = lib.ssd_fwd(ctypes.byref(p), a, a, a, a, a, a, None, None, a, None, vp((1 << 20) + 16), 1 << 30, None)
+    assert st == 3
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    x = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        m.ssd_fwd(x, torch.zeros(1, 4, 2, dtype=torch.bfloat16), torch.zeros(2), torch.zeros(2),
+                  torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16), torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16))
