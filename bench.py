@@ -1,0 +1,349 @@
+"""Benchmark of the fused SSD prefill forward: one JSON line on stdout.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one call of the whole fused path (chunk cumsum, BMM, chunk state,
+state passing, chunk scan) over one batch of synthetic inputs. The default
+workload is the Mamba-2 130M-shaped layer (batch 4, seqlen 4096, 24 heads,
+headdim 64, d_state 128, chunk 128, bf16 I/O, fp32 states, init ~ N(0, 0.1)).
+Its 116 MB of inputs and outputs fit in L2, so a 512 MiB buffer is written
+before every step, outside the timed events.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the (batch, head) chains need no exchange); the time is the
+maximum over ranks and the value counts all ranks' tokens.
+
+--impl reference times the CPU oracle (fp64 token-by-token recurrence) on the
+host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "SSD prefill tokens/s per layer at 1 GB300; % of roofline (HBM vs tensor)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "m130-bf16"
+FLUSH_BYTES = 512 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic(w):
+    """Algorithmic bytes and causal MMA flops of one call (on-chip intermediates not counted)."""
+    T = w.batch * w.seqlen
+    e = 4 if w.io == "f32" else 2
+    es = 4 if w.state == "f32" else 2
+    states = w.batch * w.nheads * w.headdim * w.dstate * es
+    nbytes = T * e * (2 * w.nheads * w.headdim + w.nheads + 2 * w.ngroups * w.dstate)
+    nbytes += states * (2 if w.init != "none" else 1)  # init read (when given) + final write
+    q1 = (w.chunk + 1) / 2.0
+    macs = T * (w.ngroups * w.dstate * q1 + w.nheads * w.headdim * q1 + 2 * w.nheads * w.dstate * w.headdim)
+    return nbytes, 2.0 * macs
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("ssd_tc.cu", "sm100_ptx.cuh", "ssd_common.cuh"):
+        h.update(open(os.path.join(ROOT, "mamba_ssd_prefill_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples taken while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 6:
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, inp_cpu, budget_s, min_reps=1):
+    """Time the oracle on whole chains of the workload for about budget_s; returns (tokens/s, sample text, threads)."""
+    import oracle
+
+    b, L, H, P = inp_cpu["x"].shape
+    per = H // w.ngroups
+    # gather chains once (float64), outside the timed region
+    rng = np.random.default_rng(0)
+    order = [(bi, h) for bi in range(b) for h in range(H)]
+    rng.shuffle(order)
+    threads = oracle.default_threads()
+    # size the sample: start with one chain per thread and grow
+    n = min(len(order), threads)
+    chains = order[:n]
+
+    def gather(ch):
+        x = np.stack([inp_cpu["x"][bi, :, h].double().numpy() for bi, h in ch])
+        dtr = np.stack([inp_cpu["dt_raw"][bi, :, h].double().numpy() for bi, h in ch])
+        B = np.stack([inp_cpu["B"][bi, :, h // per].double().numpy() for bi, h in ch])
+        C = np.stack([inp_cpu["C"][bi, :, h // per].double().numpy() for bi, h in ch])
+        hs = np.array([h for _, h in ch])
+        init = None
+        if inp_cpu["init_states"] is not None:
+            init = np.stack([inp_cpu["init_states"][bi, h].double().numpy() for bi, h in ch])
+        return (x, dtr, inp_cpu["dt_bias"].double().numpy()[hs], inp_cpu["A"].double().numpy()[hs], B, C,
+                inp_cpu["D"].double().numpy()[hs], init)
+
+    args = gather(chains)
+    t0 = time.perf_counter()
+    oracle.ssd_chains(*args, nthreads=threads)
+    dt1 = time.perf_counter() - t0
+    reps = max(min_reps, int(budget_s / max(dt1, 1e-3)))
+    reps = min(reps, 50)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.ssd_chains(*args, nthreads=threads)
+    el = time.perf_counter() - t0
+    chain_tokens = reps * len(chains) * L
+    tok_s = chain_tokens / H / el  # a token is one position across all heads
+    sample = (f"{len(chains)} of {b * H} (batch, head) chains x {L} tokens, {reps} repetitions, "
+              f"{el:.1f} s; tokens/s = chain-tokens / nheads / seconds")
+    return tok_s, sample, threads
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    inp = make_inputs(w, device="cpu")
+    cfg = workload_config(w)
+    per_step = []
+    budget = min(args.ref_budget, 150.0 / (args.warmup + args.steps))  # whole run within a few minutes
+    for s in range(args.warmup + args.steps):
+        tok_s, sample, threads = oracle_sample(w, inp, budget_s=budget)
+        if s >= args.warmup:
+            per_step.append(tok_s)
+    v = float(np.median(per_step))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": w.tokens / v * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+            "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk, "io": w.io, "state": w.state,
+            "init_states": w.init, "parallelism": "replicas"}
+
+
+def run_gpu(args, w):
+    import mamba_ssd_prefill_gb300 as m
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st = DTYPES[w.state]
+    inp = make_inputs(w, device=dev, seed=w.seed + rank)
+    prob = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io], st)
+    kernel = m.kernel_for(prob)
+    ws = m.Workspace(dev)
+    y = torch.empty_like(inp["x"])
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=st, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=st, workspace=ws, y=y, final_states=fin)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    m.check(ws)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush, outside the events
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    m.check(ws)
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(float(np.mean(times)), world)
+    value = world * w.tokens / (ms * 1e-3)
+
+    # end to end through the public API with host buffers: pinned H2D of the inputs, the call, D2H of y + final
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in inp.items()}
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    f_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        m.ssd_fwd(**dev_in, chunk_size=w.chunk, state_dtype=st, workspace=ws, y=y, final_states=fin)
+        y_host.copy_(y, non_blocking=True)
+        f_host.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    m.check(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    if rank != 0:
+        return
+    hbm, tflops, kind = peaks()
+    nbytes, flops = algorithmic(w)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    t_mem, t_tc = nbytes / (hbm * 1e9), flops / (tflops * 1e12)
+    bound = "hbm" if t_mem >= t_tc else "tensor"
+    roof = {"bound": bound, "achieved": achieved if bound == "hbm" else flops / (ms * 1e-3) / 1e12,
+            "peak": hbm if bound == "hbm" else tflops, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "traffic": traffic_for(w.name), "peak_kind": kind,
+            "roofline_time_us": max(t_mem, t_tc) * 1e6, "algorithmic_bytes": nbytes, "causal_flops": flops}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    cfg = workload_config(w)
+    cfg.update({"kernel": kernel, "l2": f"{FLUSH_BYTES >> 20} MiB buffer written before every step, outside the events",
+                "wall_s_timed_region": round(wall, 3)})
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg, "roofline": roof,
+            "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "clocks": clk.summary()}
+    if world == 1 and not args.no_cpu_baseline:
+        tok_s, sample, threads = oracle_sample(w, {k: (v.cpu() if v is not None else None) for k, v in inp.items()},
+                                               budget_s=args.ref_budget)
+        line["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

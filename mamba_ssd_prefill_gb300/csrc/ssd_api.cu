@@ -2,6 +2,7 @@
 // kernel selection and launch. Host code only.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -81,6 +82,11 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     double units;
     if (pl.kernel == SSD_KERNEL_TC) {
         pl.heads_per_unit = ssd::tc_heads_per_unit(pr->batch, pr->nheads, pr->ngroups, pl.nc, std::max(1, sm_count()));
+        // test knob: force the heads per work unit (must divide nheads / ngroups, at most 8)
+        if (const char *env = getenv("SSD_TC_HEADS_PER_UNIT")) {
+            const int hs = atoi(env);
+            if (hs >= 1 && hs <= 8 && (pr->nheads / pr->ngroups) % hs == 0) pl.heads_per_unit = hs;
+        }
         units = (double)ssd::tc_total_units(pr->batch, pr->nheads, pr->ngroups, pl.nc, pl.heads_per_unit);
     } else {
         units = (double)chains * (double)pl.nc;

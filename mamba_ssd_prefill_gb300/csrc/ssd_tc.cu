@@ -1,13 +1,759 @@
-// tcgen05 / TMA tensor-core kernel of the fused SSD prefill forward (bf16/fp16 I/O).
+// Tensor-core (tcgen05 / TMEM / TMA) kernel of the fused SSD prefill forward,
+// bf16 or fp16 I/O, headdim P = 64, d_state N = 128, chunk Q = 128.
+//
+// One persistent CTA per SM pulls work units (chunk c, batch b, group g, slice
+// of `hs` heads of that group) from an atomic ticket in chunk-major order and
+// runs the five SSD steps of "Accelerating Mamba2 with Kernel Fusion" (chunk
+// cumsum, BMM, chunk state, state passing, chunk scan) for them:
+//
+//   CB      = C_c B_c^T                       (tcgen05, once per unit, TMEM)
+//   P       = CB o exp(segsum(dt*A)) o dt_j   (+ D on the diagonal; fp16 in TMEM)
+//   y_intra = P x_c                           (tcgen05, A operand from TMEM)
+//   s_c     = B_c^T (exp(cs_last - cs_j) dt_j x_j)   (decay applied to x, the
+//                                             inner dimension of the contraction)
+//   S_c+1   = exp(cs_last) S_c + s_c          (flag-ordered chain across CTAs)
+//   y       = y_intra + exp(cs_i) C_c S_c     (tcgen05 C.S, fused epilogue)
+//
+// Warp roles (320 threads):
+//   warp 0      scheduler + TMA producer (tickets, dt_raw, B/C and x tiles)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 2-5   "math": bf16->fp16 tile conversion, cumsum tables, decay mask
+//               P -> TMEM, X_s, epilogue y = y_intra + exp(cs) y_inter
+//   warps 6-9   "chain": state passing (wait flag, S_in, S_out, publish), S_in
+//               -> shared memory as the C.S operand, final states
+// All MMA operands are fp16 (bf16 inputs are converted on chip; the contractions
+// with P, X_s and S need fp16's 11-bit significand to hold 1e-2).
+//
+// TMEM (512 columns): CB [0,128), P / y_inter x2 [128,256), y_intra x2
+// [256,384), chunk state s x2 [384,512).
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "sm100_ptx.cuh"
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
+namespace {
 
-bool tc_supports(int64_t, int64_t, int64_t, int) { return false; }
-size_t tc_ring_bytes(int64_t, int64_t, int64_t, int) { return 0; }
-uint32_t tc_total_units(int64_t, int64_t, int64_t, int64_t, int) { return 0; }
-int tc_heads_per_unit(int64_t, int64_t, int64_t, int64_t, int) { return 1; }
-cudaError_t launch_tc(Params, int, int, int, int, cudaStream_t) { return cudaErrorNotSupported; }
+using namespace sm100;
+
+constexpr int kQ = 128;
+constexpr int kP = 64;
+constexpr int kN = 128;
+constexpr int kMaxHs = 8;
+constexpr int kThreads = 320;
+constexpr uint32_t kTile = 16384;  // [128 rows x 128 B] 128B-swizzled 16-bit tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kColCB = 0, kColP = 128, kColYI = 256, kColS = 384;
+constexpr uint32_t kBarMath = 1, kBarChain = 2;  // named barriers (0 is __syncthreads)
+
+struct Sched {
+    int32_t valid, b, c, g, h0, rows;
+};
+
+struct __align__(1024) Smem {
+    uint8_t bc[2][4][kTile];   // per unit stage: B n[0,64), B n[64,128), C n[0,64), C n[64,128)
+    uint8_t x[2][kTile];       // per head buffer: x tile (fp16 after conversion)
+    uint8_t xs[2][kTile];      // per head buffer: X_s, then S_in (fp16, C.S operand)
+    float cs2[2][kMaxHs][kQ];  // raw dt_raw from the producer, then log2(e) * cumsum(dt*A)
+    float dt[2][kMaxHs][kQ];   // dt
+    float wt[2][kMaxHs][kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
+    float wsum[4][kMaxHs];     // per-warp scan totals
+    Sched sched[2];
+    uint64_t bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty;
+    uint64_t x_full[2], x_empty[2], p_full[2], mma1[2], s_free[2], sin_full[2], mma2[2], drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+__device__ __forceinline__ float ex2(float v) {
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+__device__ __forceinline__ void sts128(void *p, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <typename IO> __device__ __forceinline__ uint32_t pack_io(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack_io<__half>(float lo, float hi) { return pack_f16(lo, hi); }
+template <> __device__ __forceinline__ uint32_t pack_io<__nv_bfloat16>(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <typename IO> __device__ __forceinline__ float2 unpack_io(uint32_t v);
+template <> __device__ __forceinline__ float2 unpack_io<__half>(uint32_t v) {
+    return __half22float2(*reinterpret_cast<__half2 *>(&v));
+}
+template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&v));
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
+
+// Bounded wait on an intra-CTA mbarrier phase. On timeout (a broken pipeline)
+// it records the error, raises the CTA abort flag and returns false; every
+// other wait then gives up too and the CTA drains to its teardown. Its limit
+// is four times the state-passing limit plus 100 ms: a pipeline stage may
+// legitimately sit behind one full state-passing wait, which must time out
+// (and report itself) first.
+__device__ __noinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
+    for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) return false;
+            if (globaltimer() - t0 > limit) break;
+        }
+    }
+    *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
+    report_error(hdr, epoch, DEV_PIPE, 0, 0, WAIT_PIPE);
+    return false;
+}
+
+template <typename IO, typename ST>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
+              const __grid_constant__ CUtensorMap map_c, const int hs) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    WsHeader *hdr = p.hdr;
+    const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
+    constexpr bool kBf16 = sizeof(IO) == 2 && !std::is_same<IO, __half>::value;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.bc_full[i], 1);
+            mbar_init(&sm.bc_conv[i], 1);
+            mbar_init(&sm.bc_empty[i], 1);
+            mbar_init(&sm.x_full[i], 1);
+            mbar_init(&sm.x_empty[i], 1);
+            mbar_init(&sm.p_full[i], 1);
+            mbar_init(&sm.mma1[i], 1);
+            mbar_init(&sm.s_free[i], 1);
+            mbar_init(&sm.sin_full[i], 1);
+            mbar_init(&sm.mma2[i], 1);
+        }
+        mbar_init(&sm.cb_full, 1);
+        mbar_init(&sm.cb_empty, 1);
+        mbar_init(&sm.drain, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int64_t slices = p.heads_per_group / hs;
+    const int64_t per_chunk = p.batch * p.G * slices;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&map_x);
+            prefetch_tensormap(&map_b);
+            prefetch_tensormap(&map_c);
+        }
+        const IO *dtr = static_cast<const IO *>(p.dt_raw);
+        uint32_t hc = 0;
+        int armed_bc = -1, armed_x = 0;  // for the drain at teardown
+        uint32_t bc_par[2] = {0, 0}, x_par[2] = {0, 0};
+        bool ok = true;
+        for (uint32_t v = 0; ok; ++v) {
+            const uint32_t u = v & 1, nn = v >> 1;
+            uint32_t t = 0;
+            if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
+            if (t >= p.total_units) {
+                if (lane == 0) {
+                    sm.sched[u].valid = 0;
+                    mbar_arrive(&sm.bc_full[u]);
+                }
+                break;
+            }
+            const int64_t c = t / per_chunk;
+            int64_t r = t % per_chunk;
+            const int64_t b = r / (p.G * slices);
+            r %= p.G * slices;
+            const int64_t g = r / slices;
+            const int64_t h0 = g * p.heads_per_group + (r % slices) * hs;
+            const int64_t row0 = c * kQ;
+            const int rows = (int)((p.L - row0) < kQ ? (p.L - row0) : kQ);
+            for (int e = lane; e < hs * kQ; e += 32) {
+                const int i = e / hs, hh = e % hs;
+                float raw = -INFINITY;  // rows past the sequence end: dt = softplus(-inf) = 0
+                if (i < rows) raw = to_f32(dtr[(b * p.L + row0 + i) * p.H + h0 + hh]);
+                sm.cs2[u][hh][i] = raw;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                sm.sched[u] = Sched{1, (int32_t)b, (int32_t)c, (int32_t)g, (int32_t)h0, rows};
+                mbar_arrive_expect_tx(&sm.bc_full[u], 4 * kTile);
+                tma_load_4d(sm.bc[u][0], &map_b, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
+                tma_load_4d(sm.bc[u][1], &map_b, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
+                tma_load_4d(sm.bc[u][2], &map_c, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
+                tma_load_4d(sm.bc[u][3], &map_c, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
+                armed_bc = (int)u;
+                bc_par[u] = nn & 1;
+                for (int hh = 0; hh < hs; ++hh, ++hc) {
+                    const uint32_t k = hc & 1, n = hc >> 1;
+                    if (!bwait(&sm.x_empty[k], (n & 1) ^ 1, sm, hdr, epoch)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.x_full[k], kTile);
+                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, (int)(h0 + hh), (int)row0, (int)b);
+                    armed_x |= 1 << k;
+                    x_par[k] = n & 1;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            hc = __shfl_sync(0xffffffffu, hc, 0);
+        }
+        // teardown: make sure no TMA write into this CTA's shared memory is still in flight
+        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
+            for (int u = 0; u < 2; ++u)
+                if (armed_bc >= 0) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(&sm.bc_full[u], bc_par[u]) && globaltimer() - t0 < 100000000ull) {
+                    }
+                }
+            for (int k = 0; k < 2; ++k)
+                if (armed_x & (1 << k)) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
+                    }
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idCB = idesc_f16_f32(128, 128, false, false);
+            constexpr uint32_t idPX = idesc_f16_f32(128, 64, false, true);
+            constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true);
+            constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
+            uint32_t hc = 0;
+            bool pend = false;
+            uint32_t pk = 0, pn = 0, pu = 0;
+            bool plast = false;
+            bool ok = true;
+            auto issue_cs = [&](uint32_t k, uint32_t n, uint32_t u, bool last) -> bool {
+                if (!bwait(&sm.sin_full[k], n & 1, sm, hdr, epoch)) return false;
+                tc_fence_after();
+                const uint32_t ca = smem_u32(sm.bc[u][2]), sa = smem_u32(sm.xs[k]);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
+                    mma_ss(tmem + kColP + 64 * k, desc_sw128(ca + off, 16, 1024),
+                           desc_sw128(sa + 2048 * s, 8192, 1024), idCS, s > 0);
+                }
+                mma_commit(&sm.mma2[k]);
+                if (last) mma_commit(&sm.bc_empty[u]);
+                return true;
+            };
+            for (uint32_t v = 0; ok; ++v) {
+                const uint32_t u = v & 1, nn = v >> 1;
+                if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) {
+                    ok = false;
+                    break;
+                }
+                if (!*reinterpret_cast<volatile int32_t *>(&sm.sched[u].valid)) break;
+                if (!bwait(&sm.cb_empty, (v & 1) ^ 1, sm, hdr, epoch)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ba = smem_u32(sm.bc[u][0]), ca = smem_u32(sm.bc[u][2]);
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
+                    mma_ss(tmem + kColCB, desc_sw128(ca + off, 16, 1024), desc_sw128(ba + off, 16, 1024), idCB, s > 0);
+                }
+                mma_commit(&sm.cb_full);
+                for (int hh = 0; hh < hs; ++hh, ++hc) {
+                    const uint32_t k = hc & 1, n = hc >> 1;
+                    if (!bwait(&sm.p_full[k], n & 1, sm, hdr, epoch) ||
+                        !bwait(&sm.s_free[k], (n & 1) ^ 1, sm, hdr, epoch)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = smem_u32(sm.x[k]), xsa = smem_u32(sm.xs[k]);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_ts(tmem + kColYI + 64 * k, tmem + kColP + 64 * k + 8 * s,
+                               desc_sw128(xa + 2048 * s, 8192, 1024), idPX, s > 0);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        mma_ss(tmem + kColS + 64 * k, desc_sw128(ba + 2048 * s, kTile, 1024),
+                               desc_sw128(xsa + 2048 * s, 8192, 1024), idST, s > 0);
+                    mma_commit(&sm.mma1[k]);
+                    mma_commit(&sm.x_empty[k]);
+                    if (pend && !issue_cs(pk, pn, pu, plast)) {
+                        ok = false;
+                        break;
+                    }
+                    pend = true;
+                    pk = k;
+                    pn = n;
+                    pu = u;
+                    plast = hh == hs - 1;
+                }
+            }
+            if (ok && pend) issue_cs(pk, pn, pu, plast);
+            // drain: every MMA issued above has completed before TMEM is released
+            mma_commit(&sm.drain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+            }
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ math warpgroup
+        const int q = warp & 3;              // TMEM lane quarter of this warp
+        const int i = 32 * q + lane;         // tile row (token within the chunk) owned by this thread
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        const bool leader = warp == 2 && lane == 0;
+        IO *yg = static_cast<IO *>(p.y);
+        uint32_t hc = 0;
+        bool pend = false;
+        uint32_t pk = 0, pn = 0;
+        float pecs = 0.f;
+        int64_t pbase = 0;
+        bool pvalid = false;
+        bool ok = true;
+        auto epilogue = [&]() -> bool {
+            if (!bwait(&sm.mma2[pk], pn & 1, sm, hdr, epoch)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                uint32_t a[16], c2[16];
+                tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * m, a);
+                tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * m, c2);
+                tmem_ld_wait();
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y0 = __uint_as_float(a[2 * e]) + pecs * __uint_as_float(c2[2 * e]);
+                    const float y1 = __uint_as_float(a[2 * e + 1]) + pecs * __uint_as_float(c2[2 * e + 1]);
+                    o[e] = pack_io<IO>(y0, y1);
+                }
+                if (pvalid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(yg + pbase + 16 * m);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            return true;
+        };
+        for (uint32_t v = 0; ok; ++v) {
+            const uint32_t u = v & 1, nn = v >> 1;
+            if (!bwait(&sm.bc_full[u], nn & 1, sm, hdr, epoch)) {
+                ok = false;
+                break;
+            }
+            const Sched sc = sm.sched[u];
+            if (!sc.valid) {
+                if (leader) mbar_arrive(&sm.bc_conv[u]);
+                break;
+            }
+            // (1) bf16 -> fp16 in place for the B and C tiles (same 16-bit positions, same swizzle)
+            if (kBf16) {
+#pragma unroll
+                for (int reg = 0; reg < 4; ++reg) {
+                    uint8_t *row = sm.bc[u][reg] + i * 128;
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) {
+                        uint8_t *ad = row + ((lc ^ (i & 7)) << 4);
+                        uint4 w = lds128(ad);
+                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_io<IO>(wv[e]);
+                            wv[e] = pack_f16(f.x, f.y);
+                        }
+                        sts128(ad, w);
+                    }
+                }
+            }
+            // (2) chunk cumsum: dt = softplus(dt_raw + dt_bias), inclusive scan of dt*A over the 128 rows
+            float dtv[kMaxHs], scn[kMaxHs];
+#pragma unroll
+            for (int hh = 0; hh < kMaxHs; ++hh) {
+                if (hh < hs) {
+                    const int h = sc.h0 + hh;
+                    dtv[hh] = softplus_f32(sm.cs2[u][hh][i] + p.dt_bias[h]);
+                    float s = dtv[hh] * p.A[h];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float w = __shfl_up_sync(0xffffffffu, s, o);
+                        if (lane >= o) s += w;
+                    }
+                    scn[hh] = s;
+                    if (lane == 31) sm.wsum[q][hh] = s;
+                }
+            }
+            bar_sync(kBarMath, 128);
+#pragma unroll
+            for (int hh = 0; hh < kMaxHs; ++hh) {
+                if (hh < hs) {
+                    float pre = 0.f;
+                    for (int qq = 0; qq < q; ++qq) pre += sm.wsum[qq][hh];
+                    sm.cs2[u][hh][i] = (scn[hh] + pre) * kLog2e;
+                    sm.dt[u][hh][i] = dtv[hh];
+                }
+            }
+            bar_sync(kBarMath, 128);
+#pragma unroll
+            for (int hh = 0; hh < kMaxHs; ++hh)
+                if (hh < hs) sm.wt[u][hh][i] = ex2(sm.cs2[u][hh][i | 31] - sm.cs2[u][hh][i]) * sm.dt[u][hh][i];
+            fence_proxy_async_smem();
+            bar_sync(kBarMath, 128);
+            if (leader) mbar_arrive(&sm.bc_conv[u]);
+
+            // (3) per head: X_s, P, then the previous head's epilogue
+            for (int hh = 0; hh < hs; ++hh, ++hc) {
+                const uint32_t k = hc & 1, n = hc >> 1;
+                const int h = sc.h0 + hh;
+                if (!bwait(&sm.x_full[k], n & 1, sm, hdr, epoch)) {
+                    ok = false;
+                    break;
+                }
+                const float cs2i = sm.cs2[u][hh][i];
+                const float xscale = ex2(sm.cs2[u][hh][kQ - 1] - cs2i) * sm.dt[u][hh][i];
+                {
+                    uint8_t *xr = sm.x[k] + i * 128;
+                    uint8_t *sr = sm.xs[k] + i * 128;
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) {
+                        const int off = (lc ^ (i & 7)) << 4;
+                        uint4 w = lds128(xr + off);
+                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+                        uint4 s4;
+                        uint32_t *sv = reinterpret_cast<uint32_t *>(&s4);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_io<IO>(wv[e]);
+                            sv[e] = pack_f16(f.x * xscale, f.y * xscale);
+                            if (kBf16) wv[e] = pack_f16(f.x, f.y);
+                        }
+                        if (kBf16) sts128(xr + off, w);
+                        sts128(sr + off, s4);
+                    }
+                }
+                fence_proxy_async_smem();
+                if (hh == 0) {
+                    if (!bwait(&sm.cb_full, v & 1, sm, hdr, epoch)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                // P = CB o decay o dt (+ D on the diagonal), masked above the diagonal, fp16 into TMEM
+                const float Dh = p.D ? p.D[h] : 0.f;
+                const float *cs2r = sm.cs2[u][hh];
+                const float *dtr = sm.dt[u][hh];
+                const float *wtr = sm.wt[u][hh];
+#pragma unroll
+                for (int J = 0; J < 4; ++J) {
+                    uint32_t pk16[16];
+                    if (J > q) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk16[e] = 0u;
+                    } else {
+                        uint32_t cb[32];
+                        tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
+                        tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
+                        tmem_ld_wait();
+                        if (J < q) {
+                            // below the diagonal block: exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j),
+                            // a = last row of block J; both factors <= 1
+                            const float ui = ex2(cs2i - cs2r[32 * J + 31]);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float v0 = __uint_as_float(cb[2 * e]) * ui * wtr[32 * J + 2 * e];
+                                const float v1 = __uint_as_float(cb[2 * e + 1]) * ui * wtr[32 * J + 2 * e + 1];
+                                pk16[e] = pack_f16(v0, v1);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int j0 = 32 * J + 2 * e, j1 = j0 + 1;
+                                float v0 = __uint_as_float(cb[2 * e]) * ex2(cs2i - cs2r[j0]) * dtr[j0];
+                                float v1 = __uint_as_float(cb[2 * e + 1]) * ex2(cs2i - cs2r[j1]) * dtr[j1];
+                                v0 = j0 < i ? v0 : (j0 == i ? v0 + Dh : 0.f);
+                                v1 = j1 < i ? v1 : (j1 == i ? v1 + Dh : 0.f);
+                                pk16[e] = pack_f16(v0, v1);
+                            }
+                        }
+                    }
+                    tmem_st16(tmem + lrow + kColP + 64 * k + 16 * J, pk16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                bar_sync(kBarMath, 128);
+                if (leader) {
+                    mbar_arrive(&sm.p_full[k]);
+                    if (hh == hs - 1) mbar_arrive(&sm.cb_empty);
+                }
+                if (pend && !epilogue()) {
+                    ok = false;
+                    break;
+                }
+                pend = true;
+                pk = k;
+                pn = n;
+                pecs = ex2(cs2i);
+                pvalid = i < sc.rows;
+                pbase = ((int64_t)sc.b * p.L + (int64_t)sc.c * kQ + i) * p.H * kP + (int64_t)h * kP;
+            }
+        }
+        if (ok && pend) epilogue();
+    } else {
+        // ------------------------------------------------------------ chain warpgroup
+        const int q = warp & 3;
+        const int nrow = 32 * q + lane;  // state row (d_state index) owned by this thread
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        const bool leader = warp == 6 && lane == 0;
+        const uint64_t limit = hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs;
+        const int64_t skip = hdr->skip_publish - 1;
+        const ST *init = static_cast<const ST *>(p.init);
+        ST *fin = static_cast<ST *>(p.final_states);
+        ST *ring = static_cast<ST *>(p.ring);
+        uint32_t hc = 0;
+        bool ok = true;
+        for (uint32_t v = 0; ok; ++v) {
+            const uint32_t u = v & 1, nn = v >> 1;
+            if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) break;
+            const Sched sc = sm.sched[u];
+            if (!sc.valid) break;
+            for (int hh = 0; hh < hs; ++hh, ++hc) {
+                const uint32_t k = hc & 1, n = hc >> 1;
+                const int64_t chain = (int64_t)sc.b * p.H + sc.h0 + hh;
+                if (!bwait(&sm.mma1[k], n & 1, sm, hdr, epoch)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[kP];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lrow + kColS + 64 * k + 16 * m, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) s[16 * m + e] = __uint_as_float(r[e]);
+                }
+                tc_fence_before();
+                bar_sync(kBarChain, 128);
+                if (leader) mbar_arrive(&sm.s_free[k]);
+                const float a = ex2(sm.cs2[u][hh][kQ - 1]);  // decay across the chunk
+                float S[kP];
+                if (sc.c == 0) {
+#pragma unroll
+                    for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                } else {
+                    const bool got = !aborted(hdr, epoch) &&
+                                     wait_flag(&p.flags[chain * p.nc + sc.c - 1], epoch, hdr, limit, 0, sc.c);
+                    const ST *slot = ring + (chain * 2 + (sc.c & 1)) * (int64_t)(kP * kN);
+                    if (got) {
+                        if (sizeof(ST) == 4) {
+                            const float4 *src = reinterpret_cast<const float4 *>(slot);
+#pragma unroll
+                            for (int m = 0; m < kP / 4; ++m) {
+                                const float4 f = __ldcg(src + m * kN + nrow);
+                                S[4 * m] = f.x;
+                                S[4 * m + 1] = f.y;
+                                S[4 * m + 2] = f.z;
+                                S[4 * m + 3] = f.w;
+                            }
+                        } else {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(slot);
+#pragma unroll
+                            for (int m = 0; m < kP / 8; ++m) {
+                                const uint4 w = __ldcg(src + m * kN + nrow);
+                                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = unpack_f16(wv[e]);
+                                    S[8 * m + 2 * e] = f.x;
+                                    S[8 * m + 2 * e + 1] = f.y;
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+                    }
+                }
+                // S_out = a S_in + s (kept in s[])
+#pragma unroll
+                for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
+                if (sc.c == p.nc - 1) {
+                    if (fin) {
+#pragma unroll
+                        for (int pp = 0; pp < kP; ++pp) fin[(chain * kP + pp) * kN + nrow] = from_f32<ST>(s[pp]);
+                    }
+                } else if (sc.c != skip) {
+                    ST *slot = ring + (chain * 2 + ((sc.c + 1) & 1)) * (int64_t)(kP * kN);
+                    if (sizeof(ST) == 4) {
+                        float4 *dst = reinterpret_cast<float4 *>(slot);
+#pragma unroll
+                        for (int m = 0; m < kP / 4; ++m)
+                            __stcg(dst + m * kN + nrow, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(slot);
+#pragma unroll
+                        for (int m = 0; m < kP / 8; ++m)
+                            __stcg(dst + m * kN + nrow,
+                                   make_uint4(pack_f16(s[8 * m], s[8 * m + 1]), pack_f16(s[8 * m + 2], s[8 * m + 3]),
+                                              pack_f16(s[8 * m + 4], s[8 * m + 5]), pack_f16(s[8 * m + 6], s[8 * m + 7])));
+                    }
+                    __threadfence();
+                    bar_sync(kBarChain, 128);
+                    if (leader) st_release_gpu(&p.flags[chain * p.nc + sc.c], epoch);
+                }
+                // S_in (fp16) -> the C.S operand: K-row nrow of a [128 x 64] MN-major 128B-swizzled tile
+                {
+                    uint8_t *row = sm.xs[k] + nrow * 128;
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc)
+                        sts128(row + ((lc ^ (nrow & 7)) << 4),
+                               make_uint4(pack_f16(S[8 * lc], S[8 * lc + 1]), pack_f16(S[8 * lc + 2], S[8 * lc + 3]),
+                                          pack_f16(S[8 * lc + 4], S[8 * lc + 5]), pack_f16(S[8 * lc + 6], S[8 * lc + 7])));
+                }
+                fence_proxy_async_smem();
+                bar_sync(kBarChain, 128);
+                if (leader) mbar_arrive(&sm.sin_full[k]);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (tid == 0) {
+        __threadfence();
+        const uint32_t d = atomicAdd(&hdr->done, 1u);
+        if (d == gridDim.x - 1) {
+            hdr->ticket = 0;
+            hdr->done = 0;
+            __threadfence();
+            st_relaxed_gpu(&hdr->epoch, epoch);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 4-D map over a [batch, L, mid, inner] 16-bit tensor, box = [1, 128 rows, 1, 64 inner], 128B swizzle.
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t L, int64_t batch) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2),
+                                   (cuuint64_t)(inner * mid * L * 2)};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kQ, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+               const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename IO, typename ST>
+cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
+    CUtensorMap mx, mb, mc;
+    const bool bf = !std::is_same<IO, __half>::value;
+    if (!make_map(&mx, p.x, bf, kP, p.H, p.L, p.batch) || !make_map(&mb, p.B, bf, kN, p.G, p.L, p.batch) ||
+        !make_map(&mc, p.C, bf, kN, p.G, p.L, p.batch))
+        return cudaErrorInvalidValue;
+    const size_t smem = sizeof(Smem) + 1024;
+    auto k = tc_kernel<IO, ST>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, hs);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype) {
+    return P == kP && N == kN && Q == kQ && (io_dtype == 1 || io_dtype == 2);
+}
+
+size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
+    return (size_t)chains * 2 * (size_t)(P * N) * (state_dtype == 0 ? 4 : 2);
+}
+
+uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {
+    (void)G;
+    return (uint32_t)(nc * batch * (H / hs));
+}
+
+// Heads per work unit: the largest divisor of heads-per-group (<= 8) that still
+// leaves at least two units per SM; small problems fall back to 1.
+int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms) {
+    const int64_t hpg = H / G;
+    for (int d = kMaxHs; d >= 1; --d)
+        if (hpg % d == 0 && nc * batch * (H / d) >= 2 * (int64_t)sms) return d;
+    return 1;
+}
+
+cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
+    if (io_dtype == 1)
+        return state_dtype == 0 ? launch_t<__nv_bfloat16, float>(p, hs, sms, stream)
+                                : launch_t<__nv_bfloat16, __half>(p, hs, sms, stream);
+    return state_dtype == 0 ? launch_t<__half, float>(p, hs, sms, stream) : launch_t<__half, __half>(p, hs, sms, stream);
+}
 
 }  // namespace ssd

@@ -125,3 +125,117 @@ def test_injected_missing_publish_times_out_and_recovers():
     m.debug_set(ws, timeout_ns=0, skip_publish=-1)
     y1, f1 = run_gpu(w, inp, kernel="simt", ws=ws)
     assert torch.equal(y0, y1) and torch.equal(f0, f1)
+
+
+# ----------------------------------------------------------------------------- tensor-core kernel
+TC_SMALL = [
+    ("m130-bf16", dict(batch=2, seqlen=300, nheads=4, ngroups=2)),              # ragged tail, 2 groups
+    ("m130-bf16", dict(batch=1, seqlen=257, nheads=2, io="f16", state="f16")),  # fp16 I/O and states
+    ("m130-bf16", dict(batch=3, seqlen=1, nheads=2)),                           # one token
+    ("m130-bf16", dict(batch=1, seqlen=2048, nheads=8, init="none")),           # 16 chunks, no init
+    ("m130-bf16", dict(batch=2, seqlen=1000, nheads=6, ngroups=3, state="f16")),
+]
+
+
+@pytest.mark.parametrize("name,over", TC_SMALL, ids=[f"{n}-{i}" for i, (n, _) in enumerate(TC_SMALL)])
+def test_tc_parity_small(name, over):
+    w = WORKLOADS[name].with_(**over)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp, kernel="tc")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"tc {name} {over}")
+
+
+@pytest.mark.parametrize("hs", [1, 2, 4, 8])
+def test_tc_heads_per_unit(hs, monkeypatch):
+    monkeypatch.setenv("SSD_TC_HEADS_PER_UNIT", str(hs))
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=700, nheads=16, ngroups=2, seed=50 + hs)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp, kernel="tc")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"tc hs={hs}")
+
+
+def test_tc_no_D_alias_and_determinism():
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=600, nheads=8)
+    inp = make_inputs(w, device="cuda")
+    inp["D"] = None
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    ws = m.Workspace("cuda")
+    init = inp["init_states"].clone()
+    y, fin = run_gpu(w, dict(inp, init_states=init), kernel="tc", ws=ws, final_states=init)
+    assert fin.data_ptr() == init.data_ptr()
+    assert_parity(w, y, fin, yr, fr)
+    for _ in range(2):
+        y2, f2 = run_gpu(w, inp, kernel="tc", ws=ws)
+        assert torch.equal(y, y2) and torch.equal(fin, f2)
+
+
+def test_tc_injected_missing_publish_times_out_and_recovers():
+    w = WORKLOADS["m130-bf16"].with_(batch=1, seqlen=1024, nheads=8)
+    inp = make_inputs(w, device="cuda")
+    ws = m.Workspace("cuda")
+    y0, f0 = run_gpu(w, inp, kernel="tc", ws=ws)
+    m.debug_set(ws, timeout_ns=50_000_000, skip_publish=2)
+    m.ssd_fwd(**inp, chunk_size=w.chunk, kernel="tc", workspace=ws)
+    with pytest.raises(m.SsdError) as e:
+        m.check(ws)
+    assert e.value.status == 5
+    m.debug_set(ws, timeout_ns=0, skip_publish=-1)
+    y1, f1 = run_gpu(w, inp, kernel="tc", ws=ws)
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)
+
+
+def test_tc_matches_simt_kernel():
+    """Both kernels against each other on the same inputs (a second, oracle-free cross-check)."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=900, nheads=8)
+    inp = make_inputs(w, device="cuda")
+    yt, ft = run_gpu(w, inp, kernel="tc")
+    ys, fs = run_gpu(w, inp, kernel="simt")
+    a, b = yt.double().cpu().numpy(), ys.double().cpu().numpy()
+    # each output is within 1e-2 + 2^-8 |y| of the exact value, so the two are within twice that
+    excess = np.abs(a - b) - (2e-2 + 2.0 ** -7 * np.abs(b))
+    assert excess.max() <= 0, float(excess.max())
+
+
+# full-size workloads, in the launch configuration the benchmark times; the oracle checks sampled chains
+FULL = ["m130-bf16", "m2p7-L16k-q128", "m2p7-L8k-b1", "m2p7-L8k-b8", "m2p7-L8k-b32", "long-L256k-g8"]
+
+
+def sampled_chains(w, n):
+    g = np.random.default_rng(w.seed)
+    all_c = [(b, h) for b in range(w.batch) for h in range(w.nheads)]
+    if len(all_c) <= n:
+        return all_c
+    idx = sorted(g.choice(len(all_c), size=n, replace=False))
+    # always include the first and last chain
+    return sorted(set([all_c[0], all_c[-1]] + [all_c[i] for i in idx]))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_tc_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp)
+    assert m.kernel_for(m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk,
+                                       DTYPES[w.io], DTYPES[w.state])) == "tc"
+    n = 96 if w.seqlen <= 4096 else (12 if w.seqlen <= 16384 else 4)
+    chains = sampled_chains(w, n)
+    per = w.nheads // w.ngroups
+    sub = dict(
+        x=torch.stack([inp["x"][b, :, h] for b, h in chains])[:, :, None].cpu(),
+        dt_raw=torch.stack([inp["dt_raw"][b, :, h] for b, h in chains])[:, :, None].cpu(),
+        B=torch.stack([inp["B"][b, :, h // per] for b, h in chains])[:, :, None].cpu(),
+        C=torch.stack([inp["C"][b, :, h // per] for b, h in chains])[:, :, None].cpu(),
+    )
+    ys = torch.stack([y[b, :, h] for b, h in chains]).double().cpu().numpy()
+    fs = torch.stack([fin[b, h] for b, h in chains]).double().cpu().numpy()
+    hs = np.array([h for _, h in chains])
+    init = None if inp["init_states"] is None else torch.stack([inp["init_states"][b, h] for b, h in chains])
+    yr, fr = oracle.ssd_chains(sub["x"][:, :, 0], sub["dt_raw"][:, :, 0], inp["dt_bias"].cpu()[hs],
+                               inp["A"].cpu()[hs], sub["B"][:, :, 0], sub["C"][:, :, 0], inp["D"].cpu()[hs],
+                               None if init is None else init.cpu())
+    ok, s = gate_y(ys, yr, w.io)
+    assert ok, f"{name}: {s}"
+    okf, sf = gate_final(fs, fr, w.io, w.state)
+    assert okf, f"{name} final: {sf}"
