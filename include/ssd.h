@@ -108,6 +108,31 @@ SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);
  *                 injection: no memory fault, no trap, the kernel returns. */
 SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream);
 
+/* ssd_fwd without a workspace argument, for callers that cannot allocate
+ * device memory (no counterpart on the pages; it is a library convenience).
+ * Some callers hand a kernel only its inputs and outputs: host applications or
+ * plugin frameworks that own every byte of device memory, or latency-critical
+ * loops that cannot afford a cudaMalloc, which may synchronise the device.
+ * This entry point takes its scratch from a 16 MiB array compiled into the
+ * library (every GPU that loads the library holds it until the process exits)
+ * and allocates nothing.
+ *  - Problems whose ssd_fwd_workspace_size() exceeds 16 MiB are rejected with
+ *    SSD_ERR_WORKSPACE (at headdim 64, d_state 128 this is roughly 250 (batch x
+ *    head) chains with fp32 states, 500 with fp16 states).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array. Each call zero-fills the part it uses on
+ *    `stream` before launching, so earlier contents do not matter, but calls
+ *    that overlap on the GPU (unordered streams or host threads) race on it.
+ *  - A device-side wait that gives up is not reported (there is no workspace
+ *    to pass to ssd_fwd_check); it needs a device malfunction to happen.
+ * Arguments, layouts and the other errors are those of ssd_fwd. */
+SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob, const void *x, const void *dt_raw,
+                                            const float *dt_bias, const float *A, const void *B, const void *C,
+                                            const float *D, const void *init_states, void *y, void *final_states,
+                                            void *stream);
+
 /* Which kernel ssd_fwd would run for `prob` (SSD_KERNEL_SIMT or _TC), or a
  * negative ssd_status_t if the problem is rejected. */
 SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob);

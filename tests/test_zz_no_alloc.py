@@ -1,0 +1,70 @@
+"""The allocation-free entry point ssd_fwd_static_scratch, called through the C ABI.
+
+It serves callers that cannot allocate device memory (a host application or
+plugin framework that owns all device memory, or a loop that cannot afford a
+cudaMalloc): the scratch comes from an array compiled into the library. Its
+results must match ssd_fwd with a caller workspace, on two calls in a row
+(the second one reuses the array the first left behind, with a different
+problem size).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import mamba_ssd_prefill_gb300 as m
+from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs
+from parity import gate_final, gate_y
+
+pytestmark = pytest.mark.gpu
+
+
+def _entry():
+    L = m.lib()
+    f = L.ssd_fwd_static_scratch
+    f.argtypes = [ctypes.POINTER(m.SsdProblem)] + [ctypes.c_void_p] * 11
+    f.restype = ctypes.c_int
+    return f
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _call_static(w, inp):
+    st = DTYPES[w.state]
+    prob = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io], st)
+    y = torch.empty_like(inp["x"])
+    fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=st, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = _entry()(ctypes.byref(prob), _p(inp["x"]), _p(inp["dt_raw"]), _p(inp["dt_bias"]), _p(inp["A"]), _p(inp["B"]),
+                  _p(inp["C"]), _p(inp["D"]), _p(inp["init_states"]), _p(y), _p(fin), stream)
+    assert rc == 0, m.STATUS.get(rc, rc)
+    torch.cuda.synchronize()
+    return y, fin
+
+
+def test_static_scratch_matches_workspace_entry_point_twice():
+    cases = [WORKLOADS["m130-bf16"].with_(batch=2, seqlen=1000, nheads=8, seed=71),
+             WORKLOADS["m130-bf16"].with_(batch=4, seqlen=2048, nheads=24, state="f16", seed=72)]
+    for w in cases:  # two calls in a row, the second with a larger scratch footprint
+        inp = make_inputs(w, device="cuda")
+        y_s, f_s = _call_static(w, inp)
+        ws = m.Workspace("cuda")
+        y_w, f_w = m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], workspace=ws)
+        m.check(ws)
+        ok, s = gate_y(y_s.double().cpu().numpy(), y_w.double().cpu().numpy(), w.io)
+        assert ok, s
+        okf, sf = gate_final(f_s.double().cpu().numpy(), f_w.double().cpu().numpy(), w.io, w.state)
+        assert okf, sf
+
+
+def test_static_scratch_rejects_problems_over_the_limit():
+    w = WORKLOADS["m2p7-L8k-b32"]
+    prob = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io],
+                          DTYPES[w.state])
+    assert m.workspace_size(prob) > 16 << 20
+    x = torch.empty(16, dtype=torch.uint8, device="cuda")
+    rc = _entry()(ctypes.byref(prob), *([_p(x)] * 10), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 3  # SSD_ERR_WORKSPACE, nothing launched
