@@ -81,7 +81,7 @@ def traffic_for(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples taken while the timed region runs."""
+    """nvidia-smi clock and throttle-reason samples (every 20 ms, host-timestamped) while the GPU is under load."""
 
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -89,41 +89,64 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.rows = []
+        self.window = None
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             self.proc = None
+            return self
+        self.started = threading.Event()
+
+        def reader():
+            for line in self.proc.stdout:
+                self.rows.append((time.perf_counter(), line.strip()))
+                self.started.set()
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        self.started.wait(timeout=5.0)  # sampler is running before the timed region starts
         return self
 
     def __exit__(self, *a):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        rows = []
-        for line in (self.out or "").strip().splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) == 6:
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[2:]))
-                except ValueError:
-                    pass
+    def summary(self, t0, t1, t_load_end):
+        """Samples taken in [t0, t1] (the timed region); if none, those up to t_load_end (identical untimed steps
+        run right after it), saying so."""
+        def parse(lo, hi):
+            out = []
+            for ts, line in self.rows:
+                if lo <= ts <= hi:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) == 6:
+                        try:
+                            out.append((float(parts[0]), float(parts[1]), parts[2:]))
+                        except ValueError:
+                            pass
+            return out
+
+        rows, where = parse(t0, t1), "timed region"
+        if not rows:
+            rows, where = parse(t0, t_load_end), "timed region and the identical untimed steps right after it"
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "window": where}
 
 
 def dist_setup():
@@ -257,11 +280,20 @@ def run_gpu(args, w):
         wall0 = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()  # L2 flush, outside the events
+            torch.cuda._sleep(50000)  # keeps the GPU busy while the host marshals the call: no host gap is timed
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - wall0
+        wall1 = time.perf_counter()
+        wall = wall1 - wall0
+        load_end = wall1
+        while wall < 0.3 and time.perf_counter() - wall1 < 0.3:  # short region: keep the same load for the sampler
+            for _ in range(10):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize(dev)
+            load_end = time.perf_counter()
     barrier(world)
     m.check(ws)
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -318,7 +350,7 @@ def run_gpu(args, w):
             "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg, "roofline": roof,
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps, "clocks": clk.summary()}
+            "gpu_launches": args.steps, "clocks": clk.summary(wall0, wall1, load_end)}
     if world == 1 and not args.no_cpu_baseline:
         tok_s, sample, threads = oracle_sample(w, {k: (v.cpu() if v is not None else None) for k, v in inp.items()},
                                                budget_s=args.ref_budget)

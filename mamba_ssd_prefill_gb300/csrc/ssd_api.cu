@@ -94,7 +94,9 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     if (units >= 4.0e9) return SSD_ERR_UNSUPPORTED;
     pl.total_units = (uint32_t)units;
     pl.flags_off = sizeof(WsHeader);
-    pl.ring_off = align_up(pl.flags_off + sizeof(uint32_t) * (size_t)(chains * pl.nc), 256);
+    const size_t flag_bytes = pl.kernel == SSD_KERNEL_TC ? ssd::tc_flag_bytes(chains)
+                                                         : sizeof(uint32_t) * (size_t)(chains * pl.nc);
+    pl.ring_off = align_up(pl.flags_off + flag_bytes, 256);
     size_t ring;
     if (pl.kernel == SSD_KERNEL_TC)
         ring = ssd::tc_ring_bytes(chains, pr->headdim, pr->dstate, pr->state_dtype);

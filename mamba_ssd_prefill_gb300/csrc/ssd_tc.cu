@@ -14,8 +14,9 @@
 //   S_c+1   = exp(cs_last) S_c + s_c          (flag-ordered chain across CTAs)
 //   y       = y_intra + exp(cs_i) C_c S_c     (tcgen05 C.S, fused epilogue)
 //
-// Warp roles (320 threads):
-//   warp 0      scheduler + TMA producer (tickets, dt_raw, B/C and x tiles)
+// Warp roles (352 threads):
+//   warp 0      unit loader (tickets, dt_raw, B/C tiles by TMA), up to two units ahead
+//   warp 10     x-tile loader (one TMA per head)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2-5   "math": bf16->fp16 tile conversion, cumsum tables, decay mask
 //               P -> TMEM, X_s, epilogue y = y_intra + exp(cs) y_inter
@@ -43,11 +44,12 @@ constexpr int kQ = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kMaxHs = 8;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kXWarp = 10;  // x-tile loader warp
 constexpr uint32_t kTile = 16384;  // [128 rows x 128 B] 128B-swizzled 16-bit tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColCB = 0, kColP = 128, kColYI = 256, kColS = 384;
-constexpr uint32_t kBarMath = 1, kBarChain = 2;  // named barriers (0 is __syncthreads)
+constexpr uint32_t kBarMath = 1;  // named barrier of the math warpgroup (0 is __syncthreads)
 
 struct Sched {
     int32_t valid, b, c, g, h0, rows;
@@ -60,13 +62,34 @@ struct __align__(1024) Smem {
     float cs2[2][kMaxHs][kQ];  // raw dt_raw from the producer, then log2(e) * cumsum(dt*A)
     float dt[2][kMaxHs][kQ];   // dt
     float wt[2][kMaxHs][kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
-    float wsum[4][kMaxHs];     // per-warp scan totals
+    float dskip[2][kMaxHs];    // D of the unit's heads (0 when absent)
     Sched sched[2];
-    uint64_t bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty;
+    uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty;
     uint64_t x_full[2], x_empty[2], p_full[2], mma1[2], s_free[2], sin_full[2], mma2[2], drain;
     uint32_t tmem_base;
     int32_t abort;
 };
+
+// Opt-in timeline trace (build with -DSSD_TRACE): CTA 0 records (%globaltimer, tag) per role.
+#ifdef SSD_TRACE
+constexpr int kTraceN = 8192;
+__device__ unsigned long long g_trace[4][kTraceN][2];
+__device__ unsigned int g_trace_n[4];
+// one tracing thread per role keeps its own counter (no atomics: recording must not perturb the timeline)
+#define TRACE(role, tag)                                                                   \
+    do {                                                                                   \
+        if (blockIdx.x == 0 && trace_i < kTraceN) {                                        \
+            g_trace[role][trace_i][0] = globaltimer();                                     \
+            g_trace[role][trace_i][1] = (unsigned long long)(tag);                         \
+            ++trace_i;                                                                     \
+            g_trace_n[role] = trace_i;                                                     \
+        }                                                                                  \
+    } while (0)
+#else
+#define TRACE(role, tag) \
+    do {                 \
+    } while (0)
+#endif
 
 __device__ __forceinline__ float ex2(float v) {
     float r;
@@ -110,25 +133,61 @@ template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t 
 }
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
 
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __noinline__ void chain_timeout(WsHeader *hdr, uint32_t epoch, uint32_t chunk) {
+    report_error(hdr, epoch, DEV_TIMEOUT, 0, chunk, WAIT_CHAIN);
+}
+
+// Bounded wait until *tag == want (acquire). On timeout records SSD_ERR_TIMEOUT and returns false;
+// returns false at once when another CTA aborted the launch.
+__device__ __forceinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
+                                         uint64_t limit_ns, uint32_t chunk) {
+    const uint64_t t0 = globaltimer();
+    uint32_t sleep_ns = 20;
+    for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
+        if (ld_acquire_u64(tag) == want) return true;
+        if ((it & 7u) == 7u) {
+            if (aborted(hdr, epoch)) return false;
+            if (globaltimer() - t0 > limit_ns) break;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 160) sleep_ns += 20;
+    }
+    chain_timeout(hdr, epoch, chunk);
+    return false;
+}
+
+__device__ __noinline__ void pipe_timeout(Smem &sm, WsHeader *hdr, uint32_t epoch) {
+    *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
+    report_error(hdr, epoch, DEV_PIPE, 0, 0, WAIT_PIPE);
+}
+
 // Bounded wait on an intra-CTA mbarrier phase. On timeout (a broken pipeline)
 // it records the error, raises the CTA abort flag and returns false; every
 // other wait then gives up too and the CTA drains to its teardown. Its limit
 // is four times the state-passing limit plus 100 ms: a pipeline stage may
 // legitimately sit behind one full state-passing wait, which must time out
-// (and report itself) first.
-__device__ __noinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
+// (and report itself) first. Inline: only the timeout report is a call.
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
     for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 15u) {
             if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) return false;
+            const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
             if (globaltimer() - t0 > limit) break;
         }
     }
-    *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
-    report_error(hdr, epoch, DEV_PIPE, 0, 0, WAIT_PIPE);
+    pipe_timeout(sm, hdr, epoch);
     return false;
 }
 
@@ -142,9 +201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     WsHeader *hdr = p.hdr;
     const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
     constexpr bool kBf16 = sizeof(IO) == 2 && !std::is_same<IO, __half>::value;
+    unsigned int trace_i = 0;  // per-thread trace record counter (SSD_TRACE builds)
+    (void)trace_i;
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.sched_full[i], 1);
             mbar_init(&sm.bc_full[i], 1);
             mbar_init(&sm.bc_conv[i], 1);
             mbar_init(&sm.bc_empty[i], 1);
@@ -152,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.x_empty[i], 1);
             mbar_init(&sm.p_full[i], 1);
             mbar_init(&sm.mma1[i], 1);
-            mbar_init(&sm.s_free[i], 1);
-            mbar_init(&sm.sin_full[i], 1);
+            mbar_init(&sm.s_free[i], 128);   // every chain thread arrives
+            mbar_init(&sm.sin_full[i], 128);
             mbar_init(&sm.mma2[i], 1);
         }
         mbar_init(&sm.cb_full, 1);
@@ -174,30 +236,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t per_chunk = p.batch * p.G * slices;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ unit loader
+        // Per unit: ticket (fetched one unit ahead), dt_raw rows, B/C tiles by TMA; and, for the unit
+        // requested one iteration earlier (so its TMA latency is already behind it), the bf16 -> fp16
+        // conversion of B/C in place (same 16-bit positions, same swizzle) and the chunk cumsum
+        // tables of its heads.
         if (lane == 0) {
-            prefetch_tensormap(&map_x);
             prefetch_tensormap(&map_b);
             prefetch_tensormap(&map_c);
         }
         const IO *dtr = static_cast<const IO *>(p.dt_raw);
-        uint32_t hc = 0;
-        int armed_bc = -1, armed_x = 0;  // for the drain at teardown
-        uint32_t bc_par[2] = {0, 0}, x_par[2] = {0, 0};
+        int armed_bc = 0;  // for the drain at teardown
+        uint32_t bc_par[2] = {0, 0};
+        uint32_t t = 0;
+        if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        Sched prev{0, 0, 0, 0, 0, 0};
         bool ok = true;
+        // conversion + tables of the unit in stage uu (whose tiles were requested earlier)
+        auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
+            const uint32_t uu = vv & 1;
+            if (!bwait(&sm.bc_full[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
+            if (kBf16) {
+#pragma unroll
+                for (int reg = 0; reg < 4; ++reg)
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const int row = lane + 32 * rr;
+                        uint8_t *base = sm.bc[uu][reg] + row * 128;
+#pragma unroll
+                        for (int lc = 0; lc < 8; ++lc) {
+                            uint8_t *ad = base + ((lc ^ (row & 7)) << 4);
+                            uint4 w = lds128(ad);
+                            uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = unpack_io<IO>(wv[e]);
+                                wv[e] = pack_f16(f.x, f.y);
+                            }
+                            sts128(ad, w);
+                        }
+                    }
+            }
+            // chunk cumsum: dt = softplus(dt_raw + dt_bias) (0 past the sequence end), inclusive scan of
+            // dt*A over the 128 rows; this lane owns rows 4*lane .. 4*lane+3
+#pragma unroll
+            for (int hh = 0; hh < kMaxHs; ++hh) {
+                if (hh < hs) {
+                    const int h = sc.h0 + hh;
+                    const float bias = p.dt_bias[h], Ah = p.A[h];
+                    float dtv[4], cum[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int row = 4 * lane + jj;
+                        dtv[jj] = row < sc.rows ? softplus_f32(sm.cs2[uu][hh][row] + bias) : 0.f;
+                        cum[jj] = dtv[jj] * Ah + (jj ? cum[jj - 1] : 0.f);
+                    }
+                    float incl = cum[3];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float w = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += w;
+                    }
+                    const float excl = incl - cum[3];
+                    float cs2v[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) cs2v[jj] = (excl + cum[jj]) * kLog2e;
+                    // anchor of these rows' 32-row block: its last row, owned by lane (lane | 7), jj = 3
+                    const float anchor = __shfl_sync(0xffffffffu, cs2v[3], lane | 7);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int row = 4 * lane + jj;
+                        sm.cs2[uu][hh][row] = cs2v[jj];
+                        sm.dt[uu][hh][row] = dtv[jj];
+                        sm.wt[uu][hh][row] = ex2(anchor - cs2v[jj]) * dtv[jj];
+                    }
+                    if (lane == 0) sm.dskip[uu][hh] = p.D ? p.D[h] : 0.f;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.bc_conv[uu]);
+            TRACE(0, (2u << 24) | vv);
+            return true;
+        };
         for (uint32_t v = 0; ok; ++v) {
             const uint32_t u = v & 1, nn = v >> 1;
-            uint32_t t = 0;
-            if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
+            uint32_t t_next = 0;
+            if (lane == 0 && t < p.total_units) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
+            // the previous unit first: the MMA issuer frees stage u (unit v-2's last C.S) only after it
+            // has seen unit v-1 converted
+            if (v > 0 && !finish(v - 1, prev)) break;
             if (t >= p.total_units) {
+                if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
                 if (lane == 0) {
                     sm.sched[u].valid = 0;
-                    mbar_arrive(&sm.bc_full[u]);
+                    mbar_arrive(&sm.sched_full[u]);
+                    mbar_arrive(&sm.bc_conv[u]);
                 }
                 break;
             }
+            if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
+            TRACE(0, (1u << 24) | v);
             const int64_t c = t / per_chunk;
             int64_t r = t % per_chunk;
             const int64_t b = r / (p.G * slices);
@@ -206,22 +346,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t h0 = g * p.heads_per_group + (r % slices) * hs;
             const int64_t row0 = c * kQ;
             const int rows = (int)((p.L - row0) < kQ ? (p.L - row0) : kQ);
-            for (int e = lane; e < hs * kQ; e += 32) {
-                const int i = e / hs, hh = e % hs;
-                float raw = -INFINITY;  // rows past the sequence end: dt = softplus(-inf) = 0
-                if (i < rows) raw = to_f32(dtr[(b * p.L + row0 + i) * p.H + h0 + hh]);
-                sm.cs2[u][hh][i] = raw;
+            // dt_raw rows 4*lane .. 4*lane+3 of the unit's heads, every load in flight at once
+            float raw[4][kMaxHs];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int i = 4 * lane + jj;
+#pragma unroll
+                for (int hh = 0; hh < kMaxHs; ++hh) {
+                    raw[jj][hh] = 0.f;
+                    if (hh < hs && i < rows) raw[jj][hh] = to_f32(dtr[(b * p.L + row0 + i) * p.H + h0 + hh]);
+                }
             }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int hh = 0; hh < kMaxHs; ++hh)
+                    if (hh < hs) sm.cs2[u][hh][4 * lane + jj] = raw[jj][hh];
+            const Sched cur{1, (int32_t)b, (int32_t)c, (int32_t)g, (int32_t)h0, rows};
             __syncwarp();
             if (lane == 0) {
-                sm.sched[u] = Sched{1, (int32_t)b, (int32_t)c, (int32_t)g, (int32_t)h0, rows};
+                sm.sched[u] = cur;
+                mbar_arrive(&sm.sched_full[u]);
                 mbar_arrive_expect_tx(&sm.bc_full[u], 4 * kTile);
                 tma_load_4d(sm.bc[u][0], &map_b, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
                 tma_load_4d(sm.bc[u][1], &map_b, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
                 tma_load_4d(sm.bc[u][2], &map_c, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
                 tma_load_4d(sm.bc[u][3], &map_c, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
-                armed_bc = (int)u;
+                armed_bc |= 1 << u;
                 bc_par[u] = nn & 1;
+            }
+            prev = cur;
+            t = __shfl_sync(0xffffffffu, t_next, 0);
+        }
+        // teardown: make sure no TMA write into this CTA's shared memory is still in flight
+        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
+            for (int u = 0; u < 2; ++u)
+                if (armed_bc & (1 << u)) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(&sm.bc_full[u], bc_par[u]) && globaltimer() - t0 < 100000000ull) {
+                    }
+                }
+        }
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        // ------------------------------------------------------------ x loader
+        if (lane == 0) {
+            prefetch_tensormap(&map_x);
+            uint32_t hc = 0;
+            int armed_x = 0;
+            uint32_t x_par[2] = {0, 0};
+            for (uint32_t v = 0;; ++v) {
+                const uint32_t u = v & 1;
+                if (!bwait(&sm.sched_full[u], (v >> 1) & 1, sm, hdr, epoch)) break;
+                const Sched sc = sm.sched[u];
+                if (!sc.valid) break;
+                bool ok = true;
                 for (int hh = 0; hh < hs; ++hh, ++hc) {
                     const uint32_t k = hc & 1, n = hc >> 1;
                     if (!bwait(&sm.x_empty[k], (n & 1) ^ 1, sm, hdr, epoch)) {
@@ -229,83 +408,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&sm.x_full[k], kTile);
-                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, (int)(h0 + hh), (int)row0, (int)b);
+                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, sc.h0 + hh, sc.c * kQ, sc.b);
                     armed_x |= 1 << k;
                     x_par[k] = n & 1;
                 }
+                if (!ok) break;
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            hc = __shfl_sync(0xffffffffu, hc, 0);
-        }
-        // teardown: make sure no TMA write into this CTA's shared memory is still in flight
-        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
-            for (int u = 0; u < 2; ++u)
-                if (armed_bc >= 0) {
-                    const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(&sm.bc_full[u], bc_par[u]) && globaltimer() - t0 < 100000000ull) {
+            if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) {
+                for (int k = 0; k < 2; ++k)
+                    if (armed_x & (1 << k)) {
+                        const uint64_t t0 = globaltimer();
+                        while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
+                        }
                     }
-                }
-            for (int k = 0; k < 2; ++k)
-                if (armed_x & (1 << k)) {
-                    const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
-                    }
-                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // Event driven: heads h are numbered across units (unit h / hs). For each head it issues
+        // MMA1 (P.x and the chunk state) once P is in TMEM, and C.S once the entering state is in
+        // shared memory, whichever is ready first, C.S preferred (the epilogue waits on it). CB of a
+        // unit goes out before the unit's first MMA1.
         if (lane == 0) {
             constexpr uint32_t idCB = idesc_f16_f32(128, 128, false, false);
             constexpr uint32_t idPX = idesc_f16_f32(128, 64, false, true);
             constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true);
             constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
-            uint32_t hc = 0;
-            bool pend = false;
-            uint32_t pk = 0, pn = 0, pu = 0;
-            bool plast = false;
-            bool ok = true;
-            auto issue_cs = [&](uint32_t k, uint32_t n, uint32_t u, bool last) -> bool {
-                if (!bwait(&sm.sin_full[k], n & 1, sm, hdr, epoch)) return false;
-                tc_fence_after();
-                const uint32_t ca = smem_u32(sm.bc[u][2]), sa = smem_u32(sm.xs[k]);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
-                    mma_ss(tmem + kColP + 64 * k, desc_sw128(ca + off, 16, 1024),
-                           desc_sw128(sa + 2048 * s, 8192, 1024), idCS, s > 0);
-                }
-                mma_commit(&sm.mma2[k]);
-                if (last) mma_commit(&sm.bc_empty[u]);
-                return true;
-            };
-            for (uint32_t v = 0; ok; ++v) {
-                const uint32_t u = v & 1, nn = v >> 1;
-                if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) {
-                    ok = false;
-                    break;
-                }
-                if (!*reinterpret_cast<volatile int32_t *>(&sm.sched[u].valid)) break;
-                if (!bwait(&sm.cb_empty, (v & 1) ^ 1, sm, hdr, epoch)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ba = smem_u32(sm.bc[u][0]), ca = smem_u32(sm.bc[u][2]);
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
-                    mma_ss(tmem + kColCB, desc_sw128(ca + off, 16, 1024), desc_sw128(ba + off, 16, 1024), idCB, s > 0);
-                }
-                mma_commit(&sm.cb_full);
-                for (int hh = 0; hh < hs; ++hh, ++hc) {
-                    const uint32_t k = hc & 1, n = hc >> 1;
-                    if (!bwait(&sm.p_full[k], n & 1, sm, hdr, epoch) ||
-                        !bwait(&sm.s_free[k], (n & 1) ^ 1, sm, hdr, epoch)) {
-                        ok = false;
-                        break;
-                    }
+            const uint32_t uhs = (uint32_t)hs;
+            uint32_t v_cb = 0;                // next unit whose CB is due
+            uint32_t h1 = 0, h2 = 0;          // next head for MMA1 / for C.S (h2 <= h1)
+            uint32_t end_heads = 0xffffffffu; // total heads, once the end-of-work unit is seen
+            uint64_t idle_since = globaltimer();
+            const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
+            for (uint32_t spin = 0;; ++spin) {
+                bool progress = false;
+                // C.S of head h2: y_inter = C . S_in
+                if (h2 < h1 && mbar_try_wait_ns(&sm.sin_full[h2 & 1], (h2 >> 1) & 1, 64)) {
+                    const uint32_t k = h2 & 1, vu = h2 / uhs, u = vu & 1;
                     tc_fence_after();
+                    const uint32_t ca = smem_u32(sm.bc[u][2]), sa = smem_u32(sm.xs[k]);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
+                        mma_ss(tmem + kColP + 64 * k, desc_sw128(ca + off, 16, 1024),
+                               desc_sw128(sa + 2048 * s, 8192, 1024), idCS, s > 0);
+                    }
+                    mma_commit(&sm.mma2[k]);
+                    if (h2 % uhs == uhs - 1) mma_commit(&sm.bc_empty[u]);  // last reader of the unit's B/C
+                    TRACE(1, (3u << 24) | h2);
+                    ++h2;
+                    progress = true;
+                }
+                if (end_heads != 0xffffffffu && h2 == end_heads) break;
+                // CB of unit v_cb, due when MMA1 has reached its first head
+                if (end_heads == 0xffffffffu && h1 == v_cb * uhs &&
+                    mbar_test_wait(&sm.bc_conv[v_cb & 1], (v_cb >> 1) & 1)) {
+                    const uint32_t u = v_cb & 1;
+                    if (!*reinterpret_cast<volatile int32_t *>(&sm.sched[u].valid)) {
+                        end_heads = v_cb * uhs;
+                        progress = true;
+                    } else if (mbar_test_wait(&sm.cb_empty, (v_cb & 1) ^ 1)) {
+                        tc_fence_after();
+                        const uint32_t ba = smem_u32(sm.bc[u][0]), ca = smem_u32(sm.bc[u][2]);
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
+                            mma_ss(tmem + kColCB, desc_sw128(ca + off, 16, 1024), desc_sw128(ba + off, 16, 1024),
+                                   idCB, s > 0);
+                        }
+                        mma_commit(&sm.cb_full);
+                        TRACE(1, (1u << 24) | v_cb);
+                        ++v_cb;
+                        progress = true;
+                    }
+                }
+                // MMA1 of head h1: y_intra = P . x and s = B^T . X_s
+                if (h1 < v_cb * uhs && mbar_try_wait_ns(&sm.p_full[h1 & 1], (h1 >> 1) & 1, 64) &&
+                    mbar_test_wait(&sm.s_free[h1 & 1], ((h1 >> 1) & 1) ^ 1)) {
+                    const uint32_t k = h1 & 1, u = (h1 / uhs) & 1;
+                    tc_fence_after();
+                    const uint32_t ba = smem_u32(sm.bc[u][0]);
                     const uint32_t xa = smem_u32(sm.x[k]), xsa = smem_u32(sm.xs[k]);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
@@ -317,18 +500,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                desc_sw128(xsa + 2048 * s, 8192, 1024), idST, s > 0);
                     mma_commit(&sm.mma1[k]);
                     mma_commit(&sm.x_empty[k]);
-                    if (pend && !issue_cs(pk, pn, pu, plast)) {
-                        ok = false;
+                    TRACE(1, (2u << 24) | h1);
+                    ++h1;
+                    progress = true;
+                }
+                if (progress) {
+                    idle_since = globaltimer();
+                } else if ((spin & 15u) == 15u) {
+                    if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) break;
+                    if (globaltimer() - idle_since > limit) {
+                        pipe_timeout(sm, hdr, epoch);
                         break;
                     }
-                    pend = true;
-                    pk = k;
-                    pn = n;
-                    pu = u;
-                    plast = hh == hs - 1;
                 }
             }
-            if (ok && pend) issue_cs(pk, pn, pu, plast);
             // drain: every MMA issued above has completed before TMEM is released
             mma_commit(&sm.drain);
             const uint64_t t0 = globaltimer();
@@ -352,18 +537,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         auto epilogue = [&]() -> bool {
             if (!bwait(&sm.mma2[pk], pn & 1, sm, hdr, epoch)) return false;
+            if (leader) TRACE(2, (6u << 24) | (pn * 2 + pk));
             tc_fence_after();
+            uint32_t a[2][16], c2[2][16];
+            tmem_ld16(tmem + lrow + kColYI + 64 * pk, a[0]);
+            tmem_ld16(tmem + lrow + kColP + 64 * pk, c2[0]);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                uint32_t a[16], c2[16];
-                tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * m, a);
-                tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * m, c2);
                 tmem_ld_wait();
+                if (m + 1 < 4) {  // next 16 columns in flight while this block is combined and stored
+                    tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * (m + 1), a[(m + 1) & 1]);
+                    tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * (m + 1), c2[(m + 1) & 1]);
+                }
                 uint32_t o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float y0 = __uint_as_float(a[2 * e]) + pecs * __uint_as_float(c2[2 * e]);
-                    const float y1 = __uint_as_float(a[2 * e + 1]) + pecs * __uint_as_float(c2[2 * e + 1]);
+                    const float y0 = __uint_as_float(a[m & 1][2 * e]) + pecs * __uint_as_float(c2[m & 1][2 * e]);
+                    const float y1 =
+                        __uint_as_float(a[m & 1][2 * e + 1]) + pecs * __uint_as_float(c2[m & 1][2 * e + 1]);
                     o[e] = pack_io<IO>(y0, y1);
                 }
                 if (pvalid) {
@@ -372,72 +563,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                 }
             }
+            if (leader) TRACE(2, (7u << 24) | (pn * 2 + pk));
             return true;
         };
         for (uint32_t v = 0; ok; ++v) {
             const uint32_t u = v & 1, nn = v >> 1;
-            if (!bwait(&sm.bc_full[u], nn & 1, sm, hdr, epoch)) {
+            if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) {
                 ok = false;
                 break;
             }
             const Sched sc = sm.sched[u];
-            if (!sc.valid) {
-                if (leader) mbar_arrive(&sm.bc_conv[u]);
-                break;
-            }
-            // (1) bf16 -> fp16 in place for the B and C tiles (same 16-bit positions, same swizzle)
-            if (kBf16) {
-#pragma unroll
-                for (int reg = 0; reg < 4; ++reg) {
-                    uint8_t *row = sm.bc[u][reg] + i * 128;
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) {
-                        uint8_t *ad = row + ((lc ^ (i & 7)) << 4);
-                        uint4 w = lds128(ad);
-                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_io<IO>(wv[e]);
-                            wv[e] = pack_f16(f.x, f.y);
-                        }
-                        sts128(ad, w);
-                    }
-                }
-            }
-            // (2) chunk cumsum: dt = softplus(dt_raw + dt_bias), inclusive scan of dt*A over the 128 rows
-            float dtv[kMaxHs], scn[kMaxHs];
-#pragma unroll
-            for (int hh = 0; hh < kMaxHs; ++hh) {
-                if (hh < hs) {
-                    const int h = sc.h0 + hh;
-                    dtv[hh] = softplus_f32(sm.cs2[u][hh][i] + p.dt_bias[h]);
-                    float s = dtv[hh] * p.A[h];
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float w = __shfl_up_sync(0xffffffffu, s, o);
-                        if (lane >= o) s += w;
-                    }
-                    scn[hh] = s;
-                    if (lane == 31) sm.wsum[q][hh] = s;
-                }
-            }
-            bar_sync(kBarMath, 128);
-#pragma unroll
-            for (int hh = 0; hh < kMaxHs; ++hh) {
-                if (hh < hs) {
-                    float pre = 0.f;
-                    for (int qq = 0; qq < q; ++qq) pre += sm.wsum[qq][hh];
-                    sm.cs2[u][hh][i] = (scn[hh] + pre) * kLog2e;
-                    sm.dt[u][hh][i] = dtv[hh];
-                }
-            }
-            bar_sync(kBarMath, 128);
-#pragma unroll
-            for (int hh = 0; hh < kMaxHs; ++hh)
-                if (hh < hs) sm.wt[u][hh][i] = ex2(sm.cs2[u][hh][i | 31] - sm.cs2[u][hh][i]) * sm.dt[u][hh][i];
-            fence_proxy_async_smem();
-            bar_sync(kBarMath, 128);
-            if (leader) mbar_arrive(&sm.bc_conv[u]);
+            if (!sc.valid) break;
+            if (leader) TRACE(2, (1u << 24) | v);
 
             // (3) per head: X_s, P, then the previous head's epilogue
             for (int hh = 0; hh < hs; ++hh, ++hc) {
@@ -447,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                if (leader) TRACE(2, (2u << 24) | hc);
                 const float cs2i = sm.cs2[u][hh][i];
                 const float xscale = ex2(sm.cs2[u][hh][kQ - 1] - cs2i) * sm.dt[u][hh][i];
                 {
@@ -469,7 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sts128(sr + off, s4);
                     }
                 }
+                if (leader) TRACE(2, (8u << 24) | hc);
                 fence_proxy_async_smem();
+                if (leader) TRACE(2, (5u << 24) | hc);
                 if (hh == 0) {
                     if (!bwait(&sm.cb_full, v & 1, sm, hdr, epoch)) {
                         ok = false;
@@ -478,10 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                 }
                 // P = CB o decay o dt (+ D on the diagonal), masked above the diagonal, fp16 into TMEM
-                const float Dh = p.D ? p.D[h] : 0.f;
+                const float Dh = sm.dskip[u][hh];
                 const float *cs2r = sm.cs2[u][hh];
                 const float *dtr = sm.dt[u][hh];
                 const float *wtr = sm.wt[u][hh];
+                // CB blocks J <= q are loaded one block ahead of their use (one tcgen05.wait::ld per block)
+                uint32_t cb[2][32];
+                tmem_ld16(tmem + lrow + kColCB, *reinterpret_cast<uint32_t(*)[16]>(&cb[0][0]));
+                tmem_ld16(tmem + lrow + kColCB + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[0][16]));
 #pragma unroll
                 for (int J = 0; J < 4; ++J) {
                     uint32_t pk16[16];
@@ -489,26 +633,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) pk16[e] = 0u;
                     } else {
-                        uint32_t cb[32];
-                        tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
-                        tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
                         tmem_ld_wait();
+                        if (leader) TRACE(2, ((9u + J) << 24) | hc);
+                        if (J + 1 <= q) {
+                            tmem_ld16(tmem + lrow + kColCB + 32 * (J + 1),
+                                      *reinterpret_cast<uint32_t(*)[16]>(&cb[(J + 1) & 1][0]));
+                            tmem_ld16(tmem + lrow + kColCB + 32 * (J + 1) + 16,
+                                      *reinterpret_cast<uint32_t(*)[16]>(&cb[(J + 1) & 1][16]));
+                        }
+                        const uint32_t *cbj = cb[J & 1];
                         if (J < q) {
                             // below the diagonal block: exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j),
                             // a = last row of block J; both factors <= 1
                             const float ui = ex2(cs2i - cs2r[32 * J + 31]);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
-                                const float v0 = __uint_as_float(cb[2 * e]) * ui * wtr[32 * J + 2 * e];
-                                const float v1 = __uint_as_float(cb[2 * e + 1]) * ui * wtr[32 * J + 2 * e + 1];
+                                const float v0 = __uint_as_float(cbj[2 * e]) * ui * wtr[32 * J + 2 * e];
+                                const float v1 = __uint_as_float(cbj[2 * e + 1]) * ui * wtr[32 * J + 2 * e + 1];
                                 pk16[e] = pack_f16(v0, v1);
                             }
                         } else {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const int j0 = 32 * J + 2 * e, j1 = j0 + 1;
-                                float v0 = __uint_as_float(cb[2 * e]) * ex2(cs2i - cs2r[j0]) * dtr[j0];
-                                float v1 = __uint_as_float(cb[2 * e + 1]) * ex2(cs2i - cs2r[j1]) * dtr[j1];
+                                float v0 = __uint_as_float(cbj[2 * e]) * ex2(cs2i - cs2r[j0]) * dtr[j0];
+                                float v1 = __uint_as_float(cbj[2 * e + 1]) * ex2(cs2i - cs2r[j1]) * dtr[j1];
                                 v0 = j0 < i ? v0 : (j0 == i ? v0 + Dh : 0.f);
                                 v1 = j1 < i ? v1 : (j1 == i ? v1 + Dh : 0.f);
                                 pk16[e] = pack_f16(v0, v1);
@@ -518,11 +667,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(tmem + lrow + kColP + 64 * k + 16 * J, pk16);
                 }
                 tmem_st_wait();
+                if (leader) TRACE(2, (13u << 24) | hc);
                 tc_fence_before();
                 bar_sync(kBarMath, 128);
+                if (leader) TRACE(2, (14u << 24) | hc);
                 if (leader) {
                     mbar_arrive(&sm.p_full[k]);
                     if (hh == hs - 1) mbar_arrive(&sm.cb_empty);
+                    TRACE(2, (3u << 24) | hc);
                 }
                 if (pend && !epilogue()) {
                     ok = false;
@@ -539,120 +691,179 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && pend) epilogue();
     } else {
         // ------------------------------------------------------------ chain warpgroup
+        // Thread n owns d_state row n of every state. It publishes its own row with its own
+        // release flag (a 64-bit tag epoch:chunk in a 2-slot ring per chain), so neither side of a
+        // hop needs a CTA barrier; and it prefetches the next head's entering state before that
+        // release, so the release's wait for the row's stores overlaps the prefetch loads.
         const int q = warp & 3;
         const int nrow = 32 * q + lane;  // state row (d_state index) owned by this thread
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
-        const bool leader = warp == 6 && lane == 0;
         const uint64_t limit = hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs;
         const int64_t skip = hdr->skip_publish - 1;
         const ST *init = static_cast<const ST *>(p.init);
         ST *fin = static_cast<ST *>(p.final_states);
         ST *ring = static_cast<ST *>(p.ring);
+        uint64_t *tags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]
+        float S[kP];          // entering state of the current head (fp32)
+        uint4 Sraw[kP / 8];   // fp16 states: the raw prefetched row, unpacked at use
+        bool have_S = false;  // the current head's entering state is (being) loaded into registers
+        Sched sc;
+        uint32_t v = 0;
+        int hh = 0;
+        auto enter_unit = [&](uint32_t vv) -> bool {
+            const uint32_t uu = vv & 1;
+            if (!bwait(&sm.bc_conv[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
+            sc = sm.sched[uu];
+            return sc.valid != 0;
+        };
+        // Load row nrow of the state entering chunk c of `chain`. Without `block` it only loads when the
+        // producer's tag is already visible and returns whether it did.
+        auto fetch = [&](int64_t chain, int c, bool block) -> bool {
+            if (c == 0) {
+#pragma unroll
+                for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                if (sizeof(ST) == 2) {
+#pragma unroll
+                    for (int m = 0; m < kP / 8; ++m)
+                        Sraw[m] = make_uint4(pack_f16(S[8 * m], S[8 * m + 1]), pack_f16(S[8 * m + 2], S[8 * m + 3]),
+                                             pack_f16(S[8 * m + 4], S[8 * m + 5]), pack_f16(S[8 * m + 6], S[8 * m + 7]));
+                }
+                return true;
+            }
+            const uint64_t *tag = tags + (chain * 2 + (c & 1)) * kN + nrow;
+            const uint64_t want = ((uint64_t)epoch << 32) | (uint32_t)c;
+            if (ld_acquire_u64(tag) != want) {
+                if (!block) return false;
+                if (aborted(hdr, epoch) || !wait_tag(tag, want, epoch, hdr, limit, (uint32_t)c)) {
+#pragma unroll
+                    for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+#pragma unroll
+                    for (int m = 0; m < kP / 8; ++m) Sraw[m] = make_uint4(0, 0, 0, 0);
+                    return true;  // the error is recorded; carry on with zeros so the CTA drains
+                }
+            }
+            const ST *slot = ring + (chain * 2 + (c & 1)) * (int64_t)(kP * kN);
+            if (sizeof(ST) == 4) {
+                const float4 *src = reinterpret_cast<const float4 *>(slot);
+#pragma unroll
+                for (int m = 0; m < kP / 4; ++m) {
+                    const float4 f = __ldcg(src + m * kN + nrow);
+                    S[4 * m] = f.x;
+                    S[4 * m + 1] = f.y;
+                    S[4 * m + 2] = f.z;
+                    S[4 * m + 3] = f.w;
+                }
+            } else {
+                const uint4 *src = reinterpret_cast<const uint4 *>(slot);
+#pragma unroll
+                for (int m = 0; m < kP / 8; ++m) Sraw[m] = __ldcg(src + m * kN + nrow);
+            }
+            return true;
+        };
+        bool more = enter_unit(0);
+        int64_t chain = 0;
+        int c = 0;
+        if (more) {
+            chain = (int64_t)sc.b * p.H + sc.h0;
+            c = sc.c;
+            have_S = fetch(chain, c, false);
+        }
         uint32_t hc = 0;
-        bool ok = true;
-        for (uint32_t v = 0; ok; ++v) {
-            const uint32_t u = v & 1, nn = v >> 1;
-            if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) break;
-            const Sched sc = sm.sched[u];
-            if (!sc.valid) break;
-            for (int hh = 0; hh < hs; ++hh, ++hc) {
-                const uint32_t k = hc & 1, n = hc >> 1;
-                const int64_t chain = (int64_t)sc.b * p.H + sc.h0 + hh;
-                if (!bwait(&sm.mma1[k], n & 1, sm, hdr, epoch)) {
-                    ok = false;
-                    break;
+        while (more) {
+            const uint32_t k = hc & 1, n = hc >> 1;
+            // chunk state s_c from TMEM
+            if (!bwait(&sm.mma1[k], n & 1, sm, hdr, epoch)) break;
+            tc_fence_after();
+            float s[kP];
+            {
+                uint32_t r[4][16];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) tmem_ld16(tmem + lrow + kColS + 64 * k + 16 * m, r[m]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) s[16 * m + e] = __uint_as_float(r[m][e]);
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.s_free[k]);
+            if (warp == 6 && lane == 0) TRACE(3, (1u << 24) | hc);
+            const float a = ex2(sm.cs2[v & 1][hh][kQ - 1]);  // decay across the chunk
+            // state entering the chunk
+            if (!have_S) fetch(chain, c, true);
+            if (sizeof(ST) == 2) {
+#pragma unroll
+                for (int m = 0; m < kP / 8; ++m) {
+                    const uint32_t wv[4] = {Sraw[m].x, Sraw[m].y, Sraw[m].z, Sraw[m].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_f16(wv[e]);
+                        S[8 * m + 2 * e] = f.x;
+                        S[8 * m + 2 * e + 1] = f.y;
+                    }
                 }
-                tc_fence_after();
-                float s[kP];
+            }
+            // state leaving the chunk: S_out = a S_in + s (kept in s[])
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem + lrow + kColS + 64 * k + 16 * m, r);
-                    tmem_ld_wait();
+            for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
+            const bool publish = c != p.nc - 1 && c != skip;
+            if (c == p.nc - 1) {
+                if (fin) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) s[16 * m + e] = __uint_as_float(r[e]);
+                    for (int pp = 0; pp < kP; ++pp) fin[(chain * kP + pp) * kN + nrow] = from_f32<ST>(s[pp]);
                 }
-                tc_fence_before();
-                bar_sync(kBarChain, 128);
-                if (leader) mbar_arrive(&sm.s_free[k]);
-                const float a = ex2(sm.cs2[u][hh][kQ - 1]);  // decay across the chunk
-                float S[kP];
-                if (sc.c == 0) {
+            } else if (publish) {
+                ST *slot = ring + (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP * kN);
+                if (sizeof(ST) == 4) {
+                    float4 *dst = reinterpret_cast<float4 *>(slot);
 #pragma unroll
-                    for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                    for (int m = 0; m < kP / 4; ++m)
+                        __stcg(dst + m * kN + nrow, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
                 } else {
-                    const bool got = !aborted(hdr, epoch) &&
-                                     wait_flag(&p.flags[chain * p.nc + sc.c - 1], epoch, hdr, limit, 0, sc.c);
-                    const ST *slot = ring + (chain * 2 + (sc.c & 1)) * (int64_t)(kP * kN);
-                    if (got) {
-                        if (sizeof(ST) == 4) {
-                            const float4 *src = reinterpret_cast<const float4 *>(slot);
+                    uint4 *dst = reinterpret_cast<uint4 *>(slot);
 #pragma unroll
-                            for (int m = 0; m < kP / 4; ++m) {
-                                const float4 f = __ldcg(src + m * kN + nrow);
-                                S[4 * m] = f.x;
-                                S[4 * m + 1] = f.y;
-                                S[4 * m + 2] = f.z;
-                                S[4 * m + 3] = f.w;
-                            }
-                        } else {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(slot);
-#pragma unroll
-                            for (int m = 0; m < kP / 8; ++m) {
-                                const uint4 w = __ldcg(src + m * kN + nrow);
-                                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 f = unpack_f16(wv[e]);
-                                    S[8 * m + 2 * e] = f.x;
-                                    S[8 * m + 2 * e + 1] = f.y;
-                                }
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
-                    }
+                    for (int m = 0; m < kP / 8; ++m)
+                        __stcg(dst + m * kN + nrow,
+                               make_uint4(pack_f16(s[8 * m], s[8 * m + 1]), pack_f16(s[8 * m + 2], s[8 * m + 3]),
+                                          pack_f16(s[8 * m + 4], s[8 * m + 5]), pack_f16(s[8 * m + 6], s[8 * m + 7])));
                 }
-                // S_out = a S_in + s (kept in s[])
+            }
+            // S_in (fp16) -> the C.S operand: K-row nrow of a [128 x 64] MN-major 128B-swizzled tile
+            {
+                uint8_t *row = sm.xs[k] + nrow * 128;
 #pragma unroll
-                for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
-                if (sc.c == p.nc - 1) {
-                    if (fin) {
-#pragma unroll
-                        for (int pp = 0; pp < kP; ++pp) fin[(chain * kP + pp) * kN + nrow] = from_f32<ST>(s[pp]);
-                    }
-                } else if (sc.c != skip) {
-                    ST *slot = ring + (chain * 2 + ((sc.c + 1) & 1)) * (int64_t)(kP * kN);
-                    if (sizeof(ST) == 4) {
-                        float4 *dst = reinterpret_cast<float4 *>(slot);
-#pragma unroll
-                        for (int m = 0; m < kP / 4; ++m)
-                            __stcg(dst + m * kN + nrow, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(slot);
-#pragma unroll
-                        for (int m = 0; m < kP / 8; ++m)
-                            __stcg(dst + m * kN + nrow,
-                                   make_uint4(pack_f16(s[8 * m], s[8 * m + 1]), pack_f16(s[8 * m + 2], s[8 * m + 3]),
-                                              pack_f16(s[8 * m + 4], s[8 * m + 5]), pack_f16(s[8 * m + 6], s[8 * m + 7])));
-                    }
-                    __threadfence();
-                    bar_sync(kBarChain, 128);
-                    if (leader) st_release_gpu(&p.flags[chain * p.nc + sc.c], epoch);
+                for (int lc = 0; lc < 8; ++lc)
+                    sts128(row + ((lc ^ (nrow & 7)) << 4),
+                           make_uint4(pack_f16(S[8 * lc], S[8 * lc + 1]), pack_f16(S[8 * lc + 2], S[8 * lc + 3]),
+                                      pack_f16(S[8 * lc + 4], S[8 * lc + 5]), pack_f16(S[8 * lc + 6], S[8 * lc + 7])));
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.sin_full[k]);
+            if (warp == 6 && lane == 0) TRACE(3, (3u << 24) | hc);
+            // prefetch the next head of this unit, then publish this head's row (the release orders the
+            // row's stores before the tag and waits for them together with the prefetch loads)
+            const int64_t pub_chain = chain;
+            const int pub_c = c;
+            const bool last_in_unit = hh + 1 >= hs;
+            ++hc;
+            have_S = false;
+            if (!last_in_unit) {
+                ++hh;
+                chain = (int64_t)sc.b * p.H + sc.h0 + hh;
+                have_S = fetch(chain, c, false);
+            }
+            if (publish)
+                st_release_u64(tags + (pub_chain * 2 + ((pub_c + 1) & 1)) * kN + nrow,
+                               ((uint64_t)epoch << 32) | (uint32_t)(pub_c + 1));
+            if (last_in_unit) {  // next unit: published first, so a slow schedule cannot delay this hop
+                ++v;
+                hh = 0;
+                more = enter_unit(v);
+                if (more) {
+                    chain = (int64_t)sc.b * p.H + sc.h0;
+                    c = sc.c;
+                    have_S = fetch(chain, c, false);
                 }
-                // S_in (fp16) -> the C.S operand: K-row nrow of a [128 x 64] MN-major 128B-swizzled tile
-                {
-                    uint8_t *row = sm.xs[k] + nrow * 128;
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc)
-                        sts128(row + ((lc ^ (nrow & 7)) << 4),
-                               make_uint4(pack_f16(S[8 * lc], S[8 * lc + 1]), pack_f16(S[8 * lc + 2], S[8 * lc + 3]),
-                                          pack_f16(S[8 * lc + 4], S[8 * lc + 5]), pack_f16(S[8 * lc + 6], S[8 * lc + 7])));
-                }
-                fence_proxy_async_smem();
-                bar_sync(kBarChain, 128);
-                if (leader) mbar_arrive(&sm.sin_full[k]);
             }
         }
     }
@@ -731,6 +942,8 @@ bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype) {
     return P == kP && N == kN && Q == kQ && (io_dtype == 1 || io_dtype == 2);
 }
 
+size_t tc_flag_bytes(int64_t chains) { return (size_t)chains * 2 * kN * sizeof(uint64_t); }
+
 size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
     return (size_t)chains * 2 * (size_t)(P * N) * (state_dtype == 0 ? 4 : 2);
 }
@@ -757,3 +970,12 @@ cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, 
 }
 
 }  // namespace ssd
+
+#ifdef SSD_TRACE
+extern "C" __attribute__((visibility("default"))) int ssd_trace_read(unsigned long long *dst, unsigned int *counts) {
+    if (cudaMemcpyFromSymbol(counts, ssd::g_trace_n, sizeof(ssd::g_trace_n)) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(dst, ssd::g_trace, sizeof(ssd::g_trace)) != cudaSuccess) return -1;
+    static const unsigned int zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(ssd::g_trace_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
+}
+#endif
