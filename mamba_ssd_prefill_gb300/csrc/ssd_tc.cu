@@ -101,18 +101,11 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(const void *p) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(smem_u32(p)));
-    return v;
-}
-__device__ __forceinline__ void sts128(void *p, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
+// Plain C++ shared-memory vector accesses, so the compiler can batch and overlap them; their
+// ordering against TMA, tensor-core reads and barriers comes from those operations' volatile asm
+// (memory clobbers) and from the proxy fences.
+__device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ void sts128(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -195,8 +188,11 @@ template <typename IO, typename ST>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
               const __grid_constant__ CUtensorMap map_c, const int hs) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base (128B-swizzle atoms). Computed as smem_raw + pad, not through an integer
+    // round trip, so the compiler keeps the shared address space and emits LDS/STS for every access.
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw + pad);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader *hdr = p.hdr;
     const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
@@ -258,29 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t uu = vv & 1;
             if (!bwait(&sm.bc_full[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
             if (kBf16) {
+#pragma unroll 1
+                for (int it = 0; it < 16; ++it) {  // 4 tiles x 4 rows per lane
+                    const int row = lane + 32 * (it & 3);
+                    uint8_t *base = sm.bc[uu][it >> 2] + row * 128;
+                    uint4 w[8];
+                    // chunk order rotated by row: the lanes of a quarter-warp hit 8 different bank groups
 #pragma unroll
-                for (int reg = 0; reg < 4; ++reg)
+                    for (int lc = 0; lc < 8; ++lc) w[lc] = lds128(base + ((lc ^ (row & 7)) << 4));
 #pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        const int row = lane + 32 * rr;
-                        uint8_t *base = sm.bc[uu][reg] + row * 128;
+                    for (int lc = 0; lc < 8; ++lc) {
+                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w[lc]);
 #pragma unroll
-                        for (int lc = 0; lc < 8; ++lc) {
-                            uint8_t *ad = base + ((lc ^ (row & 7)) << 4);
-                            uint4 w = lds128(ad);
-                            uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_io<IO>(wv[e]);
-                                wv[e] = pack_f16(f.x, f.y);
-                            }
-                            sts128(ad, w);
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_io<IO>(wv[e]);
+                            wv[e] = pack_f16(f.x, f.y);
                         }
+                        sts128(base + ((lc ^ (row & 7)) << 4), w[lc]);
                     }
+                }
             }
             // chunk cumsum: dt = softplus(dt_raw + dt_bias) (0 past the sequence end), inclusive scan of
             // dt*A over the 128 rows; this lane owns rows 4*lane .. 4*lane+3
-#pragma unroll
+#pragma unroll 1
             for (int hh = 0; hh < kMaxHs; ++hh) {
                 if (hh < hs) {
                     const int h = sc.h0 + hh;
@@ -539,22 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!bwait(&sm.mma2[pk], pn & 1, sm, hdr, epoch)) return false;
             if (leader) TRACE(2, (6u << 24) | (pn * 2 + pk));
             tc_fence_after();
-            uint32_t a[2][16], c2[2][16];
-            tmem_ld16(tmem + lrow + kColYI + 64 * pk, a[0]);
-            tmem_ld16(tmem + lrow + kColP + 64 * pk, c2[0]);
-#pragma unroll
+#pragma unroll 1
             for (int m = 0; m < 4; ++m) {
+                uint32_t a[16], c2[16];
+                tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * m, a);
+                tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * m, c2);
                 tmem_ld_wait();
-                if (m + 1 < 4) {  // next 16 columns in flight while this block is combined and stored
-                    tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * (m + 1), a[(m + 1) & 1]);
-                    tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * (m + 1), c2[(m + 1) & 1]);
-                }
                 uint32_t o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float y0 = __uint_as_float(a[m & 1][2 * e]) + pecs * __uint_as_float(c2[m & 1][2 * e]);
-                    const float y1 =
-                        __uint_as_float(a[m & 1][2 * e + 1]) + pecs * __uint_as_float(c2[m & 1][2 * e + 1]);
+                    const float y0 = __uint_as_float(a[2 * e]) + pecs * __uint_as_float(c2[2 * e]);
+                    const float y1 = __uint_as_float(a[2 * e + 1]) + pecs * __uint_as_float(c2[2 * e + 1]);
                     o[e] = pack_io<IO>(y0, y1);
                 }
                 if (pvalid) {
@@ -590,11 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 {
                     uint8_t *xr = sm.x[k] + i * 128;
                     uint8_t *sr = sm.xs[k] + i * 128;
+                    uint4 w[8];
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) w[lc] = lds128(xr + ((lc ^ (i & 7)) << 4));
 #pragma unroll
                     for (int lc = 0; lc < 8; ++lc) {
                         const int off = (lc ^ (i & 7)) << 4;
-                        uint4 w = lds128(xr + off);
-                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w[lc]);
                         uint4 s4;
                         uint32_t *sv = reinterpret_cast<uint32_t *>(&s4);
 #pragma unroll
@@ -603,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sv[e] = pack_f16(f.x * xscale, f.y * xscale);
                             if (kBf16) wv[e] = pack_f16(f.x, f.y);
                         }
-                        if (kBf16) sts128(xr + off, w);
+                        if (kBf16) sts128(xr + off, w[lc]);
                         sts128(sr + off, s4);
                     }
                 }
@@ -622,45 +615,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *cs2r = sm.cs2[u][hh];
                 const float *dtr = sm.dt[u][hh];
                 const float *wtr = sm.wt[u][hh];
-                // CB blocks J <= q are loaded one block ahead of their use (one tcgen05.wait::ld per block)
-                uint32_t cb[2][32];
-                tmem_ld16(tmem + lrow + kColCB, *reinterpret_cast<uint32_t(*)[16]>(&cb[0][0]));
-                tmem_ld16(tmem + lrow + kColCB + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[0][16]));
-#pragma unroll
+                // One 32-column block of CB per iteration (rolled: keeps the hot code small). Blocks above
+                // the diagonal block are zero; below it exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j)
+                // with a the block's last row (both factors <= 1); the diagonal block takes exp directly.
+#pragma unroll 1
                 for (int J = 0; J < 4; ++J) {
                     uint32_t pk16[16];
                     if (J > q) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) pk16[e] = 0u;
                     } else {
+                        uint32_t cb[32];
+                        tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
+                        tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
                         tmem_ld_wait();
                         if (leader) TRACE(2, ((9u + J) << 24) | hc);
-                        if (J + 1 <= q) {
-                            tmem_ld16(tmem + lrow + kColCB + 32 * (J + 1),
-                                      *reinterpret_cast<uint32_t(*)[16]>(&cb[(J + 1) & 1][0]));
-                            tmem_ld16(tmem + lrow + kColCB + 32 * (J + 1) + 16,
-                                      *reinterpret_cast<uint32_t(*)[16]>(&cb[(J + 1) & 1][16]));
-                        }
-                        const uint32_t *cbj = cb[J & 1];
                         if (J < q) {
-                            // below the diagonal block: exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j),
-                            // a = last row of block J; both factors <= 1
                             const float ui = ex2(cs2i - cs2r[32 * J + 31]);
+                            const float4 *w4 = reinterpret_cast<const float4 *>(wtr + 32 * J);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float v0 = __uint_as_float(cbj[2 * e]) * ui * wtr[32 * J + 2 * e];
-                                const float v1 = __uint_as_float(cbj[2 * e + 1]) * ui * wtr[32 * J + 2 * e + 1];
-                                pk16[e] = pack_f16(v0, v1);
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 wv = w4[e];
+                                pk16[2 * e] = pack_f16(__uint_as_float(cb[4 * e]) * ui * wv.x,
+                                                       __uint_as_float(cb[4 * e + 1]) * ui * wv.y);
+                                pk16[2 * e + 1] = pack_f16(__uint_as_float(cb[4 * e + 2]) * ui * wv.z,
+                                                           __uint_as_float(cb[4 * e + 3]) * ui * wv.w);
                             }
                         } else {
+                            const float4 *c4 = reinterpret_cast<const float4 *>(cs2r + 32 * J);
+                            const float4 *d4 = reinterpret_cast<const float4 *>(dtr + 32 * J);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int j0 = 32 * J + 2 * e, j1 = j0 + 1;
-                                float v0 = __uint_as_float(cbj[2 * e]) * ex2(cs2i - cs2r[j0]) * dtr[j0];
-                                float v1 = __uint_as_float(cbj[2 * e + 1]) * ex2(cs2i - cs2r[j1]) * dtr[j1];
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 cv = c4[e], dv = d4[e];
+                                const int j0 = 32 * J + 4 * e;
+                                float v0 = __uint_as_float(cb[4 * e]) * ex2(cs2i - cv.x) * dv.x;
+                                float v1 = __uint_as_float(cb[4 * e + 1]) * ex2(cs2i - cv.y) * dv.y;
+                                float v2 = __uint_as_float(cb[4 * e + 2]) * ex2(cs2i - cv.z) * dv.z;
+                                float v3 = __uint_as_float(cb[4 * e + 3]) * ex2(cs2i - cv.w) * dv.w;
                                 v0 = j0 < i ? v0 : (j0 == i ? v0 + Dh : 0.f);
-                                v1 = j1 < i ? v1 : (j1 == i ? v1 + Dh : 0.f);
-                                pk16[e] = pack_f16(v0, v1);
+                                v1 = j0 + 1 < i ? v1 : (j0 + 1 == i ? v1 + Dh : 0.f);
+                                v2 = j0 + 2 < i ? v2 : (j0 + 2 == i ? v2 + Dh : 0.f);
+                                v3 = j0 + 3 < i ? v3 : (j0 + 3 == i ? v3 + Dh : 0.f);
+                                pk16[2 * e] = pack_f16(v0, v1);
+                                pk16[2 * e + 1] = pack_f16(v2, v3);
                             }
                         }
                     }
