@@ -140,8 +140,8 @@ __device__ __noinline__ void chain_timeout(WsHeader *hdr, uint32_t epoch, uint32
 }
 
 // Bounded wait until *tag == want (acquire). On timeout records SSD_ERR_TIMEOUT and returns false;
-// returns false at once when another CTA aborted the launch.
-__device__ __forceinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
+// returns false at once when another CTA aborted the launch. Out of line: it is the slow path.
+__device__ __noinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
                                          uint64_t limit_ns, uint32_t chunk) {
     const uint64_t t0 = globaltimer();
     uint32_t sleep_ns = 20;
@@ -168,9 +168,9 @@ __device__ __noinline__ void pipe_timeout(Smem &sm, WsHeader *hdr, uint32_t epoc
 // other wait then gives up too and the CTA drains to its teardown. Its limit
 // is four times the state-passing limit plus 100 ms: a pipeline stage may
 // legitimately sit behind one full state-passing wait, which must time out
-// (and report itself) first. Inline: only the timeout report is a call.
-__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
-    if (mbar_try_wait(bar, parity)) return true;
+// (and report itself) first. Only the first probe is inline: the polling loop
+// is one out-of-line copy, so the hot code of every role stays small.
+__device__ __noinline__ bool bwait_slow(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -182,6 +182,9 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, 
     }
     pipe_timeout(sm, hdr, epoch);
     return false;
+}
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
+    return mbar_try_wait(bar, parity) || bwait_slow(bar, parity, sm, hdr, epoch);
 }
 
 template <typename IO, typename ST>
@@ -713,32 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sc = sm.sched[uu];
             return sc.valid != 0;
         };
-        // Load row nrow of the state entering chunk c of `chain`. Without `block` it only loads when the
-        // producer's tag is already visible and returns whether it did.
-        auto fetch = [&](int64_t chain, int c, bool block) -> bool {
-            if (c == 0) {
-#pragma unroll
-                for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
-                if (sizeof(ST) == 2) {
-#pragma unroll
-                    for (int m = 0; m < kP / 8; ++m)
-                        Sraw[m] = make_uint4(pack_f16(S[8 * m], S[8 * m + 1]), pack_f16(S[8 * m + 2], S[8 * m + 3]),
-                                             pack_f16(S[8 * m + 4], S[8 * m + 5]), pack_f16(S[8 * m + 6], S[8 * m + 7]));
-                }
-                return true;
-            }
-            const uint64_t *tag = tags + (chain * 2 + (c & 1)) * kN + nrow;
-            const uint64_t want = ((uint64_t)epoch << 32) | (uint32_t)c;
-            if (ld_acquire_u64(tag) != want) {
-                if (!block) return false;
-                if (aborted(hdr, epoch) || !wait_tag(tag, want, epoch, hdr, limit, (uint32_t)c)) {
-#pragma unroll
-                    for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
-#pragma unroll
-                    for (int m = 0; m < kP / 8; ++m) Sraw[m] = make_uint4(0, 0, 0, 0);
-                    return true;  // the error is recorded; carry on with zeros so the CTA drains
-                }
-            }
+        // Row nrow of the state entering chunk c > 0 of `chain`, from the ring (the caller has seen its tag).
+        auto load_ring = [&](int64_t chain, int c) {
             const ST *slot = ring + (chain * 2 + (c & 1)) * (int64_t)(kP * kN);
             if (sizeof(ST) == 4) {
                 const float4 *src = reinterpret_cast<const float4 *>(slot);
@@ -755,6 +734,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int m = 0; m < kP / 8; ++m) Sraw[m] = __ldcg(src + m * kN + nrow);
             }
+        };
+        auto tag_of = [&](int64_t chain, int c) { return tags + (chain * 2 + (c & 1)) * kN + nrow; };
+        auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
+        // Prefetch: load the entering state now when its producer's tag is already visible.
+        auto prefetch = [&](int64_t chain, int c) -> bool {
+            if (c == 0 || ld_acquire_u64(tag_of(chain, c)) != want_of(c)) return false;
+            load_ring(chain, c);
             return true;
         };
         bool more = enter_unit(0);
@@ -763,7 +749,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (more) {
             chain = (int64_t)sc.b * p.H + sc.h0;
             c = sc.c;
-            have_S = fetch(chain, c, false);
         }
         uint32_t hc = 0;
         while (more) {
@@ -787,7 +772,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 6 && lane == 0) TRACE(3, (1u << 24) | hc);
             const float a = ex2(sm.cs2[v & 1][hh][kQ - 1]);  // decay across the chunk
             // state entering the chunk
-            if (!have_S) fetch(chain, c, true);
+            if (!have_S) {
+                if (c == 0) {
+#pragma unroll
+                    for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                    if (sizeof(ST) == 2) {
+#pragma unroll
+                        for (int m = 0; m < kP / 8; ++m)
+                            Sraw[m] = make_uint4(pack_f16(S[8 * m], S[8 * m + 1]), pack_f16(S[8 * m + 2], S[8 * m + 3]),
+                                                 pack_f16(S[8 * m + 4], S[8 * m + 5]),
+                                                 pack_f16(S[8 * m + 6], S[8 * m + 7]));
+                    }
+                } else if ((ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
+                            (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c)))) {
+                    load_ring(chain, c);
+                } else {  // the error is recorded; carry on with zeros so the CTA drains
+#pragma unroll
+                    for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+#pragma unroll
+                    for (int m = 0; m < kP / 8; ++m) Sraw[m] = make_uint4(0, 0, 0, 0);
+                }
+            }
             if (sizeof(ST) == 2) {
 #pragma unroll
                 for (int m = 0; m < kP / 8; ++m) {
@@ -837,31 +842,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             mbar_arrive(&sm.sin_full[k]);
             if (warp == 6 && lane == 0) TRACE(3, (3u << 24) | hc);
-            // prefetch the next head of this unit, then publish this head's row (the release orders the
-            // row's stores before the tag and waits for them together with the prefetch loads)
-            const int64_t pub_chain = chain;
-            const int pub_c = c;
-            const bool last_in_unit = hh + 1 >= hs;
-            ++hc;
-            have_S = false;
-            if (!last_in_unit) {
-                ++hh;
-                chain = (int64_t)sc.b * p.H + sc.h0 + hh;
-                have_S = fetch(chain, c, false);
-            }
+            // publish this head's row (the release orders the row's stores before the tag), then move to
+            // the next head and prefetch its entering state
             if (publish)
-                st_release_u64(tags + (pub_chain * 2 + ((pub_c + 1) & 1)) * kN + nrow,
-                               ((uint64_t)epoch << 32) | (uint32_t)(pub_c + 1));
-            if (last_in_unit) {  // next unit: published first, so a slow schedule cannot delay this hop
+                st_release_u64(tags + (chain * 2 + ((c + 1) & 1)) * kN + nrow,
+                               ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
+            ++hc;
+            if (hh + 1 < hs) {
+                ++hh;
+                ++chain;
+            } else {
                 ++v;
                 hh = 0;
                 more = enter_unit(v);
-                if (more) {
-                    chain = (int64_t)sc.b * p.H + sc.h0;
-                    c = sc.c;
-                    have_S = fetch(chain, c, false);
-                }
+                if (!more) break;
+                chain = (int64_t)sc.b * p.H + sc.h0;
+                c = sc.c;
             }
+            have_S = prefetch(chain, c);
         }
     }
 
