@@ -619,8 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *dtr = sm.dt[u][hh];
                 const float *wtr = sm.wt[u][hh];
                 // One 32-column block of CB per iteration (rolled: keeps the hot code small). Blocks above
-                // the diagonal block are zero; below it exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j)
-                // with a the block's last row (both factors <= 1); the diagonal block takes exp directly.
+                // the diagonal block are zero. Elsewhere exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j)
+                // with a the block's last row: below the diagonal block both factors are <= 1; in the
+                // diagonal block the first is >= 1, so it is used only while the block's whole decay range
+                // keeps it <= 2^100 (warp-uniform test), else the diagonal block takes exp directly. The
+                // shared-memory tables are read before the TMEM load so their latency overlaps it.
 #pragma unroll 1
                 for (int J = 0; J < 4; ++J) {
                     uint32_t pk16[16];
@@ -628,28 +631,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) pk16[e] = 0u;
                     } else {
+                        const bool diag = J == q;
+                        const float ca = cs2r[32 * J + 31];
+                        const bool fac = !diag || cs2r[32 * J] - ca <= 100.f;
+                        float4 t1[8], t2[8];
+                        const float4 *s1 = reinterpret_cast<const float4 *>((fac ? wtr : cs2r) + 32 * J);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t1[e] = s1[e];
+                        if (!fac) {
+                            const float4 *d4 = reinterpret_cast<const float4 *>(dtr + 32 * J);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) t2[e] = d4[e];
+                        }
+                        const float ui = ex2(cs2i - ca);
                         uint32_t cb[32];
                         tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
                         tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
                         tmem_ld_wait();
                         if (leader) TRACE(2, ((9u + J) << 24) | hc);
-                        if (J < q) {
-                            const float ui = ex2(cs2i - cs2r[32 * J + 31]);
-                            const float4 *w4 = reinterpret_cast<const float4 *>(wtr + 32 * J);
+                        if (fac) {
+                            const int lim = diag ? i : (1 << 30);  // columns j < lim are kept; j == i also takes D
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                const float4 wv = w4[e];
-                                pk16[2 * e] = pack_f16(__uint_as_float(cb[4 * e]) * ui * wv.x,
-                                                       __uint_as_float(cb[4 * e + 1]) * ui * wv.y);
-                                pk16[2 * e + 1] = pack_f16(__uint_as_float(cb[4 * e + 2]) * ui * wv.z,
-                                                           __uint_as_float(cb[4 * e + 3]) * ui * wv.w);
+                                const int j0 = 32 * J + 4 * e;
+                                float v0 = __uint_as_float(cb[4 * e]) * ui * t1[e].x;
+                                float v1 = __uint_as_float(cb[4 * e + 1]) * ui * t1[e].y;
+                                float v2 = __uint_as_float(cb[4 * e + 2]) * ui * t1[e].z;
+                                float v3 = __uint_as_float(cb[4 * e + 3]) * ui * t1[e].w;
+                                v0 = j0 < lim ? v0 : (j0 == i ? v0 + Dh : 0.f);
+                                v1 = j0 + 1 < lim ? v1 : (j0 + 1 == i ? v1 + Dh : 0.f);
+                                v2 = j0 + 2 < lim ? v2 : (j0 + 2 == i ? v2 + Dh : 0.f);
+                                v3 = j0 + 3 < lim ? v3 : (j0 + 3 == i ? v3 + Dh : 0.f);
+                                pk16[2 * e] = pack_f16(v0, v1);
+                                pk16[2 * e + 1] = pack_f16(v2, v3);
                             }
                         } else {
-                            const float4 *c4 = reinterpret_cast<const float4 *>(cs2r + 32 * J);
-                            const float4 *d4 = reinterpret_cast<const float4 *>(dtr + 32 * J);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                const float4 cv = c4[e], dv = d4[e];
+                                const float4 cv = t1[e], dv = t2[e];
                                 const int j0 = 32 * J + 4 * e;
                                 float v0 = __uint_as_float(cb[4 * e]) * ex2(cs2i - cv.x) * dv.x;
                                 float v1 = __uint_as_float(cb[4 * e + 1]) * ex2(cs2i - cv.y) * dv.y;

@@ -1,4 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -6,7 +8,7 @@ import torch
 import mamba_ssd_prefill_gb300 as m
 import oracle
 from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs
-from parity import gate_final, gate_y
+from parity import gate_final, gate_y, gate_y_tc_envelope
 
 pytestmark = pytest.mark.gpu
 
@@ -144,6 +146,32 @@ def test_tc_parity_small(name, over):
     y, fin = run_gpu(w, inp, kernel="tc")
     yr, fr = oracle.ssd_reference(**cpu(inp))
     assert_parity(w, y, fin, yr, fr, f"tc {name} {over}")
+
+
+@pytest.mark.parametrize("dt_bias,A", [(-6.0, -0.5), (2.0, -16.0), (0.5, None)],
+                         ids=["weak-decay", "strong-decay", "mixed-decay"])
+def test_decay_regimes(dt_bias, A):
+    """Decay from almost none to total within a few tokens, so both ways of forming the decay mask run:
+    the two-factor split and the direct exponential of the diagonal blocks (decay range over 100 in log2).
+    The strong and mixed cases drive |y| into the hundreds and the states far above 10, well outside the
+    pages' workloads: there the SIMT kernel (fp32 throughout) still meets the gate, and the tensor-core
+    kernel, whose P, X_s and S_in are fp16, is held to its operand envelope."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=777, nheads=6, ngroups=2, seed=77)
+    inp = make_inputs(w, device="cuda")
+    inp["dt_bias"] = torch.full_like(inp["dt_bias"], dt_bias)
+    if A is None:  # per head from -16 to -0.01
+        inp["A"] = -torch.logspace(math.log10(16.0), -2.0, w.nheads, device="cuda", dtype=torch.float32)
+    else:
+        inp["A"] = torch.full_like(inp["A"], A)
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    y, fin = run_gpu(w, inp, kernel="simt")
+    assert_parity(w, y, fin, yr, fr, f"simt decay dt_bias={dt_bias} A={A}")
+    y, fin = run_gpu(w, inp, kernel="tc")
+    if dt_bias < 0:  # inside the pages' regime: the plain gate
+        assert_parity(w, y, fin, yr, fr, f"tc decay dt_bias={dt_bias} A={A}")
+    else:
+        ok, s = gate_y_tc_envelope(y.double().cpu().numpy(), yr)
+        assert ok, f"tc decay dt_bias={dt_bias} A={A}: {s}"
 
 
 @pytest.mark.parametrize("hs", [1, 2, 4, 8])
