@@ -18,8 +18,8 @@
 //   warp 0      unit loader (tickets, dt_raw, B/C tiles by TMA), up to two units ahead
 //   warp 10     x-tile loader (one TMA per head)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2-5   "math": bf16->fp16 tile conversion, cumsum tables, decay mask
-//               P -> TMEM, X_s, epilogue y = y_intra + exp(cs) y_inter
+//   warps 2-5   "math": X_s (and the x tile to fp16), decay mask P -> TMEM, epilogue
+//               y = y_intra + exp(cs) y_inter staged in shared memory, TMA-stored
 //   warps 6-9   "chain": state passing (wait flag, S_in, S_out, publish), S_in
 //               -> shared memory as the C.S operand, final states
 // All MMA operands are fp16 (bf16 inputs are converted on chip; the contractions
@@ -190,7 +190,7 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, 
 template <typename IO, typename ST>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-              const __grid_constant__ CUtensorMap map_c, const int hs) {
+              const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_y, const int hs) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base (128B-swizzle atoms). Computed as smem_raw + pad, not through an integer
     // round trip, so the compiler keeps the shared address space and emits LDS/STS for every access.
@@ -526,18 +526,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = 32 * q + lane;         // tile row (token within the chunk) owned by this thread
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
         const bool leader = warp == 2 && lane == 0;
-        IO *yg = static_cast<IO *>(p.y);
+        if (lane == 0) prefetch_tensormap(&map_y);
         uint32_t hc = 0;
         bool pend = false;
         uint32_t pk = 0, pn = 0;
         float pecs = 0.f;
-        int64_t pbase = 0;
-        bool pvalid = false;
+        int ph = 0, prow = 0, pb = 0;  // y tile of the pending head: head, first token of this warp's rows, batch
         bool ok = true;
+        // y = y_intra + exp(cs_i) y_inter of the pending head, staged in its C.S operand tile (free once C.S
+        // has completed) with the operand's 128B swizzle, then one TMA store per warp of its 32 rows; the
+        // store clips rows past the sequence end.
         auto epilogue = [&]() -> bool {
             if (!bwait(&sm.mma2[pk], pn & 1, sm, hdr, epoch)) return false;
             if (leader) TRACE(2, (6u << 24) | (pn * 2 + pk));
             tc_fence_after();
+            uint8_t *yrow = sm.xs[pk] + i * 128;
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
                 uint32_t a[16], c2[16];
@@ -551,11 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float y1 = __uint_as_float(a[2 * e + 1]) + pecs * __uint_as_float(c2[2 * e + 1]);
                     o[e] = pack_io<IO>(y0, y1);
                 }
-                if (pvalid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(yg + pbase + 16 * m);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                }
+                sts128(yrow + (((2 * m) ^ (i & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+                sts128(yrow + (((2 * m + 1) ^ (i & 7)) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_4d(&map_y, sm.xs[pk] + 32 * q * 128, 0, ph, prow, pb);
+                bulk_commit();
             }
             if (leader) TRACE(2, (7u << 24) | (pn * 2 + pk));
             return true;
@@ -579,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (leader) TRACE(2, (2u << 24) | hc);
+                if (lane == 0) bulk_wait_read0();  // this warp's y store from xs[k] (two heads back) has read it
+                __syncwarp();
                 const float cs2i = sm.cs2[u][hh][i];
                 const float xscale = ex2(sm.cs2[u][hh][kQ - 1] - cs2i) * sm.dt[u][hh][i];
                 {
@@ -703,11 +711,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk = k;
                 pn = n;
                 pecs = ex2(cs2i);
-                pvalid = i < sc.rows;
-                pbase = ((int64_t)sc.b * p.L + (int64_t)sc.c * kQ + i) * p.H * kP + (int64_t)h * kP;
+                ph = h;
+                prow = sc.c * kQ + 32 * q;
+                pb = sc.b;
             }
         }
         if (ok && pend) epilogue();
+        if (lane == 0) bulk_wait0();  // every y store of this warp has completed
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ chain warpgroup
         // Thread n owns d_state row n of every state. It publishes its own row with its own
@@ -919,14 +930,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 4-D map over a [batch, L, mid, inner] 16-bit tensor, box = [1, 128 rows, 1, 64 inner], 128B swizzle.
-bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t L, int64_t batch) {
+// 4-D map over a [batch, L, mid, inner] 16-bit tensor, box = [1, box_rows, 1, 64 inner], 128B swizzle.
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t L, int64_t batch,
+              uint32_t box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
     const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2),
                                    (cuuint64_t)(inner * mid * L * 2)};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kQ, 1};
+    const cuuint32_t box[4] = {64, 1, box_rows, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -936,17 +948,17 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_
 
 template <typename IO, typename ST>
 cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
-    CUtensorMap mx, mb, mc;
+    CUtensorMap mx, mb, mc, my;
     const bool bf = !std::is_same<IO, __half>::value;
-    if (!make_map(&mx, p.x, bf, kP, p.H, p.L, p.batch) || !make_map(&mb, p.B, bf, kN, p.G, p.L, p.batch) ||
-        !make_map(&mc, p.C, bf, kN, p.G, p.L, p.batch))
+    if (!make_map(&mx, p.x, bf, kP, p.H, p.L, p.batch, kQ) || !make_map(&mb, p.B, bf, kN, p.G, p.L, p.batch, kQ) ||
+        !make_map(&mc, p.C, bf, kN, p.G, p.L, p.batch, kQ) || !make_map(&my, p.y, bf, kP, p.H, p.L, p.batch, 32))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem) + 1024;
     auto k = tc_kernel<IO, ST>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
-    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, hs);
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, my, hs);
     return cudaGetLastError();
 }
 
