@@ -59,8 +59,12 @@ typedef enum {
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype_t;
 
 /* Which kernel runs the problem. AUTO picks the tensor-core kernel where it
- * has an instance (bf16/fp16 I/O, headdim 64, dstate 128, chunk 128 or 256)
- * and the fp32 SIMT kernel otherwise. */
+ * has an instance (bf16/fp16 I/O, headdim 64, dstate 128, chunk_size a
+ * multiple of 128) and the fp32 SIMT kernel otherwise. The tensor-core kernel
+ * passes states every 128 tokens whatever multiple of 128 is requested: the
+ * chunked method reaches the recurrence's result exactly for any chunk size
+ * ("Mamba hardware-aware algorithms", structured state space duality), so only
+ * the rounding depends on it. */
 typedef enum { SSD_KERNEL_AUTO = 0, SSD_KERNEL_SIMT = 1, SSD_KERNEL_TC = 2 } ssd_kernel_t;
 
 typedef struct {

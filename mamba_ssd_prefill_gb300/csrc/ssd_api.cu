@@ -36,7 +36,8 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 struct Plan {
     int kernel = 0;          // SSD_KERNEL_SIMT / _TC
-    int64_t nc = 0;          // chunks per sequence
+    int64_t nc = 0;          // chunks per sequence, of exec_chunk tokens
+    int64_t exec_chunk = 0;  // tokens per state-passing step in the chosen kernel
     int heads_per_unit = 1;  // TC only
     uint32_t total_units = 0;
     size_t flags_off = 0, ring_off = 0, bytes = 0;
@@ -61,7 +62,6 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
         return SSD_ERR_INVALID_ARG;
 
     Plan pl;
-    pl.nc = (pr->seqlen + pr->chunk_size - 1) / pr->chunk_size;
     const bool tc_ok = ssd::tc_supports(pr->headdim, pr->dstate, pr->chunk_size, pr->io_dtype);
     const bool simt_ok = ssd::simt_smem_bytes(pr->headdim, pr->dstate) <= 227u * 1024u;
     if (pr->kernel == SSD_KERNEL_TC) {
@@ -78,6 +78,8 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
         else
             return SSD_ERR_UNSUPPORTED;
     }
+    pl.exec_chunk = pl.kernel == SSD_KERNEL_TC ? ssd::tc_chunk() : pr->chunk_size;
+    pl.nc = (pr->seqlen + pl.exec_chunk - 1) / pl.exec_chunk;
     const int64_t chains = pr->batch * pr->nheads;
     double units;
     if (pl.kernel == SSD_KERNEL_TC) {
@@ -180,7 +182,7 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     p.P = pr.headdim;
     p.N = pr.dstate;
     p.G = pr.ngroups;
-    p.Q = pr.chunk_size;
+    p.Q = pl.exec_chunk;
     p.nc = pl.nc;
     p.heads_per_group = pr.nheads / pr.ngroups;
     p.total_units = pl.total_units;

@@ -17,6 +17,7 @@ cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms,
 
 // tcgen05 / TMA kernel (ssd_tc.cu)
 bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype);
+int64_t tc_chunk();  // tokens per state-passing step inside the tensor-core kernel
 size_t tc_flag_bytes(int64_t chains);
 size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype);
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int heads_per_unit);

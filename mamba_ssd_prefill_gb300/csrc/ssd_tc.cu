@@ -964,9 +964,13 @@ cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
 
 }  // namespace
 
+// Any chunk size that is a multiple of 128 runs in 128-token chunks: the chunked result is exact for every
+// chunk size (only its rounding differs), so a larger requested chunk is served by passing states more often.
 bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype) {
-    return P == kP && N == kN && Q == kQ && (io_dtype == 1 || io_dtype == 2);
+    return P == kP && N == kN && Q % kQ == 0 && (io_dtype == 1 || io_dtype == 2);
 }
+
+int64_t tc_chunk() { return kQ; }
 
 size_t tc_flag_bytes(int64_t chains) { return (size_t)chains * 2 * kN * sizeof(uint64_t); }
 

@@ -81,6 +81,10 @@ def test_workspace_size_scales_with_chains(lib):
 
 def test_kernel_selection(lib):
     assert m.kernel_for(prob(io_dtype=torch.float32, dstate=64)) == "simt"
+    assert m.kernel_for(prob()) == "tc"
+    assert m.kernel_for(prob(chunk_size=256)) == "tc"  # served in 128-token chunks
+    assert m.kernel_for(prob(chunk_size=192)) == "simt"
+    assert m.kernel_for(prob(chunk_size=64)) == "simt"
     assert m.kernel_for(prob(kernel="simt")) == "simt"
     # shapes the SIMT kernel cannot hold in shared memory are rejected
     with pytest.raises(m.SsdError) as e:

@@ -136,6 +136,7 @@ TC_SMALL = [
     ("m130-bf16", dict(batch=3, seqlen=1, nheads=2)),                           # one token
     ("m130-bf16", dict(batch=1, seqlen=2048, nheads=8, init="none")),           # 16 chunks, no init
     ("m130-bf16", dict(batch=2, seqlen=1000, nheads=6, ngroups=3, state="f16")),
+    ("m130-bf16", dict(batch=2, seqlen=700, nheads=4, chunk=256)),              # chunk 256, run as 128s
 ]
 
 
@@ -227,7 +228,8 @@ def test_tc_matches_simt_kernel():
 
 
 # full-size workloads, in the launch configuration the benchmark times; the oracle checks sampled chains
-FULL = ["m130-bf16", "m2p7-L16k-q128", "m2p7-L8k-b1", "m2p7-L8k-b8", "m2p7-L8k-b32", "long-L256k-g8"]
+FULL = ["m130-bf16", "m2p7-L16k-q128", "m2p7-L16k-q256", "m2p7-L8k-b1", "m2p7-L8k-b8", "m2p7-L8k-b32",
+        "long-L256k-g8"]
 
 
 def sampled_chains(w, n):
