@@ -58,14 +58,19 @@ typedef enum {
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1, SSD_F16 = 2 } ssd_dtype_t;
 
-/* Which kernel runs the problem. AUTO picks the tensor-core kernel where it
+/* Which kernel runs the problem. AUTO picks the single-token step kernel for
+ * seqlen == 1 (decode: the recurrence advanced by one token; init_states is the
+ * cached state and final_states, which may be the same buffer, receives the
+ * advanced one; the workspace is only its 256-byte header). STEP also accepts
+ * seqlen 0 and is rejected (SSD_ERR_UNSUPPORTED) for longer sequences.
+ * Otherwise AUTO picks the tensor-core kernel where it
  * has an instance (bf16/fp16 I/O, headdim 64, dstate 128, chunk_size a
  * multiple of 128) and the fp32 SIMT kernel otherwise. The tensor-core kernel
  * passes states every 128 tokens whatever multiple of 128 is requested: the
  * chunked method reaches the recurrence's result exactly for any chunk size
  * ("Mamba hardware-aware algorithms", structured state space duality), so only
  * the rounding depends on it. */
-typedef enum { SSD_KERNEL_AUTO = 0, SSD_KERNEL_SIMT = 1, SSD_KERNEL_TC = 2 } ssd_kernel_t;
+typedef enum { SSD_KERNEL_AUTO = 0, SSD_KERNEL_SIMT = 1, SSD_KERNEL_TC = 2, SSD_KERNEL_STEP = 3 } ssd_kernel_t;
 
 typedef struct {
     int64_t batch;      /* >= 0                                              */

@@ -21,7 +21,7 @@ __all__ = ["ssd_fwd", "workspace_size", "make_problem", "check", "debug_set", "k
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
 
 _DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
-_KERNEL = {"auto": 0, "simt": 1, "tc": 2}
+_KERNEL = {"auto": 0, "simt": 1, "tc": 2, "step": 3}
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
           4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_DEVICE"}
 
@@ -92,7 +92,7 @@ def kernel_for(prob: SsdProblem) -> str:
     k = lib().ssd_fwd_kernel_for(ctypes.byref(prob))
     if k < 0:
         raise SsdError(-k, "ssd_fwd_kernel_for")
-    return {1: "simt", 2: "tc"}[k]
+    return {1: "simt", 2: "tc", 3: "step"}[k]
 
 
 class Workspace:

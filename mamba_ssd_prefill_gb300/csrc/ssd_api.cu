@@ -54,7 +54,7 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     if (pr->nheads % pr->ngroups) return SSD_ERR_INVALID_ARG;
     if (pr->io_dtype < SSD_F32 || pr->io_dtype > SSD_F16) return SSD_ERR_INVALID_ARG;
     if (pr->state_dtype != SSD_F32 && pr->state_dtype != SSD_F16) return SSD_ERR_INVALID_ARG;
-    if (pr->kernel < SSD_KERNEL_AUTO || pr->kernel > SSD_KERNEL_TC) return SSD_ERR_INVALID_ARG;
+    if (pr->kernel < SSD_KERNEL_AUTO || pr->kernel > SSD_KERNEL_STEP) return SSD_ERR_INVALID_ARG;
     // keep every element index comfortably inside int64
     const double tok = (double)pr->batch * (double)pr->seqlen;
     if (tok * (double)pr->nheads * (double)pr->headdim > 4e18 || tok * (double)pr->ngroups * (double)pr->dstate > 4e18 ||
@@ -64,7 +64,10 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     Plan pl;
     const bool tc_ok = ssd::tc_supports(pr->headdim, pr->dstate, pr->chunk_size, pr->io_dtype);
     const bool simt_ok = ssd::simt_smem_bytes(pr->headdim, pr->dstate) <= 227u * 1024u;
-    if (pr->kernel == SSD_KERNEL_TC) {
+    if (pr->kernel == SSD_KERNEL_STEP || (pr->kernel == SSD_KERNEL_AUTO && pr->seqlen == 1)) {
+        if (pr->seqlen > 1) return SSD_ERR_UNSUPPORTED;
+        pl.kernel = SSD_KERNEL_STEP;
+    } else if (pr->kernel == SSD_KERNEL_TC) {
         if (!tc_ok) return SSD_ERR_UNSUPPORTED;
         pl.kernel = SSD_KERNEL_TC;
     } else if (pr->kernel == SSD_KERNEL_SIMT) {
@@ -79,6 +82,12 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
             return SSD_ERR_UNSUPPORTED;
     }
     pl.exec_chunk = pl.kernel == SSD_KERNEL_TC ? ssd::tc_chunk() : pr->chunk_size;
+    if (pl.kernel == SSD_KERNEL_STEP) {  // no inter-CTA state passing: the workspace is its header only
+        pl.nc = pr->seqlen;
+        pl.flags_off = pl.ring_off = pl.bytes = sizeof(WsHeader);
+        *out = pl;
+        return SSD_OK;
+    }
     pl.nc = (pr->seqlen + pl.exec_chunk - 1) / pl.exec_chunk;
     const int64_t chains = pr->batch * pr->nheads;
     double units;
@@ -188,7 +197,9 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     p.total_units = pl.total_units;
 
     cudaError_t e;
-    if (pl.kernel == SSD_KERNEL_TC)
+    if (pl.kernel == SSD_KERNEL_STEP)
+        e = ssd::launch_step(p, pr.io_dtype, pr.state_dtype, sms, s);
+    else if (pl.kernel == SSD_KERNEL_TC)
         e = ssd::launch_tc(p, pr.io_dtype, pr.state_dtype, pl.heads_per_unit, sms, s);
     else
         e = ssd::launch_simt(p, pr.io_dtype, pr.state_dtype, sms, s);

@@ -15,6 +15,9 @@ namespace ssd {
 size_t simt_smem_bytes(int64_t P, int64_t N);
 cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
 
+// single-token step (ssd_step.cu)
+cudaError_t launch_step(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
+
 // tcgen05 / TMA kernel (ssd_tc.cu)
 bool tc_supports(int64_t P, int64_t N, int64_t Q, int io_dtype);
 int64_t tc_chunk();  // tokens per state-passing step inside the tensor-core kernel

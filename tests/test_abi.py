@@ -85,6 +85,13 @@ def test_kernel_selection(lib):
     assert m.kernel_for(prob(chunk_size=256)) == "tc"  # served in 128-token chunks
     assert m.kernel_for(prob(chunk_size=192)) == "simt"
     assert m.kernel_for(prob(chunk_size=64)) == "simt"
+    assert m.kernel_for(prob(seqlen=1)) == "step"  # decode: one token advances the cached state
+    assert m.kernel_for(prob(seqlen=1, kernel="tc")) == "tc"
+    assert m.kernel_for(prob(seqlen=0, kernel="step")) == "step"
+    with pytest.raises(m.SsdError) as e:
+        m.kernel_for(prob(seqlen=2, kernel="step"))
+    assert e.value.status == 2
+    assert m.workspace_size(prob(seqlen=1)) == 256  # the header only
     assert m.kernel_for(prob(kernel="simt")) == "simt"
     # shapes the SIMT kernel cannot hold in shared memory are rejected
     with pytest.raises(m.SsdError) as e:

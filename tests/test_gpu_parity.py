@@ -269,3 +269,63 @@ def test_tc_full_size_sampled(name):
     assert ok, f"{name}: {s}"
     okf, sf = gate_final(fs, fr, w.io, w.state)
     assert okf, f"{name} final: {sf}"
+
+
+# ----------------------------------------------------------------------------- single-token step (decode)
+STEP = [
+    ("m130-bf16", dict(batch=5, nheads=6, ngroups=2)),                                  # bf16, fp32 states
+    ("m130-bf16", dict(batch=3, nheads=4, io="f16", state="f16")),                     # 16-byte fp16 vectors
+    ("tiny-fp32", dict(batch=2, nheads=3, ngroups=3, init="normal")),                  # fp32, N = 64
+    ("m130-bf16", dict(batch=2, nheads=2, headdim=24, dstate=100)),                    # N % 4 != 0: element-wise
+    ("m130-bf16", dict(batch=64, nheads=80, init="none")),                             # no cached state yet
+]
+
+
+@pytest.mark.parametrize("name,over", STEP, ids=[f"{n}-{i}" for i, (n, _) in enumerate(STEP)])
+def test_step_parity(name, over):
+    w = WORKLOADS[name].with_(seqlen=1, **over)
+    inp = make_inputs(w, device="cuda")
+    assert m.kernel_for(m.make_problem(w.batch, 1, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk,
+                                       DTYPES[w.io], DTYPES[w.state])) == "step"
+    y, fin = run_gpu(w, inp)
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"step {name} {over}")
+
+
+def test_step_in_place_without_D():
+    w = WORKLOADS["m130-bf16"].with_(batch=4, seqlen=1, nheads=8)
+    inp = make_inputs(w, device="cuda")
+    inp["D"] = None
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    state = inp["init_states"].clone()
+    y, fin = run_gpu(w, dict(inp, init_states=state), final_states=state)
+    assert fin.data_ptr() == state.data_ptr()
+    assert_parity(w, y, fin, yr, fr)
+
+
+@pytest.mark.parametrize("state", ["f32", "f16"])
+def test_decode_loop_matches_prefill(state):
+    """Prefill a prompt with the tensor-core kernel, then decode six tokens one step at a time, the cached
+    state updated in place: every step's y and the last state match the oracle over the whole sequence."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=300 + 6, nheads=4, state=state, seed=91)
+    inp = make_inputs(w, device="cuda")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    T0 = 300
+    pre = dict(inp, **{k: inp[k][:, :T0].contiguous() for k in ("x", "dt_raw", "B", "C")})
+    y0, cache = run_gpu(w.with_(seqlen=T0), pre)
+    ys = [y0]
+    for t in range(T0, w.seqlen):
+        tok = dict(inp, init_states=cache, **{k: inp[k][:, t:t + 1].contiguous() for k in ("x", "dt_raw", "B", "C")})
+        yt, cache = run_gpu(w.with_(seqlen=1), tok, final_states=cache)
+        ys.append(yt)
+    y = torch.cat(ys, dim=1)
+    assert_parity(w, y, cache, yr, fr, f"decode loop {state}")
+
+
+@pytest.mark.parametrize("name", ["decode-2p7-b64", "decode-2p7-b256-f16"])
+def test_step_full_size(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp)
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, name)
