@@ -106,6 +106,26 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
                              const float *D, const void *init_states, void *y, void *final_states,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* Variable-length batch ("Mamba hardware-aware algorithms": sequences of
+ * different lengths packed along one token axis, each restarting the
+ * recurrence from its own initial state; chunks never cross a sequence
+ * boundary).
+ *  prob         batch must be 1 and seqlen the total token count T; the other
+ *               fields as for ssd_fwd (STEP is not offered here)
+ *  cu_seqlens   device int32 [nseq + 1]: sequence s holds tokens
+ *               cu_seqlens[s] .. cu_seqlens[s+1] (0 = first, T = last,
+ *               non-decreasing; zero-length sequences allowed)
+ *  x, dt_raw, B, C, y   [1, T, ...] as for ssd_fwd
+ *  init_states, final_states   [nseq, nheads, headdim, dstate] (optional)
+ * The offsets are read on the device: malformed ones are reported by
+ * ssd_fwd_check as SSD_ERR_INVALID_ARG and nothing is computed. Workspace: as
+ * for ssd_fwd, sized by ssd_fwd_varlen_workspace_size for this nseq. */
+SSD_API ssd_status_t ssd_fwd_varlen_workspace_size(const ssd_problem_t *prob, int64_t nseq, size_t *bytes);
+SSD_API ssd_status_t ssd_fwd_varlen(const ssd_problem_t *prob, const int32_t *cu_seqlens, int64_t nseq,
+                                    const void *x, const void *dt_raw, const float *dt_bias, const float *A,
+                                    const void *B, const void *C, const float *D, const void *init_states, void *y,
+                                    void *final_states, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, read the device status recorded in `workspace` by the
  * calls queued before, clear it, and return it (SSD_OK when none failed). */
 SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);

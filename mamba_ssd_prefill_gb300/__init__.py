@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["ssd_fwd", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
+__all__ = ["ssd_fwd", "ssd_fwd_varlen", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
@@ -60,6 +60,10 @@ def lib():
             L.ssd_fwd_workspace_size.restype = ctypes.c_int
             L.ssd_fwd.argtypes = [pp] + [vp] * 10 + [vp, sz, vp]
             L.ssd_fwd.restype = ctypes.c_int
+            L.ssd_fwd_varlen_workspace_size.argtypes = [pp, i64, ctypes.POINTER(sz)]
+            L.ssd_fwd_varlen_workspace_size.restype = ctypes.c_int
+            L.ssd_fwd_varlen.argtypes = [pp, vp, i64] + [vp] * 10 + [vp, sz, vp]
+            L.ssd_fwd_varlen.restype = ctypes.c_int
             L.ssd_fwd_check.argtypes = [vp, vp]
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
@@ -163,6 +167,58 @@ def ssd_fwd(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chunk_size=12
                        _stream_ptr(stream, dev))
     if st:
         raise SsdError(st, "ssd_fwd")
+    return y, final_states
+
+
+def ssd_fwd_varlen(x, dt_raw, dt_bias, A, B, C, cu_seqlens, D=None, init_states=None, chunk_size=128,
+                   state_dtype=None, *, y=None, final_states=None, return_final_states=True, workspace=None,
+                   kernel="auto", stream=None):
+    """Variable-length batch: nseq sequences packed along the token axis of x [1, T, H, P] (dt_raw [1, T, H],
+    B/C [1, T, G, N]); cu_seqlens is an int32 CUDA tensor [nseq + 1] of token offsets. init_states and the
+    returned final states are [nseq, H, P, N]. Offsets are checked on the device (see check())."""
+    if x.dim() != 4 or x.shape[0] != 1:
+        raise ValueError("x: expected [1, T, H, P] (sequences packed along T)")
+    _, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_fwd_varlen runs on CUDA tensors only (there is no CPU path)")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 \
+            or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens: expected a contiguous int32 [nseq + 1] tensor on the device of x")
+    nseq = cu_seqlens.numel() - 1
+    io = x.dtype
+    if state_dtype is None:
+        state_dtype = init_states.dtype if init_states is not None else torch.float32
+    for name, t, shape, dt in (("dt_raw", dt_raw, (1, T, H), io), ("B", B, (1, T, G, N), io), ("C", C, (1, T, G, N), io),
+                               ("dt_bias", dt_bias, (H,), torch.float32), ("A", A, (H,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dt} {shape} on {dev}, got {t.dtype} {tuple(t.shape)}")
+    if D is not None and (tuple(D.shape) != (H,) or D.dtype != torch.float32 or not D.is_contiguous()):
+        raise ValueError("D: expected contiguous fp32 [H]")
+    if init_states is not None and (tuple(init_states.shape) != (nseq, H, P, N) or init_states.dtype != state_dtype
+                                    or not init_states.is_contiguous()):
+        raise ValueError("init_states: expected contiguous [nseq, H, P, N] in the state dtype")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    prob = make_problem(1, T, H, P, N, G, chunk_size, io, state_dtype, kernel)
+    n = ctypes.c_size_t(0)
+    st = lib().ssd_fwd_varlen_workspace_size(ctypes.byref(prob), nseq, ctypes.byref(n))
+    if st:
+        raise SsdError(st, "ssd_fwd_varlen_workspace_size")
+    if y is None:
+        y = torch.empty_like(x)
+    if final_states is None and return_final_states:
+        final_states = torch.empty(nseq, H, P, N, dtype=state_dtype, device=dev)
+    if workspace is None:
+        key = (dev.index, torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream)
+        workspace = _default_ws.setdefault(key, Workspace(dev))
+    ws = workspace.get(int(n.value)) if isinstance(workspace, Workspace) else workspace
+    st = lib().ssd_fwd_varlen(ctypes.byref(prob), _ptr(cu_seqlens), nseq, _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A),
+                              _ptr(B), _ptr(C), _ptr(D), _ptr(init_states), _ptr(y), _ptr(final_states), _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+    if st:
+        raise SsdError(st, "ssd_fwd_varlen")
     return y, final_states
 
 

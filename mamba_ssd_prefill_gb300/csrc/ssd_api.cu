@@ -35,17 +35,25 @@ size_t elem_size(int dt) { return dt == SSD_F32 ? 4 : 2; }
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Plan {
-    int kernel = 0;          // SSD_KERNEL_SIMT / _TC
-    int64_t nc = 0;          // chunks per sequence, of exec_chunk tokens
+    int kernel = 0;          // SSD_KERNEL_SIMT / _TC / _STEP
+    int64_t nc = 0;          // chunks per sequence (regular) or the bound ceil(T / exec_chunk) (variable-length)
     int64_t exec_chunk = 0;  // tokens per state-passing step in the chosen kernel
+    int64_t nseq = 0;        // sequences: batch (regular) or the cu_seqlens count (variable-length)
+    bool varlen = false;
     int heads_per_unit = 1;  // TC only
     uint32_t total_units = 0;
-    size_t flags_off = 0, ring_off = 0, bytes = 0;
+    size_t flags_off = 0, ring_off = 0, tab_off = 0, bytes = 0;
 };
 
+// Variable-length tables after the ring: chunk pairs (int2), then four uint32 arrays of nc + 2 (histogram of
+// chunks per sequence, its suffix sums, fill counters, chunk starts) and the chunk-pair count.
+size_t varlen_table_bytes(int64_t nc, int64_t nseq) {
+    return align_up(sizeof(int32_t) * 2 * (size_t)(nc + nseq), 256) + sizeof(uint32_t) * (4 * (size_t)(nc + 2) + 1);
+}
+
 // Validate the problem and lay out the workspace. No CUDA calls except the
-// SM count used to size the tensor-core work units.
-ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
+// SM count used to size the tensor-core work units. nseq < 0: a regular batch.
+ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
     if (!pr || !out) return SSD_ERR_INVALID_ARG;
     if (pr->reserved != 0) return SSD_ERR_INVALID_ARG;
     if (pr->batch < 0 || pr->seqlen < 0 || pr->nheads < 1 || pr->headdim < 1 || pr->dstate < 1 ||
@@ -55,17 +63,22 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     if (pr->io_dtype < SSD_F32 || pr->io_dtype > SSD_F16) return SSD_ERR_INVALID_ARG;
     if (pr->state_dtype != SSD_F32 && pr->state_dtype != SSD_F16) return SSD_ERR_INVALID_ARG;
     if (pr->kernel < SSD_KERNEL_AUTO || pr->kernel > SSD_KERNEL_STEP) return SSD_ERR_INVALID_ARG;
+    const bool varlen = nseq >= 0;
+    if (varlen && (pr->batch != 1 || nseq > INT32_MAX || pr->seqlen > INT32_MAX)) return SSD_ERR_INVALID_ARG;
     // keep every element index comfortably inside int64
     const double tok = (double)pr->batch * (double)pr->seqlen;
+    const double seqs = varlen ? (double)nseq : (double)pr->batch;
     if (tok * (double)pr->nheads * (double)pr->headdim > 4e18 || tok * (double)pr->ngroups * (double)pr->dstate > 4e18 ||
-        (double)pr->batch * pr->nheads * pr->headdim * pr->dstate > 4e18)
+        seqs * pr->nheads * pr->headdim * pr->dstate > 4e18)
         return SSD_ERR_INVALID_ARG;
 
     Plan pl;
+    pl.varlen = varlen;
+    pl.nseq = varlen ? nseq : pr->batch;
     const bool tc_ok = ssd::tc_supports(pr->headdim, pr->dstate, pr->chunk_size, pr->io_dtype);
     const bool simt_ok = ssd::simt_smem_bytes(pr->headdim, pr->dstate) <= 227u * 1024u;
-    if (pr->kernel == SSD_KERNEL_STEP || (pr->kernel == SSD_KERNEL_AUTO && pr->seqlen == 1)) {
-        if (pr->seqlen > 1) return SSD_ERR_UNSUPPORTED;
+    if (pr->kernel == SSD_KERNEL_STEP || (pr->kernel == SSD_KERNEL_AUTO && !varlen && pr->seqlen == 1)) {
+        if (varlen || pr->seqlen > 1) return SSD_ERR_UNSUPPORTED;
         pl.kernel = SSD_KERNEL_STEP;
     } else if (pr->kernel == SSD_KERNEL_TC) {
         if (!tc_ok) return SSD_ERR_UNSUPPORTED;
@@ -84,64 +97,50 @@ ssd_status_t plan(const ssd_problem_t *pr, Plan *out) {
     pl.exec_chunk = pl.kernel == SSD_KERNEL_TC ? ssd::tc_chunk() : pr->chunk_size;
     if (pl.kernel == SSD_KERNEL_STEP) {  // no inter-CTA state passing: the workspace is its header only
         pl.nc = pr->seqlen;
-        pl.flags_off = pl.ring_off = pl.bytes = sizeof(WsHeader);
+        pl.flags_off = pl.ring_off = pl.tab_off = pl.bytes = sizeof(WsHeader);
         *out = pl;
         return SSD_OK;
     }
+    // regular: chunks per sequence; variable-length: no sequence has more than ceil(T / chunk)
     pl.nc = (pr->seqlen + pl.exec_chunk - 1) / pl.exec_chunk;
-    const int64_t chains = pr->batch * pr->nheads;
+    const int64_t chains = pl.nseq * pr->nheads;
     double units;
     if (pl.kernel == SSD_KERNEL_TC) {
-        pl.heads_per_unit = ssd::tc_heads_per_unit(pr->batch, pr->nheads, pr->ngroups, pl.nc, std::max(1, sm_count()));
+        // for a variable-length batch the chunk count is only bounded here (pairs <= nc + nseq); it sizes the units
+        const int64_t pairs = varlen ? pl.nc + pl.nseq : pl.nc * pr->batch;
+        pl.heads_per_unit = ssd::tc_heads_per_unit(1, pr->nheads, pr->ngroups, pairs, std::max(1, sm_count()));
         // test knob: force the heads per work unit (must divide nheads / ngroups, at most 8)
         if (const char *env = getenv("SSD_TC_HEADS_PER_UNIT")) {
             const int hs = atoi(env);
             if (hs >= 1 && hs <= 8 && (pr->nheads / pr->ngroups) % hs == 0) pl.heads_per_unit = hs;
         }
-        units = (double)ssd::tc_total_units(pr->batch, pr->nheads, pr->ngroups, pl.nc, pl.heads_per_unit);
+        units = (double)pairs * (double)(pr->nheads / pl.heads_per_unit);
     } else {
-        units = (double)chains * (double)pl.nc;
+        units = (double)(varlen ? pl.nc + pl.nseq : pl.nc * pr->batch) * (double)pr->nheads;
     }
     if (units >= 4.0e9) return SSD_ERR_UNSUPPORTED;
-    pl.total_units = (uint32_t)units;
+    pl.total_units = varlen ? 0u : (uint32_t)units;
     pl.flags_off = sizeof(WsHeader);
-    const size_t flag_bytes = pl.kernel == SSD_KERNEL_TC ? ssd::tc_flag_bytes(chains)
-                                                         : sizeof(uint32_t) * (size_t)(chains * pl.nc);
+    const size_t flag_bytes = pl.kernel == SSD_KERNEL_TC ? ssd::tc_flag_bytes(chains) : sizeof(uint64_t) * 2 * (size_t)chains;
     pl.ring_off = align_up(pl.flags_off + flag_bytes, 256);
     size_t ring;
     if (pl.kernel == SSD_KERNEL_TC)
         ring = ssd::tc_ring_bytes(chains, pr->headdim, pr->dstate, pr->state_dtype);
     else
         ring = (size_t)chains * 2 * (size_t)(pr->headdim * pr->dstate) * elem_size(pr->state_dtype);
-    pl.bytes = align_up(pl.ring_off + ring, 256);
+    pl.tab_off = align_up(pl.ring_off + ring, 256);
+    pl.bytes = align_up(pl.tab_off + (varlen ? varlen_table_bytes(pl.nc, pl.nseq) : 0), 256);
     *out = pl;
     return SSD_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes) {
-    if (!bytes) return SSD_ERR_INVALID_ARG;
+// Argument checks and launch shared by the regular and the variable-length entry points.
+ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seqlens, const void *x, const void *dt_raw,
+                 const float *dt_bias, const float *A, const void *B, const void *C, const float *D,
+                 const void *init_states, void *y, void *final_states, void *workspace, size_t workspace_bytes,
+                 void *stream) {
     Plan pl;
-    const ssd_status_t st = plan(prob, &pl);
-    if (st != SSD_OK) return st;
-    *bytes = pl.bytes;
-    return SSD_OK;
-}
-
-SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob) {
-    Plan pl;
-    const ssd_status_t st = plan(prob, &pl);
-    return st == SSD_OK ? pl.kernel : -(int)st;
-}
-
-SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw, const float *dt_bias,
-                             const float *A, const void *B, const void *C, const float *D, const void *init_states,
-                             void *y, void *final_states, void *workspace, size_t workspace_bytes, void *stream) {
-    Plan pl;
-    ssd_status_t st = plan(prob, &pl);
+    ssd_status_t st = plan(prob, nseq, &pl);
     if (st != SSD_OK) return st;
     const ssd_problem_t &pr = *prob;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -152,15 +151,16 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     if (!aligned(dt_bias, 4) || !aligned(A, 4) || (D && !aligned(D, 4))) return SSD_ERR_INVALID_ARG;
     if (init_states && !aligned(init_states, 16)) return SSD_ERR_INVALID_ARG;
     if (final_states && !aligned(final_states, 16)) return SSD_ERR_INVALID_ARG;
+    if (pl.varlen && pl.nseq > 0 && (!cu_seqlens || !aligned(cu_seqlens, 4))) return SSD_ERR_INVALID_ARG;
     if (tokens) {
         if (!x || !dt_raw || !B || !C || !y) return SSD_ERR_INVALID_ARG;
         if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) || !aligned(dt_raw, es))
             return SSD_ERR_INVALID_ARG;
     }
-    if (pr.batch == 0) return SSD_OK;
-    if (pr.seqlen == 0) {  // nothing to scan: the final state is the initial one
+    if (pl.nseq == 0) return SSD_OK;
+    if (pr.seqlen == 0) {  // nothing to scan: every final state is the initial one
         if (!final_states) return SSD_OK;
-        const size_t n = (size_t)(pr.batch * pr.nheads * pr.headdim * pr.dstate) * ses;
+        const size_t n = (size_t)(pl.nseq * pr.nheads * pr.headdim * pr.dstate) * ses;
         const cudaError_t e = init_states ? cudaMemcpyAsync(final_states, init_states, n, cudaMemcpyDeviceToDevice, s)
                                           : cudaMemsetAsync(final_states, 0, n, s);
         return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
@@ -183,7 +183,7 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     p.final_states = final_states;
     char *ws = static_cast<char *>(workspace);
     p.hdr = reinterpret_cast<WsHeader *>(ws);
-    p.flags = reinterpret_cast<uint32_t *>(ws + pl.flags_off);
+    p.flags = reinterpret_cast<uint64_t *>(ws + pl.flags_off);
     p.ring = ws + pl.ring_off;
     p.batch = pr.batch;
     p.L = pr.seqlen;
@@ -195,8 +195,20 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     p.nc = pl.nc;
     p.heads_per_group = pr.nheads / pr.ngroups;
     p.total_units = pl.total_units;
+    p.nseq = pl.nseq;
 
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
+    if (pl.varlen) {
+        // chunk-major (sequence, chunk) table from cu_seqlens, on the device
+        char *tab = ws + pl.tab_off;
+        int2 *ctab = reinterpret_cast<int2 *>(tab);
+        uint32_t *scratch = reinterpret_cast<uint32_t *>(tab + align_up(sizeof(int32_t) * 2 * (size_t)(pl.nc + pl.nseq), 256));
+        p.cu = cu_seqlens;
+        p.ctab = ctab;
+        p.vtot = scratch + 4 * (size_t)(pl.nc + 2);
+        e = ssd::launch_varlen_plan(p, scratch, ses, s);
+        if (e != cudaSuccess) return SSD_ERR_CUDA;
+    }
     if (pl.kernel == SSD_KERNEL_STEP)
         e = ssd::launch_step(p, pr.io_dtype, pr.state_dtype, sms, s);
     else if (pl.kernel == SSD_KERNEL_TC)
@@ -204,6 +216,50 @@ SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const voi
     else
         e = ssd::launch_simt(p, pr.io_dtype, pr.state_dtype, sms, s);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes) {
+    if (!bytes) return SSD_ERR_INVALID_ARG;
+    Plan pl;
+    const ssd_status_t st = plan(prob, -1, &pl);
+    if (st != SSD_OK) return st;
+    *bytes = pl.bytes;
+    return SSD_OK;
+}
+
+SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob) {
+    Plan pl;
+    const ssd_status_t st = plan(prob, -1, &pl);
+    return st == SSD_OK ? pl.kernel : -(int)st;
+}
+
+SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw, const float *dt_bias,
+                             const float *A, const void *B, const void *C, const float *D, const void *init_states,
+                             void *y, void *final_states, void *workspace, size_t workspace_bytes, void *stream) {
+    return run(prob, -1, nullptr, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, workspace,
+               workspace_bytes, stream);
+}
+
+SSD_API ssd_status_t ssd_fwd_varlen_workspace_size(const ssd_problem_t *prob, int64_t nseq, size_t *bytes) {
+    if (!bytes || nseq < 0) return SSD_ERR_INVALID_ARG;
+    Plan pl;
+    const ssd_status_t st = plan(prob, nseq, &pl);
+    if (st != SSD_OK) return st;
+    *bytes = pl.bytes;
+    return SSD_OK;
+}
+
+SSD_API ssd_status_t ssd_fwd_varlen(const ssd_problem_t *prob, const int32_t *cu_seqlens, int64_t nseq, const void *x,
+                                    const void *dt_raw, const float *dt_bias, const float *A, const void *B,
+                                    const void *C, const float *D, const void *init_states, void *y,
+                                    void *final_states, void *workspace, size_t workspace_bytes, void *stream) {
+    if (nseq < 0) return SSD_ERR_INVALID_ARG;
+    return run(prob, nseq, cu_seqlens, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, workspace,
+               workspace_bytes, stream);
 }
 
 SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream) {
@@ -216,6 +272,7 @@ SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream) {
     if (status == 0) return SSD_OK;
     if (cudaMemset(&hdr->status, 0, sizeof(status)) != cudaSuccess) return SSD_ERR_CUDA;
     if (status == ssd::DEV_TIMEOUT) return SSD_ERR_TIMEOUT;
+    if (status == ssd::DEV_BAD_SEQLENS) return SSD_ERR_INVALID_ARG;
     return SSD_ERR_DEVICE;
 }
 

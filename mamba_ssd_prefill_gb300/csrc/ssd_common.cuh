@@ -41,10 +41,14 @@ enum WaitSite : uint32_t {
     WAIT_PIPE = 2,    // intra-CTA mbarrier (tensor-core kernel)
 };
 
-enum DevStatus : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 5, DEV_PIPE = 6 };
+enum DevStatus : uint32_t { DEV_OK = 0, DEV_BAD_SEQLENS = 1, DEV_TIMEOUT = 5, DEV_PIPE = 6 };
 
-// Parameters common to both kernels. Element strides are implied by the
-// packed layouts documented in ssd.h.
+// Parameters common to the kernels. Element strides are implied by the packed
+// layouts documented in ssd.h. Tokens are addressed on one packed axis: a
+// regular batch is nseq = batch sequences of L tokens each (token s*L + t), a
+// variable-length batch has its sequences at the offsets cu[s] .. cu[s+1].
+// Chunks never straddle two sequences: chunk c of sequence s starts at token
+// offset(s) + c*Q, and the last chunk of a sequence may be ragged.
 struct Params {
     const void *x;
     const void *dt_raw;
@@ -57,12 +61,53 @@ struct Params {
     void *y;
     void *final_states; // may be null
     WsHeader *hdr;
-    uint32_t *flags;    // [batch * nheads * nchunks]
+    uint64_t *flags;    // state-passing tags, [chain][ring slot] (per state row too in the tensor-core kernel)
     void *ring;         // state ring, layout per kernel
     int64_t batch, L, H, P, N, G, Q, nc;
     int64_t heads_per_group;
-    uint32_t total_units;
+    uint32_t total_units;  // regular batches; variable-length: *vtot chunk pairs times the units per chunk pair
+    int64_t nseq;          // sequences (= batch for a regular batch)
+    const int32_t *cu;     // variable-length: token offsets [nseq + 1]; null for a regular batch
+    const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
+    const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
 };
+
+// Chunk pair cp (one chunk of one sequence) in chunk-major order -> sequence, chunk, first token, length.
+struct SeqChunk {
+    int64_t s, c, tok0, len;
+};
+__device__ __forceinline__ SeqChunk seq_chunk(const Params &p, int64_t cp) {
+    SeqChunk r;
+    if (p.ctab) {
+        const int2 e = p.ctab[cp];
+        r.s = e.x;
+        r.c = e.y;
+        r.tok0 = p.cu[r.s];
+        r.len = p.cu[r.s + 1] - r.tok0;
+    } else {
+        r.s = cp % p.nseq;
+        r.c = cp / p.nseq;
+        r.tok0 = r.s * p.L;
+        r.len = p.L;
+    }
+    return r;
+}
+// Chunk pairs of this launch (regular batches know it on the host; variable-length ones read the device count).
+__device__ __forceinline__ uint32_t total_units(const Params &p, uint32_t units_per_pair) {
+    return p.ctab ? *p.vtot * units_per_pair : p.total_units;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t chain_tag(uint32_t epoch, int64_t chunk) {
+    return ((uint64_t)epoch << 32) | (uint32_t)chunk;
+}
 
 // ---------------------------------------------------------------------------
 // Small PTX helpers (hand-written; no library code).
@@ -109,15 +154,15 @@ __device__ __forceinline__ bool aborted(const WsHeader *hdr, uint32_t epoch) {
     return ld_relaxed_gpu(&hdr->abort) == epoch;
 }
 
-// Bounded wait until *flag == epoch (acquire). Returns false (after recording
+// Bounded wait until *tag == want (acquire). Returns false (after recording
 // a timeout) when the limit passes or another CTA aborted the launch.
-__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch, WsHeader *hdr, uint64_t limit_ns,
-                                          uint32_t unit, uint32_t chunk) {
-    if (ld_acquire_gpu(flag) == epoch) return true;
+__device__ __forceinline__ bool wait_flag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
+                                          uint64_t limit_ns, uint32_t unit, uint32_t chunk) {
+    if (ld_acquire_u64(tag) == want) return true;
     const uint64_t t0 = globaltimer();
     uint32_t sleep_ns = 20;
     for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
-        if (ld_acquire_gpu(flag) == epoch) return true;
+        if (ld_acquire_u64(tag) == want) return true;
         if ((it & 7u) == 7u) {
             if (aborted(hdr, epoch)) return false;
             if (globaltimer() - t0 > limit_ns) break;

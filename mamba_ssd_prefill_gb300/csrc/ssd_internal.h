@@ -15,6 +15,9 @@ namespace ssd {
 size_t simt_smem_bytes(int64_t P, int64_t N);
 cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
 
+// variable-length batches (ssd_varlen.cu): chunk table from cu_seqlens, final = initial for empty sequences
+cudaError_t launch_varlen_plan(const Params &p, uint32_t *scratch, size_t state_bytes, cudaStream_t stream);
+
 // single-token step (ssd_step.cu)
 cudaError_t launch_step(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
 

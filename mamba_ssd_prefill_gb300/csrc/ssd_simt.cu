@@ -6,8 +6,8 @@
 // in chunk-major order, so a unit only ever waits on a lower ticket that a
 // running CTA already holds (deadlock-free without co-residency).
 //
-// Per unit: wait for the state entering chunk c (flag of chunk c-1, epoch
-// tagged), then walk the chunk in 32-token sub-chunks with the running state
+// Per unit: wait for the state entering chunk c (the chain's 64-bit tag
+// epoch:c in a 2-slot ring), then walk the chunk in 32-token sub-chunks with the running state
 // in shared memory, doing the five SSD steps of "Accelerating Mamba2 with
 // Kernel Fusion" (chunk cumsum, BMM, chunk state, state passing, chunk scan)
 // at sub-chunk granularity, then publish the state leaving chunk c.
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
     const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
     const uint64_t limit = hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs;
     const int64_t skip = hdr->skip_publish - 1;  // -1: no chunk skipped
-    const int64_t BH = p.batch * p.H;
+    const uint32_t total = total_units(p, (uint32_t)p.H);
     const IO *x = static_cast<const IO *>(p.x);
     const IO *dtr = static_cast<const IO *>(p.dt_raw);
     const IO *Bg = static_cast<const IO *>(p.B);
@@ -57,15 +57,19 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
         __syncthreads();
         const uint32_t t = s_ticket;
         __syncthreads();
-        if (t >= p.total_units) break;
-        const int64_t c = t / BH, rem = t % BH, b = rem / p.H, h = rem % p.H;
+        if (t >= total) break;
+        const SeqChunk sq = seq_chunk(p, t / p.H);
+        const int64_t c = sq.c, h = t % p.H;
         const int64_t g = h / p.heads_per_group;
-        const int64_t chain = b * p.H + h;
+        const int64_t chain = sq.s * p.H + h;
+        const bool last = c == (sq.len + p.Q - 1) / p.Q - 1;
         const float Ah = p.A[h], bias = p.dt_bias[h], Dh = p.D ? p.D[h] : 0.f;
 
         // ---- state entering chunk c
-        if (tid == 0) s_ok = aborted(hdr, epoch) ? 0 : (c == 0 ? 1 : (int)wait_flag(&p.flags[chain * p.nc + c - 1],
-                                                                                   epoch, hdr, limit, t, (uint32_t)c));
+        if (tid == 0)
+            s_ok = aborted(hdr, epoch) ? 0
+                                       : (c == 0 ? 1 : (int)wait_flag(&p.flags[chain * 2 + (c & 1)], chain_tag(epoch, c),
+                                                                      epoch, hdr, limit, t, (uint32_t)c));
         __syncthreads();
         if (!s_ok) continue;  // launch aborted: drain the remaining tickets
         if (c == 0) {
@@ -79,13 +83,14 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
         }
         __syncthreads();
 
-        const int64_t c0 = c * p.Q, c1 = (c0 + p.Q < p.L) ? c0 + p.Q : p.L;
+        // tokens [c0, c1) of the packed token axis
+        const int64_t c0 = sq.tok0 + c * p.Q, end = sq.tok0 + sq.len, c1 = (c0 + p.Q < end) ? c0 + p.Q : end;
         for (int64_t s0 = c0; s0 < c1; s0 += kSub) {
             const int T = (int)((c1 - s0) < kSub ? (c1 - s0) : kSub);
             // step 1: dt = softplus(dt_raw + bias), inclusive cumsum of dt*A (rows >= T: dt = 0)
             if (tid < 32) {
                 float dtv = 0.f;
-                if (tid < T) dtv = softplus_f32(to_f32(dtr[(b * p.L + s0 + tid) * p.H + h]) + bias);
+                if (tid < T) dtv = softplus_f32(to_f32(dtr[(s0 + tid) * p.H + h]) + bias);
                 float sc = dtv * Ah;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -100,11 +105,11 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             }
             for (int e = tid; e < kSub * P; e += kThreads) {
                 const int r = e / P, q = e % P;
-                xs[e] = r < T ? to_f32(x[((b * p.L + s0 + r) * p.H + h) * P + q]) : 0.f;
+                xs[e] = r < T ? to_f32(x[((s0 + r) * p.H + h) * P + q]) : 0.f;
             }
             for (int e = tid; e < kSub * N; e += kThreads) {
                 const int r = e / N, q = e % N;
-                const int64_t off = ((b * p.L + s0 + r) * p.G + g) * N + q;
+                const int64_t off = ((s0 + r) * p.G + g) * N + q;
                 Bs[r * NB + q] = r < T ? to_f32(Bg[off]) : 0.f;
                 Cs[r * NB + q] = r < T ? to_f32(Cg[off]) : 0.f;
             }
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
                 for (int j = 0; j <= i; ++j) a1 = fmaf(Pm[i * kSub + j], xs[j * P + q], a1);
                 for (int n = 0; n < N; ++n) a2 = fmaf(Cs[i * NB + n], S[n * P + q], a2);
                 const float v = a1 + ecs[i] * a2 + Dh * xs[i * P + q];
-                y[((b * p.L + s0 + i) * p.H + h) * P + q] = from_f32<IO>(v);
+                y[((s0 + i) * p.H + h) * P + q] = from_f32<IO>(v);
             }
             __syncthreads();
             // steps 3 + 4 (chunk state, state passing): S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
         }
 
         // ---- publish the state leaving chunk c
-        if (c == p.nc - 1) {
+        if (last) {
             if (fin)
                 for (int e = tid; e < N * P; e += kThreads) {
                     const int q = e / N, n = e % N;
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             for (int e = tid; e < N * P; e += kThreads) __stcg(slot + e, from_f32<ST>(S[e]));
             __threadfence();
             __syncthreads();
-            if (tid == 0) st_release_gpu(&p.flags[chain * p.nc + c], epoch);
+            if (tid == 0) st_release_u64(&p.flags[chain * 2 + ((c + 1) & 1)], chain_tag(epoch, c + 1));
         }
         __syncthreads();
     }
@@ -183,7 +188,7 @@ cudaError_t launch_t(const Params &p, int sms, cudaStream_t stream) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const int64_t grid = std::min<int64_t>((int64_t)p.total_units, (int64_t)sms * per_sm);
+    const int64_t grid = p.ctab ? (int64_t)sms * per_sm : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms * per_sm);
     k<<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }

@@ -52,7 +52,7 @@ constexpr uint32_t kColCB = 0, kColP = 128, kColYI = 256, kColS = 384;
 constexpr uint32_t kBarMath = 1;  // named barrier of the math warpgroup (0 is __syncthreads)
 
 struct Sched {
-    int32_t valid, b, c, g, h0, rows;
+    int32_t valid, s, c, g, h0, rows, row0, last;  // row0: the chunk's first token on the packed token axis
 };
 
 struct __align__(1024) Smem {
@@ -125,15 +125,6 @@ template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t 
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&v));
 }
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
-
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t *p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_u64(uint64_t *p, uint64_t v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 
 __device__ __noinline__ void chain_timeout(WsHeader *hdr, uint32_t epoch, uint32_t chunk) {
     report_error(hdr, epoch, DEV_TIMEOUT, 0, chunk, WAIT_CHAIN);
@@ -232,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int64_t slices = p.heads_per_group / hs;
-    const int64_t per_chunk = p.batch * p.G * slices;
 
     if (warp == 0) {
         // ------------------------------------------------------------ unit loader
@@ -250,7 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t t = 0;
         if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
         t = __shfl_sync(0xffffffffu, t, 0);
-        Sched prev{0, 0, 0, 0, 0, 0};
+        Sched prev{0, 0, 0, 0, 0, 0, 0, 0};
+        const uint32_t total = total_units(p, (uint32_t)(p.G * slices));
         bool ok = true;
         // conversion + tables of the unit in stage uu (whose tiles were requested earlier)
         auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
@@ -322,11 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t v = 0; ok; ++v) {
             const uint32_t u = v & 1, nn = v >> 1;
             uint32_t t_next = 0;
-            if (lane == 0 && t < p.total_units) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
+            if (lane == 0 && t < total) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
             // the previous unit first: the MMA issuer frees stage u (unit v-2's last C.S) only after it
             // has seen unit v-1 converted
             if (v > 0 && !finish(v - 1, prev)) break;
-            if (t >= p.total_units) {
+            if (t >= total) {
                 if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
                 if (lane == 0) {
                     sm.sched[u].valid = 0;
@@ -337,14 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
             TRACE(0, (1u << 24) | v);
-            const int64_t c = t / per_chunk;
-            int64_t r = t % per_chunk;
-            const int64_t b = r / (p.G * slices);
-            r %= p.G * slices;
+            const SeqChunk sq = seq_chunk(p, t / (p.G * slices));
+            const int64_t r = t % (p.G * slices);
+            const int64_t c = sq.c;
             const int64_t g = r / slices;
             const int64_t h0 = g * p.heads_per_group + (r % slices) * hs;
-            const int64_t row0 = c * kQ;
-            const int rows = (int)((p.L - row0) < kQ ? (p.L - row0) : kQ);
+            const int64_t row0 = sq.tok0 + c * kQ;
+            const int rows = (int)((sq.len - c * kQ) < kQ ? (sq.len - c * kQ) : kQ);
+            const int last = c == (sq.len + kQ - 1) / kQ - 1;
             // dt_raw rows 4*lane .. 4*lane+3 of the unit's heads, every load in flight at once
             float raw[4][kMaxHs];
 #pragma unroll
@@ -353,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < kMaxHs; ++hh) {
                     raw[jj][hh] = 0.f;
-                    if (hh < hs && i < rows) raw[jj][hh] = to_f32(dtr[(b * p.L + row0 + i) * p.H + h0 + hh]);
+                    if (hh < hs && i < rows) raw[jj][hh] = to_f32(dtr[(row0 + i) * p.H + h0 + hh]);
                 }
             }
 #pragma unroll
@@ -361,16 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < kMaxHs; ++hh)
                     if (hh < hs) sm.cs2[u][hh][4 * lane + jj] = raw[jj][hh];
-            const Sched cur{1, (int32_t)b, (int32_t)c, (int32_t)g, (int32_t)h0, rows};
+            const Sched cur{1, (int32_t)sq.s, (int32_t)c, (int32_t)g, (int32_t)h0, rows, (int32_t)row0, last};
             __syncwarp();
             if (lane == 0) {
                 sm.sched[u] = cur;
                 mbar_arrive(&sm.sched_full[u]);
                 mbar_arrive_expect_tx(&sm.bc_full[u], 4 * kTile);
-                tma_load_4d(sm.bc[u][0], &map_b, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
-                tma_load_4d(sm.bc[u][1], &map_b, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
-                tma_load_4d(sm.bc[u][2], &map_c, &sm.bc_full[u], 0, (int)g, (int)row0, (int)b);
-                tma_load_4d(sm.bc[u][3], &map_c, &sm.bc_full[u], 64, (int)g, (int)row0, (int)b);
+                tma_load_4d(sm.bc[u][0], &map_b, &sm.bc_full[u], 0, (int)g, (int)row0, 0);
+                tma_load_4d(sm.bc[u][1], &map_b, &sm.bc_full[u], 64, (int)g, (int)row0, 0);
+                tma_load_4d(sm.bc[u][2], &map_c, &sm.bc_full[u], 0, (int)g, (int)row0, 0);
+                tma_load_4d(sm.bc[u][3], &map_c, &sm.bc_full[u], 64, (int)g, (int)row0, 0);
                 armed_bc |= 1 << u;
                 bc_par[u] = nn & 1;
             }
@@ -407,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&sm.x_full[k], kTile);
-                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, sc.h0 + hh, sc.c * kQ, sc.b);
+                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, sc.h0 + hh, sc.row0, 0);
                     armed_x |= 1 << k;
                     x_par[k] = n & 1;
                 }
@@ -531,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool pend = false;
         uint32_t pk = 0, pn = 0;
         float pecs = 0.f;
-        int ph = 0, prow = 0, pb = 0;  // y tile of the pending head: head, first token of this warp's rows, batch
+        int ph = 0, prow = 0, pvr = 0;  // y of the pending head: head, first token of this warp's rows, valid rows
+        IO *yg = static_cast<IO *>(p.y);
         bool ok = true;
         // y = y_intra + exp(cs_i) y_inter of the pending head, staged in its C.S operand tile (free once C.S
         // has completed) with the operand's 128B swizzle, then one TMA store per warp of its 32 rows; the
@@ -557,11 +549,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sts128(yrow + (((2 * m) ^ (i & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
                 sts128(yrow + (((2 * m + 1) ^ (i & 7)) << 4), make_uint4(o[4], o[5], o[6], o[7]));
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_4d(&map_y, sm.xs[pk] + 32 * q * 128, 0, ph, prow, pb);
-                bulk_commit();
+            if (pvr >= 32) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&map_y, sm.xs[pk] + 32 * q * 128, 0, ph, prow, 0);
+                    bulk_commit();
+                }
+            } else if (lane < pvr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
+                uint4 *dst = reinterpret_cast<uint4 *>(yg + ((int64_t)(prow + lane) * p.H + ph) * kP);
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(yrow + ((lc ^ (i & 7)) << 4));
             }
             if (leader) TRACE(2, (7u << 24) | (pn * 2 + pk));
             return true;
@@ -712,8 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pn = n;
                 pecs = ex2(cs2i);
                 ph = h;
-                prow = sc.c * kQ + 32 * q;
-                pb = sc.b;
+                prow = sc.row0 + 32 * q;
+                pvr = sc.rows - 32 * q;
             }
         }
         if (ok && pend) epilogue();
@@ -777,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t chain = 0;
         int c = 0;
         if (more) {
-            chain = (int64_t)sc.b * p.H + sc.h0;
+            chain = (int64_t)sc.s * p.H + sc.h0;
             c = sc.c;
         }
         uint32_t hc = 0;
@@ -838,8 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // state leaving the chunk: S_out = a S_in + s (kept in s[])
 #pragma unroll
             for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
-            const bool publish = c != p.nc - 1 && c != skip;
-            if (c == p.nc - 1) {
+            const bool publish = !sc.last && c != skip;
+            if (sc.last) {
                 if (fin) {
 #pragma unroll
                     for (int pp = 0; pp < kP; ++pp) fin[(chain * kP + pp) * kN + nrow] = from_f32<ST>(s[pp]);
@@ -886,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hh = 0;
                 more = enter_unit(v);
                 if (!more) break;
-                chain = (int64_t)sc.b * p.H + sc.h0;
+                chain = (int64_t)sc.s * p.H + sc.h0;
                 c = sc.c;
             }
             have_S = prefetch(chain, c);
@@ -930,9 +928,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 4-D map over a [batch, L, mid, inner] 16-bit tensor, box = [1, box_rows, 1, 64 inner], 128B swizzle.
-bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t L, int64_t batch,
-              uint32_t box_rows) {
+// 4-D map over a [1, T, mid, inner] 16-bit tensor (all sequences on one packed token axis of T tokens),
+// box = [1, box_rows, 1, 64 inner], 128B swizzle. Rows past T read as zeros; a chunk's rows past its own
+// sequence read the next sequence and are masked by dt = 0.
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t T, uint32_t box_rows) {
+    const int64_t L = T, batch = 1;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
@@ -950,14 +950,15 @@ template <typename IO, typename ST>
 cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
     CUtensorMap mx, mb, mc, my;
     const bool bf = !std::is_same<IO, __half>::value;
-    if (!make_map(&mx, p.x, bf, kP, p.H, p.L, p.batch, kQ) || !make_map(&mb, p.B, bf, kN, p.G, p.L, p.batch, kQ) ||
-        !make_map(&mc, p.C, bf, kN, p.G, p.L, p.batch, kQ) || !make_map(&my, p.y, bf, kP, p.H, p.L, p.batch, 32))
+    const int64_t T = p.batch * p.L;
+    if (!make_map(&mx, p.x, bf, kP, p.H, T, kQ) || !make_map(&mb, p.B, bf, kN, p.G, T, kQ) ||
+        !make_map(&mc, p.C, bf, kN, p.G, T, kQ) || !make_map(&my, p.y, bf, kP, p.H, T, 32))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem) + 1024;
     auto k = tc_kernel<IO, ST>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
+    const int64_t grid = p.ctab ? (int64_t)sms : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
     k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, my, hs);
     return cudaGetLastError();
 }

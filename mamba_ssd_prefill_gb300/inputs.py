@@ -104,3 +104,20 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
         init = None
     return dict(x=x, dt_raw=dt_raw, dt_bias=dt_bias.to(device), A=A.to(device), B=B, C=C, D=D.to(device),
                 init_states=init)
+
+
+def make_varlen_inputs(w: Workload, lengths, device="cpu", seed: int | None = None) -> dict:
+    """A variable-length batch with the shapes and distributions of ``w``: the sequences of ``lengths`` packed
+    along one token axis ([1, T, ...] tensors, T = sum of lengths), cu_seqlens (int32 [nseq + 1]) and, when the
+    workload has an initial state, init_states [nseq, H, P, N]."""
+    seed = w.seed if seed is None else seed
+    T = int(sum(lengths))
+    inp = make_inputs(w.with_(batch=1, seqlen=T, init="none"), device=device, seed=seed)
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(list(lengths), dtype=torch.int64), 0).to(torch.int32)
+    inp["cu_seqlens"] = cu.to(device)
+    if w.init != "none":
+        g = torch.Generator(device).manual_seed(seed + 2)
+        st = torch.randn(len(lengths), w.nheads, w.headdim, w.dstate, generator=g, device=device)
+        inp["init_states"] = (st.mul_(0.1) if w.init == "normal" else st.zero_()).to(DTYPES[w.state])
+    return inp

@@ -145,3 +145,29 @@ def ssd_reference(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chains=
         y_full[bi, :, h, :] = y[k]
         f_full[bi, h] = fin[k]
     return y_full, f_full
+
+
+def ssd_varlen_reference(x, dt_raw, dt_bias, A, B, C, cu_seqlens, D=None, init_states=None, nthreads=None):
+    """Oracle for a variable-length batch ("Mamba hardware-aware algorithms": sequences packed along one
+    token axis, each its own recurrence). x [1, T, H, P], dt_raw [1, T, H], B/C [1, T, G, N], cu_seqlens
+    [nseq + 1] token offsets, init_states [nseq, H, P, N] (None = zeros). Sequence s (tokens cu[s] .. cu[s+1])
+    runs the plain recurrence from init_states[s]; a sequence of length 0 keeps its initial state.
+    Returns (y [1, T, H, P], final [nseq, H, P, N]) as float64 arrays.
+    """
+    cu = [int(v) for v in np.asarray(cu_seqlens).reshape(-1)]
+    nseq = len(cu) - 1
+    _, T, H, P = x.shape
+    N = B.shape[3]
+    y = np.zeros((1, T, H, P), dtype=np.float64)
+    fin = np.zeros((nseq, H, P, N), dtype=np.float64)
+    for s in range(nseq):
+        a, b = cu[s], cu[s + 1]
+        init = None if init_states is None else init_states[s:s + 1]
+        if b == a:
+            if init is not None:
+                fin[s] = _f64(init)[0]
+            continue
+        ys, fs = ssd_reference(x[:, a:b], dt_raw[:, a:b], dt_bias, A, B[:, a:b], C[:, a:b], D, init, nthreads=nthreads)
+        y[0, a:b] = ys[0]
+        fin[s] = fs[0]
+    return y, fin

@@ -329,3 +329,70 @@ def test_step_full_size(name):
     y, fin = run_gpu(w, inp)
     yr, fr = oracle.ssd_reference(**cpu(inp))
     assert_parity(w, y, fin, yr, fr, name)
+
+
+@pytest.mark.parametrize("kernel,over", [("tc", {}), ("simt", {}), ("simt", dict(io="f32", state="f32")),
+                                         ("step", dict(seqlen=1))],
+                         ids=["tc", "simt-bf16", "simt-fp32", "step"])
+def test_linear_attention_A_zero(kernel, over):
+    """A = 0: no decay, the state is the running sum of dt x B^T (linear attention). Every kernel runs it with the
+    same code; the oracle's A = 0 result is pinned to that closed form on the CPU."""
+    w = WORKLOADS["m130-bf16"].with_(**dict(dict(batch=2, seqlen=400, nheads=4, ngroups=2, seed=31), **over))
+    inp = make_inputs(w, device="cuda")
+    inp["A"] = torch.zeros_like(inp["A"])
+    # dt ~ 0.007: without decay the state is a growing sum; this keeps |y| in the pages' range (below ~20)
+    inp["dt_bias"] = torch.full_like(inp["dt_bias"], -5.0)
+    y, fin = run_gpu(w, inp, kernel=kernel)
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"A=0 {kernel}")
+
+
+# ----------------------------------------------------------------------------- variable-length batches
+from mamba_ssd_prefill_gb300.inputs import make_varlen_inputs  # noqa: E402
+
+VARLEN = [
+    ("tc", "m130-bf16", dict(nheads=4, ngroups=2), [300, 0, 1, 127, 128, 129, 700]),
+    ("tc", "m130-bf16", dict(nheads=6, io="f16", state="f16", init="none"), [1000, 5, 256]),
+    ("tc", "m130-bf16", dict(nheads=8), [0, 0, 64]),
+    ("simt", "m130-bf16", dict(nheads=3, ngroups=3, chunk=64), [200, 0, 65, 1]),
+    ("simt", "tiny-fp32", dict(nheads=2, init="normal"), [130, 7, 300]),
+]
+
+
+@pytest.mark.parametrize("kernel,name,over,lengths", VARLEN, ids=[f"{k}-{i}" for i, (k, *_r) in enumerate(VARLEN)])
+def test_varlen_parity(kernel, name, over, lengths):
+    w = WORKLOADS[name].with_(**over)
+    inp = make_varlen_inputs(w, lengths, device="cuda", seed=101)
+    ws = m.Workspace("cuda")
+    y, fin = m.ssd_fwd_varlen(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel=kernel, workspace=ws)
+    m.check(ws)
+    yr, fr = oracle.ssd_varlen_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"varlen {kernel} {lengths}")
+
+
+def test_varlen_uniform_lengths_equal_regular_batch():
+    w = WORKLOADS["m130-bf16"].with_(batch=3, seqlen=333, nheads=8)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp)
+    T = w.batch * w.seqlen
+    packed = {k: (v.reshape(1, T, *v.shape[2:]) if k in ("x", "dt_raw", "B", "C") else v) for k, v in inp.items()}
+    cu = torch.arange(0, T + 1, w.seqlen, dtype=torch.int32, device="cuda")
+    yv, fv = m.ssd_fwd_varlen(**packed, cu_seqlens=cu, chunk_size=w.chunk, state_dtype=DTYPES[w.state])
+    assert torch.equal(yv.reshape(y.shape), y) and torch.equal(fv, fin)
+
+
+def test_varlen_bad_offsets_reported_then_recovers():
+    w = WORKLOADS["m130-bf16"].with_(nheads=4)
+    inp = make_varlen_inputs(w, [100, 50], device="cuda")
+    ws = m.Workspace("cuda")
+    good = inp["cu_seqlens"].clone()
+    inp["cu_seqlens"] = torch.tensor([0, 120, 100], dtype=torch.int32, device="cuda")  # decreasing, wrong end
+    m.ssd_fwd_varlen(**inp, chunk_size=w.chunk, workspace=ws)
+    with pytest.raises(m.SsdError) as e:
+        m.check(ws)
+    assert e.value.status == 1
+    inp["cu_seqlens"] = good
+    y, fin = m.ssd_fwd_varlen(**inp, chunk_size=w.chunk, workspace=ws)
+    m.check(ws)
+    yr, fr = oracle.ssd_varlen_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr)

@@ -225,3 +225,27 @@ def test_pins_catch_planted_mistakes(kind):
         except AssertionError:
             failed.append(check.__name__)
     assert failed, f"no pin caught the planted mistake {kind!r}"
+
+
+def test_varlen_oracle_against_the_worked_examples():
+    """Variable-length packing: the worked two-token examples packed twice around an empty sequence along one
+    token axis must give each example's hand-derived y and final state, and the empty sequence keeps its
+    initial state (each sequence restarts the recurrence from its own initial state)."""
+    for name in ("two_token_p1n1.json", "two_token_p2n3.json"):
+        g = json.load(open(os.path.join(GOLDEN, name)))
+        x, dtr = np.array(g["x"], float), np.array(g["dt_raw"], float)
+        B, C, h0 = np.array(g["B"], float), np.array(g["C"], float), np.array(g["init"], float)
+        P, N = h0.shape
+        xx = np.concatenate([x, x])[None, :, None, :]
+        dd = np.concatenate([dtr, dtr])[None, :, None]
+        BB = np.concatenate([B, B])[None, :, None, :]
+        CC = np.concatenate([C, C])[None, :, None, :]
+        empty_init = np.full((P, N), 7.0)
+        init = np.stack([h0, empty_init, h0])[:, None]
+        y, f = oracle.ssd_varlen_reference(xx, dd, np.array([g["dt_bias"]]), np.array([g["A"]]), BB, CC,
+                                           np.array([0, 2, 2, 4]), np.array([g["D"]]), init)
+        for half in (0, 1):
+            close(y[0, 2 * half:2 * half + 2, 0], np.array(g["y"]), 1e-12)
+        close(f[0, 0], np.array(g["final"]), 1e-12)
+        close(f[2, 0], np.array(g["final"]), 1e-12)
+        close(f[1, 0], empty_init, 0.0)
