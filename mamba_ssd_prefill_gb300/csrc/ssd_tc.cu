@@ -130,6 +130,38 @@ __device__ __noinline__ void chain_timeout(WsHeader *hdr, uint32_t epoch, uint32
     report_error(hdr, epoch, DEV_TIMEOUT, 0, chunk, WAIT_CHAIN);
 }
 
+// fp16 state ring vector: two 8-byte words, each two fp16 values and a 32-bit tag, each word single-copy atomic
+// (aligned, relaxed, gpu scope).
+__device__ __forceinline__ ulonglong2 ld_ring(const ulonglong2 *p) {
+    ulonglong2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p) : "memory");
+    return r;
+}
+__device__ __forceinline__ void st_ring(ulonglong2 *p, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+// Bounded wait until both words of the ring vector *p carry the tag `want` (the producer writes this vector of a
+// row last). On timeout records SSD_ERR_TIMEOUT and returns false; returns false at once when another CTA aborted
+// the launch. Out of line: it is the slow path.
+__device__ __noinline__ bool wait_ring(const ulonglong2 *p, uint32_t want, uint32_t epoch, WsHeader *hdr,
+                                       uint64_t limit_ns, uint32_t chunk) {
+    const uint64_t t0 = globaltimer();
+    uint32_t sleep_ns = 16;
+    for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
+        const ulonglong2 v = ld_ring(p);
+        if ((uint32_t)(v.x >> 32) == want && (uint32_t)(v.y >> 32) == want) return true;
+        if ((it & 7u) == 7u) {
+            if (aborted(hdr, epoch)) return false;
+            if (globaltimer() - t0 > limit_ns) break;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 64) sleep_ns += 16;
+    }
+    chain_timeout(hdr, epoch, chunk);
+    return false;
+}
+
 // Bounded wait until *tag == want (acquire). On timeout records SSD_ERR_TIMEOUT and returns false;
 // returns false at once when another CTA aborted the launch. Out of line: it is the slow path.
 __device__ __noinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
@@ -719,10 +751,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ chain warpgroup
-        // Thread n owns d_state row n of every state. It publishes its own row with its own
-        // release flag (a 64-bit tag epoch:chunk in a 2-slot ring per chain), so neither side of a
-        // hop needs a CTA barrier; and it prefetches the next head's entering state before that
-        // release, so the release's wait for the row's stores overlaps the prefetch loads.
+        // Thread n owns d_state row n of every state and passes it to the next chunk through a 2-slot ring per
+        // chain, with no CTA barrier on either side of a hop:
+        //  - fp32 states: the row, then its own release flag (a 64-bit tag epoch:chunk); after each publish the
+        //    next head's row is prefetched when its flag is already visible;
+        //  - fp16 states: every 8-byte ring word carries two values and the tag epoch * 4096 + chunk. An aligned
+        //    8-byte access is single-copy atomic, so a word with the expected tag holds this launch's values for
+        //    that chunk: the data is its own flag (no release, no flag load), which shortens the serial chain of
+        //    hops by a round trip. (fp32 rows would need 128 registers in flight this way.)
         const int q = warp & 3;
         const int nrow = 32 * q + lane;  // state row (d_state index) owned by this thread
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
@@ -732,8 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ST *fin = static_cast<ST *>(p.final_states);
         ST *ring = static_cast<ST *>(p.ring);
         uint64_t *tags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]
+        constexpr bool kTagged = sizeof(ST) == 2;
         float S[kP];          // entering state of the current head (fp32)
-        uint4 Sraw[kP / 8];   // fp16 states: the raw prefetched row, unpacked at use
         bool have_S = false;  // the current head's entering state is (being) loaded into registers
         Sched sc;
         uint32_t v = 0;
@@ -743,6 +779,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!bwait(&sm.bc_conv[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
             sc = sm.sched[uu];
             return sc.valid != 0;
+        };
+        ulonglong2 *ringv = static_cast<ulonglong2 *>(p.ring);  // fp16: [chain][slot][P / 4 vectors][row]
+        auto vrow_of = [&](int64_t chain, int c) { return ringv + (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow; };
+        auto vtag = [&](int c) { return epoch * 4096u + (uint32_t)(c & 4095); };
+        // fp16: the tagged row of chunk c as loaded, and whether any of its words is stale
+        uint64_t raw[kTagged ? kP / 2 : 1];
+        auto issue_tagged = [&](int64_t chain, int c) {
+            const ulonglong2 *src = vrow_of(chain, c);
+#pragma unroll
+            for (int j = 0; j < (kTagged ? kP / 4 : 0); ++j) {
+                const ulonglong2 t = ld_ring(src + j * kN);
+                raw[2 * j] = t.x;
+                raw[2 * j + 1] = t.y;
+            }
+        };
+        auto stale = [&](uint32_t want) {
+            uint32_t bad = 0;
+#pragma unroll
+            for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) bad |= (uint32_t)(raw[w] >> 32) ^ want;
+            return bad != 0;
         };
         // Row nrow of the state entering chunk c > 0 of `chain`, from the ring (the caller has seen its tag).
         auto load_ring = [&](int64_t chain, int c) {
@@ -757,17 +813,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     S[4 * m + 2] = f.z;
                     S[4 * m + 3] = f.w;
                 }
-            } else {
-                const uint4 *src = reinterpret_cast<const uint4 *>(slot);
-#pragma unroll
-                for (int m = 0; m < kP / 8; ++m) Sraw[m] = __ldcg(src + m * kN + nrow);
             }
         };
         auto tag_of = [&](int64_t chain, int c) { return tags + (chain * 2 + (c & 1)) * kN + nrow; };
         auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
-        // Prefetch: load the entering state now when its producer's tag is already visible.
+        // Prefetch (fp32 states): load the entering state now when its producer's tag is already visible.
         auto prefetch = [&](int64_t chain, int c) -> bool {
-            if (c == 0 || ld_acquire_u64(tag_of(chain, c)) != want_of(c)) return false;
+            if (kTagged || c == 0 || ld_acquire_u64(tag_of(chain, c)) != want_of(c)) return false;
             load_ring(chain, c);
             return true;
         };
@@ -781,6 +833,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hc = 0;
         while (more) {
             const uint32_t k = hc & 1, n = hc >> 1;
+            // state entering the chunk
+            auto fetch_S = [&]() {
+                if (!have_S) {
+                    if (c == 0) {
+#pragma unroll
+                        for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                    } else if (kTagged) {
+                        const uint32_t want = vtag(c);
+                        issue_tagged(chain, c);
+                        bool ok = !stale(want);
+                        while (!ok) {  // not yet published, or only partly visible: wait on the row's last vector, reload
+                            if (aborted(hdr, epoch) ||
+                                !wait_ring(vrow_of(chain, c) + (kP / 4 - 1) * kN, want, epoch, hdr, limit, (uint32_t)c))
+                                break;
+                            issue_tagged(chain, c);
+                            ok = !stale(want);
+                        }
+                        if (ok) {
+#pragma unroll
+                            for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) {
+                                const float2 f = unpack_f16((uint32_t)raw[w]);
+                                S[2 * w] = f.x;
+                                S[2 * w + 1] = f.y;
+                            }
+                        } else {  // the error is recorded; carry on with zeros so the CTA drains
+#pragma unroll
+                            for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+                        }
+                    } else if ((ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
+                                (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c)))) {
+                        load_ring(chain, c);
+                    } else {  // the error is recorded; carry on with zeros so the CTA drains
+#pragma unroll
+                        for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+                    }
+                }
+            };
+            // fp16 states fetch (and, if need be, wait for) the entering row before s_c is read, so no wait is a
+            // call with s_c's 64 registers live; fp32 states free s_c's TMEM columns first
+            if (kTagged) fetch_S();
             // chunk state s_c from TMEM
             if (!bwait(&sm.mma1[k], n & 1, sm, hdr, epoch)) break;
             tc_fence_after();
@@ -799,40 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sm.s_free[k]);
             if (warp == 6 && lane == 0) TRACE(3, (1u << 24) | hc);
             const float a = ex2(sm.cs2[v & 1][hh][kQ - 1]);  // decay across the chunk
-            // state entering the chunk
-            if (!have_S) {
-                if (c == 0) {
-#pragma unroll
-                    for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
-                    if (sizeof(ST) == 2) {
-#pragma unroll
-                        for (int m = 0; m < kP / 8; ++m)
-                            Sraw[m] = make_uint4(pack_f16(S[8 * m], S[8 * m + 1]), pack_f16(S[8 * m + 2], S[8 * m + 3]),
-                                                 pack_f16(S[8 * m + 4], S[8 * m + 5]),
-                                                 pack_f16(S[8 * m + 6], S[8 * m + 7]));
-                    }
-                } else if ((ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
-                            (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c)))) {
-                    load_ring(chain, c);
-                } else {  // the error is recorded; carry on with zeros so the CTA drains
-#pragma unroll
-                    for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
-#pragma unroll
-                    for (int m = 0; m < kP / 8; ++m) Sraw[m] = make_uint4(0, 0, 0, 0);
-                }
-            }
-            if (sizeof(ST) == 2) {
-#pragma unroll
-                for (int m = 0; m < kP / 8; ++m) {
-                    const uint32_t wv[4] = {Sraw[m].x, Sraw[m].y, Sraw[m].z, Sraw[m].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_f16(wv[e]);
-                        S[8 * m + 2 * e] = f.x;
-                        S[8 * m + 2 * e + 1] = f.y;
-                    }
-                }
-            }
+            if (!kTagged) fetch_S();
             // state leaving the chunk: S_out = a S_in + s (kept in s[])
 #pragma unroll
             for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
@@ -849,13 +908,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < kP / 4; ++m)
                         __stcg(dst + m * kN + nrow, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(slot);
+                } else {  // tagged words, the last vector last
+                    ulonglong2 *dst = vrow_of(chain, c + 1);
+                    const uint64_t tg = (uint64_t)vtag(c + 1) << 32;
 #pragma unroll
-                    for (int m = 0; m < kP / 8; ++m)
-                        __stcg(dst + m * kN + nrow,
-                               make_uint4(pack_f16(s[8 * m], s[8 * m + 1]), pack_f16(s[8 * m + 2], s[8 * m + 3]),
-                                          pack_f16(s[8 * m + 4], s[8 * m + 5]), pack_f16(s[8 * m + 6], s[8 * m + 7])));
+                    for (int j = 0; j < kP / 4; ++j)
+                        st_ring(dst + j * kN, tg | pack_f16(s[4 * j], s[4 * j + 1]), tg | pack_f16(s[4 * j + 2], s[4 * j + 3]));
                 }
             }
             // S_in (fp16) -> the C.S operand: K-row nrow of a [128 x 64] MN-major 128B-swizzled tile
@@ -872,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 6 && lane == 0) TRACE(3, (3u << 24) | hc);
             // publish this head's row (the release orders the row's stores before the tag), then move to
             // the next head and prefetch its entering state
-            if (publish)
+            if (publish && !kTagged)
                 st_release_u64(tags + (chain * 2 + ((c + 1) & 1)) * kN + nrow,
                                ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
             ++hc;
@@ -975,8 +1033,11 @@ int64_t tc_chunk() { return kQ; }
 
 size_t tc_flag_bytes(int64_t chains) { return (size_t)chains * 2 * kN * sizeof(uint64_t); }
 
+// Per chain 2 slots of P x N states: fp32 values (flagged), or fp16 values in tagged 8-byte words (two values and
+// a 32-bit tag): 4 bytes per element either way.
 size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
-    return (size_t)chains * 2 * (size_t)(P * N) * (state_dtype == 0 ? 4 : 2);
+    (void)state_dtype;
+    return (size_t)chains * 2 * (size_t)(P * N) * 4;
 }
 
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {

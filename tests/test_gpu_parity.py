@@ -200,13 +200,14 @@ def test_tc_no_D_alias_and_determinism():
         assert torch.equal(y, y2) and torch.equal(fin, f2)
 
 
-def test_tc_injected_missing_publish_times_out_and_recovers():
-    w = WORKLOADS["m130-bf16"].with_(batch=1, seqlen=1024, nheads=8)
+@pytest.mark.parametrize("state", ["f32", "f16"])  # flagged rows / tagged rows
+def test_tc_injected_missing_publish_times_out_and_recovers(state):
+    w = WORKLOADS["m130-bf16"].with_(batch=1, seqlen=1024, nheads=8, state=state)
     inp = make_inputs(w, device="cuda")
     ws = m.Workspace("cuda")
     y0, f0 = run_gpu(w, inp, kernel="tc", ws=ws)
     m.debug_set(ws, timeout_ns=50_000_000, skip_publish=2)
-    m.ssd_fwd(**inp, chunk_size=w.chunk, kernel="tc", workspace=ws)
+    m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel="tc", workspace=ws)
     with pytest.raises(m.SsdError) as e:
         m.check(ws)
     assert e.value.status == 5
