@@ -126,6 +126,35 @@ SSD_API ssd_status_t ssd_fwd_varlen(const ssd_problem_t *prob, const int32_t *cu
                                     const void *B, const void *C, const float *D, const void *init_states, void *y,
                                     void *final_states, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Activation after the depthwise convolution of ssd_fwd_conv. */
+typedef enum { SSD_ACT_NONE = 0, SSD_ACT_SILU = 1 } ssd_activation_t;
+
+/* The SSD forward on the output of a causal depthwise convolution over the
+ * tokens ("Accelerating Mamba2 with Kernel Fusion", Mamba-2 core operations
+ * item 3; "Mamba-2 compiler optimisation" section 2.2 for the conv cache):
+ *   xbc_out[t, ch] = act(conv_bias[ch] + sum_j conv_weight[ch, j] * xbc[t - (k-1) + j, ch])
+ * then x, B, C are the column slices [0, H*P), [H*P, H*P + G*N), [H*P + G*N, D)
+ * of xbc_out and the rest is ssd_fwd.
+ *  prob             as for ssd_fwd (regular batch); D = H*P + 2*G*N channels,
+ *                   H*P and G*N multiples of 16 bytes of the I/O dtype
+ *  conv_width       k, 1 .. 8;  activation  ssd_activation_t (SiLU: v * sigmoid(v))
+ *  xbc              [batch, seqlen, D] raw inputs (I/O dtype), 16-byte aligned
+ *  conv_weight      [D, k] fp32 (tap k-1 on the current token); conv_bias [D] or NULL
+ *  conv_state       [batch, D, k-1] I/O dtype: the k-1 inputs before each sequence
+ *                   (NULL: zeros, a fresh sequence)
+ *  conv_state_out   [batch, D, k-1] or NULL: the last k-1 inputs, to continue the
+ *                   sequences (by prefill or by seqlen-1 decode steps); may alias
+ *                   conv_state
+ *  xbc_out          [batch, seqlen, D] caller buffer for the convolved rows (the
+ *                   SSD reads x, B, C from it); must not alias xbc
+ *  the rest         as for ssd_fwd (y, init/final states are unchanged in layout)
+ * Two kernels run before the SSD kernel (convolution, cache). */
+SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width, int32_t activation, const void *xbc,
+                                  const float *conv_weight, const float *conv_bias, const void *conv_state,
+                                  void *conv_state_out, void *xbc_out, const void *dt_raw, const float *dt_bias,
+                                  const float *A, const float *D, const void *init_states, void *y, void *final_states,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, read the device status recorded in `workspace` by the
  * calls queued before, clear it, and return it (SSD_OK when none failed). */
 SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);

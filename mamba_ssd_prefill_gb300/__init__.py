@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["ssd_fwd", "ssd_fwd_varlen", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
+__all__ = ["ssd_fwd", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
@@ -64,6 +64,8 @@ def lib():
             L.ssd_fwd_varlen_workspace_size.restype = ctypes.c_int
             L.ssd_fwd_varlen.argtypes = [pp, vp, i64] + [vp] * 10 + [vp, sz, vp]
             L.ssd_fwd_varlen.restype = ctypes.c_int
+            L.ssd_fwd_conv.argtypes = [pp, ctypes.c_int32, ctypes.c_int32] + [vp] * 14 + [sz, vp]
+            L.ssd_fwd_conv.restype = ctypes.c_int
             L.ssd_fwd_check.argtypes = [vp, vp]
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
@@ -220,6 +222,62 @@ def ssd_fwd_varlen(x, dt_raw, dt_bias, A, B, C, cu_seqlens, D=None, init_states=
     if st:
         raise SsdError(st, "ssd_fwd_varlen")
     return y, final_states
+
+
+_ACT = {"none": 0, "silu": 1}
+
+
+def ssd_fwd_conv(xbc, conv_weight, dt_raw, dt_bias, A, nheads, headdim, ngroups, dstate, conv_bias=None, D=None,
+                 init_states=None, conv_state=None, activation="silu", chunk_size=128, state_dtype=None, *,
+                 xbc_out=None, conv_state_out=None, return_conv_state=True, y=None, final_states=None,
+                 return_final_states=True, workspace=None, kernel="auto", stream=None):
+    """Causal depthwise convolution over the tokens, then the SSD on x | B | C column slices of its output.
+
+    xbc [b, L, H*P + 2*G*N] raw (I/O dtype), conv_weight [D, k] fp32, conv_bias [D] fp32, conv_state
+    [b, D, k-1] (None: a fresh sequence). Returns (y, final_states, conv_state_out, xbc_out)."""
+    b, L, Dc = xbc.shape
+    H, P, G, N = int(nheads), int(headdim), int(ngroups), int(dstate)
+    dev = xbc.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_fwd_conv runs on CUDA tensors only (there is no CPU path)")
+    if Dc != H * P + 2 * G * N:
+        raise ValueError("xbc: the channel count must be nheads*headdim + 2*ngroups*dstate")
+    io = xbc.dtype
+    k = conv_weight.shape[1]
+    if state_dtype is None:
+        state_dtype = init_states.dtype if init_states is not None else torch.float32
+    for name, t, shape, dt in (("conv_weight", conv_weight, (Dc, k), torch.float32), ("dt_raw", dt_raw, (b, L, H), io),
+                               ("dt_bias", dt_bias, (H,), torch.float32), ("A", A, (H,), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dt} {shape} on {dev}, got {t.dtype} {tuple(t.shape)}")
+    for name, t, shape, dt in (("conv_bias", conv_bias, (Dc,), torch.float32), ("D", D, (H,), torch.float32),
+                               ("conv_state", conv_state, (b, Dc, k - 1), io),
+                               ("init_states", init_states, (b, H, P, N), state_dtype)):
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dt or t.device != dev or not t.is_contiguous()):
+            raise ValueError(f"{name}: expected contiguous {dt} {shape} on {dev}")
+    if not xbc.is_contiguous():
+        raise ValueError("xbc must be contiguous")
+    prob = make_problem(b, L, H, P, N, G, chunk_size, io, state_dtype, kernel)
+    nbytes = workspace_size(prob)
+    if xbc_out is None:
+        xbc_out = torch.empty_like(xbc)
+    if conv_state_out is None and return_conv_state:
+        conv_state_out = torch.empty(b, Dc, k - 1, dtype=io, device=dev)
+    if y is None:
+        y = torch.empty(b, L, H, P, dtype=io, device=dev)
+    if final_states is None and return_final_states:
+        final_states = torch.empty(b, H, P, N, dtype=state_dtype, device=dev)
+    if workspace is None:
+        key = (dev.index, torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream)
+        workspace = _default_ws.setdefault(key, Workspace(dev))
+    ws = workspace.get(nbytes) if isinstance(workspace, Workspace) else workspace
+    st = lib().ssd_fwd_conv(ctypes.byref(prob), int(k), _ACT[activation], _ptr(xbc), _ptr(conv_weight),
+                            _ptr(conv_bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(xbc_out), _ptr(dt_raw),
+                            _ptr(dt_bias), _ptr(A), _ptr(D), _ptr(init_states), _ptr(y), _ptr(final_states), _ptr(ws),
+                            ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+    if st:
+        raise SsdError(st, "ssd_fwd_conv")
+    return y, final_states, conv_state_out, xbc_out
 
 
 def check(workspace, stream=None):

@@ -135,10 +135,11 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
 }
 
 // Argument checks and launch shared by the regular and the variable-length entry points.
+// x_ld, bc_ld: elements from one token to the next in x and in B, C (0: packed).
 ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seqlens, const void *x, const void *dt_raw,
                  const float *dt_bias, const float *A, const void *B, const void *C, const float *D,
                  const void *init_states, void *y, void *final_states, void *workspace, size_t workspace_bytes,
-                 void *stream) {
+                 void *stream, int64_t x_ld = 0, int64_t bc_ld = 0) {
     Plan pl;
     ssd_status_t st = plan(prob, nseq, &pl);
     if (st != SSD_OK) return st;
@@ -196,6 +197,8 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.heads_per_group = pr.nheads / pr.ngroups;
     p.total_units = pl.total_units;
     p.nseq = pl.nseq;
+    p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
+    p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
 
     cudaError_t e = cudaSuccess;
     if (pl.varlen) {
@@ -260,6 +263,50 @@ SSD_API ssd_status_t ssd_fwd_varlen(const ssd_problem_t *prob, const int32_t *cu
     if (nseq < 0) return SSD_ERR_INVALID_ARG;
     return run(prob, nseq, cu_seqlens, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, workspace,
                workspace_bytes, stream);
+}
+
+SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width, int32_t activation, const void *xbc,
+                                  const float *conv_weight, const float *conv_bias, const void *conv_state,
+                                  void *conv_state_out, void *xbc_out, const void *dt_raw, const float *dt_bias,
+                                  const float *A, const float *D, const void *init_states, void *y, void *final_states,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (!prob) return SSD_ERR_INVALID_ARG;
+    const ssd_problem_t &pr = *prob;
+    if (conv_width < 1 || conv_width > 8 || (activation != SSD_ACT_NONE && activation != SSD_ACT_SILU))
+        return SSD_ERR_INVALID_ARG;
+    Plan pl;
+    ssd_status_t st = plan(prob, -1, &pl);  // the SSD problem checks
+    if (st != SSD_OK) return st;
+    const size_t es = elem_size(pr.io_dtype);
+    const int64_t hp = pr.nheads * pr.headdim, gn = pr.ngroups * pr.dstate, ch = hp + 2 * gn;
+    const int64_t vec = 16 / (int64_t)es;  // x, B, C are 16-byte aligned slices of the convolved rows
+    if (hp % vec || gn % vec) return SSD_ERR_INVALID_ARG;
+    const bool tokens = pr.batch > 0 && pr.seqlen > 0;
+    if (!conv_weight || !aligned(conv_weight, 4) || (conv_bias && !aligned(conv_bias, 4))) return SSD_ERR_INVALID_ARG;
+    if (tokens && (!xbc || !xbc_out || !aligned(xbc, 16) || !aligned(xbc_out, 16) || xbc == xbc_out))
+        return SSD_ERR_INVALID_ARG;
+    if ((conv_state && !aligned(conv_state, es)) || (conv_state_out && !aligned(conv_state_out, es)))
+        return SSD_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    if (sms <= 0) return SSD_ERR_CUDA;
+    ssd::ConvParams c;
+    c.in = xbc;
+    c.w = conv_weight;
+    c.bias = conv_bias;
+    c.state = conv_state;
+    c.out = xbc_out;
+    c.state_out = conv_state_out;
+    c.T = pr.batch * pr.seqlen;
+    c.L = pr.seqlen;
+    c.D = ch;
+    c.nseq = pr.batch;
+    c.k = conv_width;
+    c.silu = activation == SSD_ACT_SILU;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ssd::launch_conv(c, pr.io_dtype, sms, s) != cudaSuccess) return SSD_ERR_CUDA;
+    const char *xo = static_cast<const char *>(xbc_out);
+    return run(prob, -1, nullptr, xo, dt_raw, dt_bias, A, xo ? xo + hp * es : nullptr, xo ? xo + (hp + gn) * es : nullptr, D,
+               init_states, y, final_states, workspace, workspace_bytes, stream, ch, ch);
 }
 
 SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream) {

@@ -67,9 +67,22 @@ struct Params {
     int64_t heads_per_group;
     uint32_t total_units;  // regular batches; variable-length: *vtot chunk pairs times the units per chunk pair
     int64_t nseq;          // sequences (= batch for a regular batch)
+    int64_t x_ld, bc_ld;   // elements from one token to the next in x (packed: H*P) and in B, C (packed: G*N)
     const int32_t *cu;     // variable-length: token offsets [nseq + 1]; null for a regular batch
     const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
+};
+
+// Causal depthwise convolution over the packed token axis (nseq sequences of L tokens, D channels).
+struct ConvParams {
+    const void *in;       // [nseq * L, D] raw inputs
+    const float *w;       // [D, k] taps (tap k - 1 on the current token)
+    const float *bias;    // [D] or null
+    const void *state;    // [nseq, D, k - 1] inputs before each sequence, or null (zeros)
+    void *out;            // [nseq * L, D]
+    void *state_out;      // [nseq, D, k - 1] the last k - 1 inputs of each sequence, or null; may alias state
+    int64_t T, L, D, nseq;
+    int k, silu;
 };
 
 // Chunk pair cp (one chunk of one sequence) in chunk-major order -> sequence, chunk, first token, length.

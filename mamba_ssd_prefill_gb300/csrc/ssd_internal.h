@@ -18,6 +18,9 @@ cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms,
 // variable-length batches (ssd_varlen.cu): chunk table from cu_seqlens, final = initial for empty sequences
 cudaError_t launch_varlen_plan(const Params &p, uint32_t *scratch, size_t state_bytes, cudaStream_t stream);
 
+// causal depthwise convolution in front of the SSD (ssd_conv.cu)
+cudaError_t launch_conv(const ConvParams &c, int io_dtype, int sms, cudaStream_t stream);
+
 // single-token step (ssd_step.cu)
 cudaError_t launch_step(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);
 

@@ -105,11 +105,11 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             }
             for (int e = tid; e < kSub * P; e += kThreads) {
                 const int r = e / P, q = e % P;
-                xs[e] = r < T ? to_f32(x[((s0 + r) * p.H + h) * P + q]) : 0.f;
+                xs[e] = r < T ? to_f32(x[(s0 + r) * p.x_ld + h * P + q]) : 0.f;
             }
             for (int e = tid; e < kSub * N; e += kThreads) {
                 const int r = e / N, q = e % N;
-                const int64_t off = ((s0 + r) * p.G + g) * N + q;
+                const int64_t off = (s0 + r) * p.bc_ld + g * N + q;
                 Bs[r * NB + q] = r < T ? to_f32(Bg[off]) : 0.f;
                 Cs[r * NB + q] = r < T ? to_f32(Cg[off]) : 0.f;
             }

@@ -74,13 +74,14 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
         const float dt = softplus_f32(to_f32(dtr[ch]) + p.dt_bias[h]);
         const float a = expf(dt * p.A[h]);
         const float Dh = p.D ? p.D[h] : 0.f;
-        const IO *Bg = Bm + (b * p.G + g) * p.N;
-        const IO *Cg = Cm + (b * p.G + g) * p.N;
+        const IO *Bg = Bm + b * p.bc_ld + g * p.N;
+        const IO *Cg = Cm + b * p.bc_ld + g * p.N;
+        const IO *xh = x + b * p.x_ld + h * p.P;  // this chain's token
         const int64_t base = ch * p.P * p.N;
         for (int64_t r0 = (int64_t)warp * ROWS; r0 < p.P; r0 += (int64_t)kWarps * ROWS) {
             const int64_t p0 = r0 + sub, p1 = r0 + SUBS + sub;
             const bool one = p0 < p.P, two = p1 < p.P;
-            const float x0 = one ? to_f32(x[ch * p.P + p0]) : 0.f, x1 = two ? to_f32(x[ch * p.P + p1]) : 0.f;
+            const float x0 = one ? to_f32(xh[p0]) : 0.f, x1 = two ? to_f32(xh[p1]) : 0.f;
             float acc0 = 0.f, acc1 = 0.f;
             for (int64_t n0 = (int64_t)l * K; n0 < p.N; n0 += LPR * K) {
                 float h0[K], h1[K], bv[K], cv[K];

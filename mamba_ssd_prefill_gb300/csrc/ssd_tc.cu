@@ -989,13 +989,14 @@ EncodeTiledFn encode_fn() {
 // 4-D map over a [1, T, mid, inner] 16-bit tensor (all sequences on one packed token axis of T tokens),
 // box = [1, box_rows, 1, 64 inner], 128B swizzle. Rows past T read as zeros; a chunk's rows past its own
 // sequence read the next sequence and are masked by dt = 0.
-bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t T, uint32_t box_rows) {
+bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t T, int64_t ld,
+              uint32_t box_rows) {
     const int64_t L = T, batch = 1;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
-    const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2),
-                                   (cuuint64_t)(inner * mid * L * 2)};
+    // ld: elements from one token to the next (inner * mid when packed, more when a slice of wider rows)
+    const cuuint64_t strides[3] = {(cuuint64_t)(inner * 2), (cuuint64_t)(ld * 2), (cuuint64_t)(ld * L * 2)};
     const cuuint32_t box[4] = {64, 1, box_rows, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -1009,8 +1010,8 @@ cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
     CUtensorMap mx, mb, mc, my;
     const bool bf = !std::is_same<IO, __half>::value;
     const int64_t T = p.batch * p.L;
-    if (!make_map(&mx, p.x, bf, kP, p.H, T, kQ) || !make_map(&mb, p.B, bf, kN, p.G, T, kQ) ||
-        !make_map(&mc, p.C, bf, kN, p.G, T, kQ) || !make_map(&my, p.y, bf, kP, p.H, T, 32))
+    if (!make_map(&mx, p.x, bf, kP, p.H, T, p.x_ld, kQ) || !make_map(&mb, p.B, bf, kN, p.G, T, p.bc_ld, kQ) ||
+        !make_map(&mc, p.C, bf, kN, p.G, T, p.bc_ld, kQ) || !make_map(&my, p.y, bf, kP, p.H, T, p.H * kP, 32))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem) + 1024;
     auto k = tc_kernel<IO, ST>;

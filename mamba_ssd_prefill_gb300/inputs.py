@@ -121,3 +121,20 @@ def make_varlen_inputs(w: Workload, lengths, device="cpu", seed: int | None = No
         st = torch.randn(len(lengths), w.nheads, w.headdim, w.dstate, generator=g, device=device)
         inp["init_states"] = (st.mul_(0.1) if w.init == "normal" else st.zero_()).to(DTYPES[w.state])
     return inp
+
+
+def make_conv_inputs(w: Workload, width: int = 4, device="cpu", seed: int | None = None, conv_state: bool = True) -> dict:
+    """Raw inputs of the convolution in front of the SSD, with the SSD parameters of ``w``: xbc [b, L, H*P + 2*G*N]
+    ~ N(0, 1) in the I/O dtype, conv taps ~ U(-1, 1) / sqrt(width), bias ~ N(0, 0.1^2), and (optionally) a conv
+    cache [b, D, width - 1] ~ N(0, 1)."""
+    seed = w.seed if seed is None else seed
+    inp = make_inputs(w, device=device, seed=seed)
+    D = w.nheads * w.headdim + 2 * w.ngroups * w.dstate
+    g = torch.Generator(device).manual_seed(seed + 3)
+    out = dict(dt_raw=inp["dt_raw"], dt_bias=inp["dt_bias"], A=inp["A"], D=inp["D"], init_states=inp["init_states"])
+    out["xbc"] = torch.randn(w.batch, w.seqlen, D, generator=g, device=device).to(DTYPES[w.io])
+    out["conv_weight"] = ((torch.rand(D, width, generator=g, device=device) * 2 - 1) / math.sqrt(width)).contiguous()
+    out["conv_bias"] = torch.randn(D, generator=g, device=device) * 0.1
+    out["conv_state"] = (torch.randn(w.batch, D, width - 1, generator=g, device=device).to(DTYPES[w.io])
+                         if conv_state and width > 1 else None)
+    return out

@@ -171,3 +171,48 @@ def ssd_varlen_reference(x, dt_raw, dt_bias, A, B, C, cu_seqlens, D=None, init_s
         y[0, a:b] = ys[0]
         fin[s] = fs[0]
     return y, fin
+
+
+def conv1d_reference(xbc, weight, bias=None, conv_state=None, activation="silu"):
+    """Causal depthwise convolution over the token axis ("Accelerating Mamba2 with Kernel Fusion": the depthwise
+    convolution that mixes each channel's most recent tokens; "Mamba-2 compiler optimisation" section 2.2: the
+    conv cache of the last k - 1 inputs per channel, [batch, channels, k - 1]).
+
+    xbc [b, L, D] raw inputs, weight [D, k], bias [D] (None = 0), conv_state [b, D, k - 1] (None = zeros: the
+    tokens before the sequence), activation "silu" (v * sigmoid(v)) or "none". For every channel ch:
+        out[t, ch] = act(bias[ch] + sum_j weight[ch, j] * in[t - (k - 1) + j, ch])
+    with in[t' < 0] taken from conv_state. Returns (out [b, L, D], state_out [b, D, k - 1]: the last k - 1 inputs,
+    the cache for continuing the sequence) as float64 arrays.
+    """
+    x = _f64(xbc)
+    w = _f64(weight)
+    b, L, D = x.shape
+    k = w.shape[1]
+    prev = np.zeros((b, k - 1, D)) if conv_state is None else np.transpose(_f64(conv_state), (0, 2, 1))
+    full = np.concatenate([prev, x], axis=1)  # [b, k - 1 + L, D]
+    out = np.zeros((b, L, D))
+    for j in range(k):
+        out += w[None, None, :, j] * full[:, j:j + L, :]
+    if bias is not None:
+        out += _f64(bias)[None, None, :]
+    if activation == "silu":
+        out = out / (1.0 + np.exp(-out))
+    elif activation != "none":
+        raise ValueError("activation must be 'silu' or 'none'")
+    state_out = np.transpose(full[:, L:, :], (0, 2, 1)).copy()  # the last k - 1 inputs
+    return out, state_out
+
+
+def ssd_conv_reference(xbc, weight, conv_bias, dt_raw, dt_bias, A, nheads, headdim, ngroups, dstate, D=None,
+                       init_states=None, conv_state=None, activation="silu", nthreads=None):
+    """The SSD forward on the output of the causal depthwise convolution: xbc [b, L, H*P + 2*G*N] raw, convolved
+    (conv1d_reference), then split along channels into x [b, L, H, P], B and C [b, L, G, N], then ssd_reference.
+    Returns (y, final_states, conv_state_out)."""
+    out, state_out = conv1d_reference(xbc, weight, conv_bias, conv_state, activation)
+    b, L, _ = out.shape
+    hp, gn = nheads * headdim, ngroups * dstate
+    x = out[:, :, :hp].reshape(b, L, nheads, headdim)
+    B = out[:, :, hp:hp + gn].reshape(b, L, ngroups, dstate)
+    C = out[:, :, hp + gn:hp + 2 * gn].reshape(b, L, ngroups, dstate)
+    y, fin = ssd_reference(x, dt_raw, dt_bias, A, B, C, D, init_states, nthreads=nthreads)
+    return y, fin, state_out

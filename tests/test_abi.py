@@ -125,3 +125,15 @@ def test_python_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         m.ssd_fwd(x, torch.zeros(1, 4, 2, dtype=torch.bfloat16), torch.zeros(2), torch.zeros(2),
                   torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16), torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16))
+
+
+def test_new_entry_points_reject_bad_arguments_before_any_cuda_call(lib):
+    """The binding's argument lists match the C signatures (a wrong count raises TypeError here), and argument
+    errors return before anything is launched."""
+    p = prob(seqlen=64)
+    assert lib.ssd_fwd_conv(ctypes.byref(p), 0, 1, *([None] * 14), 0, None) == 1       # conv width 0
+    assert lib.ssd_fwd_conv(ctypes.byref(p), 4, 7, *([None] * 14), 0, None) == 1       # unknown activation
+    assert lib.ssd_fwd_varlen(ctypes.byref(prob(batch=1)), None, -1, *([None] * 10), None, 0, None) == 1
+    assert lib.ssd_fwd_varlen(ctypes.byref(prob(batch=2)), None, 3, *([None] * 10), None, 0, None) == 1  # batch != 1
+    n = ctypes.c_size_t()
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(prob(batch=1)), 4, ctypes.byref(n)) == 0 and n.value > 256

@@ -397,3 +397,60 @@ def test_varlen_bad_offsets_reported_then_recovers():
     m.check(ws)
     yr, fr = oracle.ssd_varlen_reference(**cpu(inp))
     assert_parity(w, y, fin, yr, fr)
+
+
+# ----------------------------------------------------------------------------- depthwise convolution in front
+from mamba_ssd_prefill_gb300.inputs import make_conv_inputs  # noqa: E402
+
+CONV = [
+    ("tc", "m130-bf16", dict(batch=2, seqlen=333, nheads=4, ngroups=2), 4, "silu"),
+    ("tc", "m130-bf16", dict(batch=1, seqlen=700, nheads=8, io="f16", state="f16", init="none"), 3, "none"),
+    ("simt", "tiny-fp32", dict(batch=2, seqlen=200, nheads=2, init="normal"), 4, "silu"),
+    ("auto", "m130-bf16", dict(batch=3, seqlen=1, nheads=4), 4, "silu"),               # decode step with the cache
+]
+
+
+def conv_reference(w, inp, width, act):
+    return oracle.ssd_conv_reference(inp["xbc"].cpu(), inp["conv_weight"].cpu(), inp["conv_bias"].cpu(),
+                                     inp["dt_raw"].cpu(), inp["dt_bias"].cpu(), inp["A"].cpu(), w.nheads, w.headdim,
+                                     w.ngroups, w.dstate, inp["D"].cpu(),
+                                     None if inp["init_states"] is None else inp["init_states"].cpu(),
+                                     None if inp["conv_state"] is None else inp["conv_state"].cpu(), act)
+
+
+@pytest.mark.parametrize("kernel,name,over,width,act", CONV, ids=[f"{c[0]}-{i}" for i, c in enumerate(CONV)])
+def test_conv_then_ssd_parity(kernel, name, over, width, act):
+    w = WORKLOADS[name].with_(**over)
+    inp = make_conv_inputs(w, width, device="cuda", seed=61)
+    ws = m.Workspace("cuda")
+    y, fin, cs, xo = m.ssd_fwd_conv(**inp, nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate,
+                                    activation=act, chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel=kernel,
+                                    workspace=ws)
+    m.check(ws)
+    yr, fr, csr = conv_reference(w, inp, width, act)
+    assert_parity(w, y, fin, yr, fr, f"conv {kernel} {over}")
+    assert np.array_equal(cs.double().cpu().numpy(), csr)  # the cache holds the raw inputs exactly
+    xr, _ = oracle.conv1d_reference(inp["xbc"].cpu(), inp["conv_weight"].cpu(), inp["conv_bias"].cpu(),
+                                    None if inp["conv_state"] is None else inp["conv_state"].cpu(), act)
+    ok, s = gate_y(xo.double().cpu().numpy(), xr, w.io)  # the convolved rows, rounded once to the I/O dtype
+    assert ok, s
+
+
+def test_conv_prefill_then_decode_continues_both_caches():
+    """Prefill 250 tokens, then 3 single-token steps carrying the SSD state and the conv cache in place: every y and
+    both final caches match the oracle over the whole 253-token sequence."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=253, nheads=4, seed=63)
+    inp = make_conv_inputs(w, 4, device="cuda")
+    yr, fr, csr = conv_reference(w, inp, 4, "silu")
+    T0 = 250
+    kw = dict(nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate, chunk_size=w.chunk)
+    part = lambda a, b: {k: (v[:, a:b].contiguous() if k in ("xbc", "dt_raw") else v) for k, v in inp.items()}
+    y0, state, cache, _ = m.ssd_fwd_conv(**part(0, T0), **kw)
+    ys = [y0]
+    for t in range(T0, w.seqlen):
+        tok = part(t, t + 1)
+        tok["init_states"], tok["conv_state"] = state, cache
+        yt, state, cache, _ = m.ssd_fwd_conv(**tok, **kw, final_states=state, conv_state_out=cache)
+        ys.append(yt)
+    assert_parity(w, torch.cat(ys, dim=1), state, yr, fr, "conv prefill + decode")
+    assert np.array_equal(cache.double().cpu().numpy(), csr)

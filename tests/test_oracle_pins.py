@@ -249,3 +249,33 @@ def test_varlen_oracle_against_the_worked_examples():
         close(f[0, 0], np.array(g["final"]), 1e-12)
         close(f[2, 0], np.array(g["final"]), 1e-12)
         close(f[1, 0], empty_init, 0.0)
+
+
+def test_conv_oracle_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "conv_k3_two_channels.json")))
+    out, st = oracle.conv1d_reference(np.array(g["xbc"]), np.array(g["weight"]), np.array(g["bias"]),
+                                      np.array(g["conv_state"]), activation="none")
+    close(out, np.array(g["out"]), 1e-15)
+    close(st, np.array(g["state_out"]), 0.0)
+
+
+def test_conv_oracle_against_numpy_convolve_and_silu():
+    """Every channel against numpy's full convolution (a library primitive) of [state, tokens] with the flipped
+    taps, plus the closed-form SiLU v / (1 + e^-v); and a split sequence continued through the conv cache."""
+    rng = np.random.default_rng(5)
+    b, L, D, k = 2, 9, 5, 4
+    x = rng.standard_normal((b, L, D))
+    w = rng.standard_normal((D, k))
+    bias = rng.standard_normal(D)
+    st = rng.standard_normal((b, D, k - 1))
+    out, st_out = oracle.conv1d_reference(x, w, bias, st, activation="silu")
+    for bi in range(b):
+        for ch in range(D):
+            seq = np.concatenate([st[bi, ch], x[bi, :, ch]])
+            ref = np.convolve(seq, w[ch, ::-1], mode="valid") + bias[ch]
+            close(out[bi, :, ch], ref / (1.0 + np.exp(-ref)), 1e-13)
+            close(st_out[bi, ch], x[bi, L - (k - 1):, ch], 0.0)
+    o1, s1 = oracle.conv1d_reference(x[:, :4], w, bias, st)
+    o2, s2 = oracle.conv1d_reference(x[:, 4:], w, bias, s1)
+    close(np.concatenate([o1, o2], axis=1), out, 1e-15)
+    close(s2, st_out, 0.0)
