@@ -9,7 +9,7 @@
 // or SiLU, v * sigmoid(v). The channels are the x | B | C concatenation of the
 // SSD inputs, so the SSD reads x, B and C as column slices of the output.
 //
-// HBM-bound: a thread walks 16 tokens of one 16-byte vector of channels with
+// HBM-bound: a thread walks 32 tokens of one 16-byte vector of channels with
 // the taps and the last k - 1 inputs in registers, so every input is read once;
 // fp32 arithmetic. A second kernel writes the cache for continuing each
 // sequence.
@@ -28,7 +28,7 @@ template <typename IO> __device__ __forceinline__ void load_vec(const IO *p, flo
     for (int i = 0; i < (int)(16 / sizeof(IO)); ++i) f[i] = to_f32(e[i]);
 }
 
-constexpr int kTokens = 16;  // tokens per thread: the taps and the window of the last k - 1 inputs stay in registers
+constexpr int kTokens = 32;  // tokens per thread: the taps and the window of the last k - 1 inputs stay in registers
 
 // Inputs before token tt of sequence s for window slot j (token tt - 1 - j): from the rows, else the cache, else 0.
 template <typename IO, int V>
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads) conv_kernel(ConvParams c) {
             uint4 o;
             IO *oe = reinterpret_cast<IO *>(&o);
 #pragma unroll
-            for (int i = 0; i < V; ++i) oe[i] = from_f32<IO>(c.silu ? acc[i] / (1.f + __expf(-acc[i])) : acc[i]);
+            for (int i = 0; i < V; ++i) oe[i] = from_f32<IO>(c.silu ? __fdividef(acc[i], 1.f + __expf(-acc[i])) : acc[i]);
             *reinterpret_cast<uint4 *>(out + t * c.D + c0) = o;
 #pragma unroll
             for (int j = K - 2; j > 0; --j)
