@@ -145,10 +145,16 @@ typedef enum { SSD_ACT_NONE = 0, SSD_ACT_SILU = 1 } ssd_activation_t;
  *  conv_state_out   [batch, D, k-1] or NULL: the last k-1 inputs, to continue the
  *                   sequences (by prefill or by seqlen-1 decode steps); may alias
  *                   conv_state
- *  xbc_out          [batch, seqlen, D] caller buffer for the convolved rows (the
- *                   SSD reads x, B, C from it); must not alias xbc
+ *  xbc_out          [batch, seqlen, D] buffer for the convolved rows, or NULL:
+ *                   - NULL: the convolution is fused into the tensor-core kernel,
+ *                     which convolves the raw rows as it loads them (no activation
+ *                     buffer, one write and one read of [b, L, D] saved); needs
+ *                     that kernel, conv_width 4 and 16-byte aligned conv_weight and
+ *                     conv_bias, else SSD_ERR_UNSUPPORTED;
+ *                   - a buffer: a convolution kernel writes it (it must not alias
+ *                     xbc) and the SSD reads x, B, C from it (any kernel, width)
  *  the rest         as for ssd_fwd (y, init/final states are unchanged in layout)
- * Two kernels run before the SSD kernel (convolution, cache). */
+ * The cache is written by one more small kernel after the others. */
 SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width, int32_t activation, const void *xbc,
                                   const float *conv_weight, const float *conv_bias, const void *conv_state,
                                   void *conv_state_out, void *xbc_out, const void *dt_raw, const float *dt_bias,

@@ -229,12 +229,14 @@ _ACT = {"none": 0, "silu": 1}
 
 def ssd_fwd_conv(xbc, conv_weight, dt_raw, dt_bias, A, nheads, headdim, ngroups, dstate, conv_bias=None, D=None,
                  init_states=None, conv_state=None, activation="silu", chunk_size=128, state_dtype=None, *,
-                 xbc_out=None, conv_state_out=None, return_conv_state=True, y=None, final_states=None,
+                 fuse=False, xbc_out=None, conv_state_out=None, return_conv_state=True, y=None, final_states=None,
                  return_final_states=True, workspace=None, kernel="auto", stream=None):
     """Causal depthwise convolution over the tokens, then the SSD on x | B | C column slices of its output.
 
     xbc [b, L, H*P + 2*G*N] raw (I/O dtype), conv_weight [D, k] fp32, conv_bias [D] fp32, conv_state
-    [b, D, k-1] (None: a fresh sequence). Returns (y, final_states, conv_state_out, xbc_out)."""
+    [b, D, k-1] (None: a fresh sequence). By default the convolved rows are written to xbc_out first (the faster
+    path on this kernel); with fuse (and no xbc_out) the tensor-core kernel convolves as it loads and no activation
+    buffer exists (xbc_out returned None). Returns (y, final_states, conv_state_out, xbc_out)."""
     b, L, Dc = xbc.shape
     H, P, G, N = int(nheads), int(headdim), int(ngroups), int(dstate)
     dev = xbc.device
@@ -259,7 +261,7 @@ def ssd_fwd_conv(xbc, conv_weight, dt_raw, dt_bias, A, nheads, headdim, ngroups,
         raise ValueError("xbc must be contiguous")
     prob = make_problem(b, L, H, P, N, G, chunk_size, io, state_dtype, kernel)
     nbytes = workspace_size(prob)
-    if xbc_out is None:
+    if xbc_out is None and not fuse:
         xbc_out = torch.empty_like(xbc)
     if conv_state_out is None and return_conv_state:
         conv_state_out = torch.empty(b, Dc, k - 1, dtype=io, device=dev)
@@ -271,10 +273,17 @@ def ssd_fwd_conv(xbc, conv_weight, dt_raw, dt_bias, A, nheads, headdim, ngroups,
         key = (dev.index, torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream)
         workspace = _default_ws.setdefault(key, Workspace(dev))
     ws = workspace.get(nbytes) if isinstance(workspace, Workspace) else workspace
-    st = lib().ssd_fwd_conv(ctypes.byref(prob), int(k), _ACT[activation], _ptr(xbc), _ptr(conv_weight),
-                            _ptr(conv_bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(xbc_out), _ptr(dt_raw),
-                            _ptr(dt_bias), _ptr(A), _ptr(D), _ptr(init_states), _ptr(y), _ptr(final_states), _ptr(ws),
-                            ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+
+    def call(out):
+        return lib().ssd_fwd_conv(ctypes.byref(prob), int(k), _ACT[activation], _ptr(xbc), _ptr(conv_weight),
+                                  _ptr(conv_bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(out), _ptr(dt_raw),
+                                  _ptr(dt_bias), _ptr(A), _ptr(D), _ptr(init_states), _ptr(y), _ptr(final_states),
+                                  _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+
+    st = call(xbc_out)
+    if st == 2 and xbc_out is None:  # no fused instance for this problem: convolve into a buffer first
+        xbc_out = torch.empty_like(xbc)
+        st = call(xbc_out)
     if st:
         raise SsdError(st, "ssd_fwd_conv")
     return y, final_states, conv_state_out, xbc_out

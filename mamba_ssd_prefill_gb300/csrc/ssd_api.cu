@@ -139,7 +139,7 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
 ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seqlens, const void *x, const void *dt_raw,
                  const float *dt_bias, const float *A, const void *B, const void *C, const float *D,
                  const void *init_states, void *y, void *final_states, void *workspace, size_t workspace_bytes,
-                 void *stream, int64_t x_ld = 0, int64_t bc_ld = 0) {
+                 void *stream, int64_t x_ld = 0, int64_t bc_ld = 0, const ssd::Params *conv = nullptr) {
     Plan pl;
     ssd_status_t st = plan(prob, nseq, &pl);
     if (st != SSD_OK) return st;
@@ -199,6 +199,13 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.nseq = pl.nseq;
     p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
     p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
+    if (conv) {  // convolution fused into the tensor-core kernel: x, B, C are slices of the raw rows
+        p.conv_w = conv->conv_w;
+        p.conv_b = conv->conv_b;
+        p.conv_state = conv->conv_state;
+        p.conv_hp = conv->conv_hp;
+        p.conv_silu = conv->conv_silu;
+    }
 
     cudaError_t e = cudaSuccess;
     if (pl.varlen) {
@@ -283,7 +290,7 @@ SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width,
     if (hp % vec || gn % vec) return SSD_ERR_INVALID_ARG;
     const bool tokens = pr.batch > 0 && pr.seqlen > 0;
     if (!conv_weight || !aligned(conv_weight, 4) || (conv_bias && !aligned(conv_bias, 4))) return SSD_ERR_INVALID_ARG;
-    if (tokens && (!xbc || !xbc_out || !aligned(xbc, 16) || !aligned(xbc_out, 16) || xbc == xbc_out))
+    if (tokens && (!xbc || !aligned(xbc, 16) || (xbc_out && (!aligned(xbc_out, 16) || xbc == xbc_out))))
         return SSD_ERR_INVALID_ARG;
     if ((conv_state && !aligned(conv_state, es)) || (conv_state_out && !aligned(conv_state_out, es)))
         return SSD_ERR_INVALID_ARG;
@@ -303,6 +310,25 @@ SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width,
     c.k = conv_width;
     c.silu = activation == SSD_ACT_SILU;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const char *xb = static_cast<const char *>(xbc);
+    if (!xbc_out && tokens) {
+        // fused: the tensor-core kernel convolves the raw rows as it loads them (no activation buffer)
+        if (pl.kernel != SSD_KERNEL_TC || conv_width != 4 || !aligned(conv_weight, 16) ||
+            (conv_bias && !aligned(conv_bias, 16)))
+            return SSD_ERR_UNSUPPORTED;
+        ssd::Params cv;
+        memset(&cv, 0, sizeof(cv));
+        cv.conv_w = conv_weight;
+        cv.conv_b = conv_bias;
+        cv.conv_state = conv_state;
+        cv.conv_hp = hp;
+        cv.conv_silu = activation == SSD_ACT_SILU;
+        st = run(prob, -1, nullptr, xb, dt_raw, dt_bias, A, xb + hp * es, xb + (hp + gn) * es, D, init_states, y,
+                 final_states, workspace, workspace_bytes, stream, ch, ch, &cv);
+        if (st != SSD_OK) return st;
+        c.T = 0;  // the cache only, after the kernel that reads the cache given on entry
+        return ssd::launch_conv(c, pr.io_dtype, sms, s) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
     if (ssd::launch_conv(c, pr.io_dtype, sms, s) != cudaSuccess) return SSD_ERR_CUDA;
     const char *xo = static_cast<const char *>(xbc_out);
     return run(prob, -1, nullptr, xo, dt_raw, dt_bias, A, xo ? xo + hp * es : nullptr, xo ? xo + (hp + gn) * es : nullptr, D,

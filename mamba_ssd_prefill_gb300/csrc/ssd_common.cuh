@@ -68,6 +68,13 @@ struct Params {
     uint32_t total_units;  // regular batches; variable-length: *vtot chunk pairs times the units per chunk pair
     int64_t nseq;          // sequences (= batch for a regular batch)
     int64_t x_ld, bc_ld;   // elements from one token to the next in x (packed: H*P) and in B, C (packed: G*N)
+    // Depthwise convolution (width 4) fused in front (tensor-core kernel): x, B, C are then slices of the raw rows
+    // [tokens, Dc = x_ld] starting at channels 0, conv_hp and conv_hp + G*N.
+    const float *conv_w;     // [Dc, 4], tap 3 on the current token
+    const float *conv_b;     // [Dc] or null
+    const void *conv_state;  // [nseq, Dc, 3] inputs before each sequence (I/O dtype), or null (zeros)
+    int64_t conv_hp;         // H * P
+    int conv_silu;
     const int32_t *cu;     // variable-length: token offsets [nseq + 1]; null for a regular batch
     const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)

@@ -59,6 +59,9 @@ struct __align__(1024) Smem {
     uint8_t bc[2][4][kTile];   // per unit stage: B n[0,64), B n[64,128), C n[0,64), C n[64,128)
     uint8_t x[2][kTile];       // per head buffer: x tile (fp16 after conversion)
     uint8_t xs[2][kTile];      // per head buffer: X_s, then S_in (fp16, C.S operand)
+    uint8_t xhalo[2][384];     // fused convolution: the 3 raw x rows before the chunk, dense [3][64] 16-bit
+    float4 xtap[2][kP];        // fused convolution: the head's taps per x channel (tap 3 on the current token)
+    float xbias[2][kP];        //                    and its bias
     float cs2[2][kMaxHs][kQ];  // raw dt_raw from the producer, then log2(e) * cumsum(dt*A)
     float dt[2][kMaxHs][kQ];   // dt
     float wt[2][kMaxHs][kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
@@ -125,6 +128,75 @@ template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t 
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&v));
 }
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
+
+// ---------------------------------------------------------------- fused depthwise convolution (width 4)
+// SiLU with one special-function op: e = 2^(-v log2 e) on the SFU, then 1 / (1 + e) by Newton-Raphson steps
+// r <- r (2 - d r) from the exponent-reflection estimate (bit pattern 0x7EF311C3 - bits(d), relative error below
+// 0.13); each step squares the error, so three leave it near 1e-7, far below what the fp16 result keeps. v is
+// clamped at -80, where SiLU is 0 in fp16.
+__device__ __forceinline__ float silu_fast(float v) {
+    v = fmaxf(v, -80.f);
+    const float d = 1.f + ex2(-v * kLog2e);
+    float r = __int_as_float(0x7EF311C3 - __float_as_int(d));
+    r = r * fmaf(-d, r, 2.f);
+    r = r * fmaf(-d, r, 2.f);
+    r = r * fmaf(-d, r, 2.f);
+    return v * r;
+}
+
+// The 3 raw inputs before token row0 of channels ch, ch + 1 (h[j] = token row0 - 3 + j): the rows themselves inside
+// the sequence (which starts at token tok0), else the conv cache of sequence s, else zeros.
+template <typename IO>
+__device__ __forceinline__ void conv_halo(const Params &p, int64_t s, int64_t tok0, int64_t row0, int64_t ch,
+                                          float (&h)[3][2]) {
+    const IO *xraw = static_cast<const IO *>(p.x);
+    const IO *st = static_cast<const IO *>(p.conv_state);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int64_t tok = row0 - 3 + j;
+        if (tok >= tok0) {
+            const float2 f = unpack_io<IO>(*reinterpret_cast<const uint32_t *>(xraw + tok * p.x_ld + ch));
+            h[j][0] = f.x;
+            h[j][1] = f.y;
+        } else if (st) {
+            h[j][0] = to_f32(st[(s * p.x_ld + ch) * 3 + 3 + (tok - tok0)]);
+            h[j][1] = to_f32(st[(s * p.x_ld + ch + 1) * 3 + 3 + (tok - tok0)]);
+        } else {
+            h[j][0] = h[j][1] = 0.f;
+        }
+    }
+}
+
+// Causal width-4 convolution in place over a [128 rows x 64 channels] 128B-swizzled 16-bit tile (1024-aligned); lane
+// owns channels 2 lane, 2 lane + 1 and walks the rows with the last 3 inputs in registers; results are fp16.
+template <typename IO>
+__device__ __forceinline__ void conv_tile(uint8_t *tile, const float4 w0, const float4 w1, float b0, float b1,
+                                          float (&h)[3][2], bool silu, int lane) {
+    const int lc = lane >> 2, wo = (lane & 3) * 4;
+#pragma unroll 1
+    for (int r0 = 0; r0 < kQ; r0 += 8) {
+        uint32_t raw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint32_t *>(tile + (r0 + u) * 128 + ((lc ^ u) << 4) + wo);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float2 v = unpack_io<IO>(raw[u]);
+            float o0 = fmaf(w0.w, v.x, fmaf(w0.z, h[2][0], fmaf(w0.y, h[1][0], fmaf(w0.x, h[0][0], b0))));
+            float o1 = fmaf(w1.w, v.y, fmaf(w1.z, h[2][1], fmaf(w1.y, h[1][1], fmaf(w1.x, h[0][1], b1))));
+            if (silu) {
+                o0 = silu_fast(o0);
+                o1 = silu_fast(o1);
+            }
+            *reinterpret_cast<uint32_t *>(tile + (r0 + u) * 128 + ((lc ^ u) << 4) + wo) = pack_f16(o0, o1);
+            h[0][0] = h[1][0];
+            h[0][1] = h[1][1];
+            h[1][0] = h[2][0];
+            h[1][1] = h[2][1];
+            h[2][0] = v.x;
+            h[2][1] = v.y;
+        }
+    }
+}
 
 __device__ __noinline__ void chain_timeout(WsHeader *hdr, uint32_t epoch, uint32_t chunk) {
     report_error(hdr, epoch, DEV_TIMEOUT, 0, chunk, WAIT_CHAIN);
@@ -210,10 +282,11 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, 
     return mbar_try_wait(bar, parity) || bwait_slow(bar, parity, sm, hdr, epoch);
 }
 
-template <typename IO, typename ST>
+template <typename IO, typename ST, bool CONV>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-              const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_y, const int hs) {
+              const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_y,
+              const __grid_constant__ CUtensorMap map_xh, const int hs) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base (128B-swizzle atoms). Computed as smem_raw + pad, not through an integer
     // round trip, so the compiler keeps the shared address space and emits LDS/STS for every access.
@@ -279,7 +352,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
             const uint32_t uu = vv & 1;
             if (!bwait(&sm.bc_full[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
-            if (kBf16) {
+            if constexpr (CONV) {  // B, C: the raw tiles convolved in place (fp16 out), halo from the rows or the cache
+                const int64_t tok0 = sc.row0 - (int64_t)sc.c * kQ;
+#pragma unroll 1
+                for (int t = 0; t < 4; ++t) {
+                    const int64_t ch = p.conv_hp + (t >= 2 ? p.G * kN : 0) + (int64_t)sc.g * kN + (t & 1) * 64 + 2 * lane;
+                    const float4 w0 = *reinterpret_cast<const float4 *>(p.conv_w + ch * 4);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(p.conv_w + (ch + 1) * 4);
+                    const float b0 = p.conv_b ? p.conv_b[ch] : 0.f, b1 = p.conv_b ? p.conv_b[ch + 1] : 0.f;
+                    float hv[3][2];
+                    conv_halo<IO>(p, sc.s, tok0, sc.row0, ch, hv);
+                    conv_tile<IO>(sm.bc[uu][t], w0, w1, b0, b1, hv, p.conv_silu != 0, lane);
+                }
+            } else if (kBf16) {
 #pragma unroll 1
                 for (int it = 0; it < 16; ++it) {  // 4 tiles x 4 rows per lane
                     const int row = lane + 32 * (it & 3);
@@ -412,38 +497,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kXWarp) {
         // ------------------------------------------------------------ x loader
+        // One TMA per head into the 2-deep x ring (lane 0). With the fused convolution it also brings the 3 raw rows
+        // before the chunk: by TMA inside the sequence, else written by the lanes from the conv cache (or zeros).
         if (lane == 0) {
             prefetch_tensormap(&map_x);
-            uint32_t hc = 0;
-            int armed_x = 0;
-            uint32_t x_par[2] = {0, 0};
-            for (uint32_t v = 0;; ++v) {
-                const uint32_t u = v & 1;
-                if (!bwait(&sm.sched_full[u], (v >> 1) & 1, sm, hdr, epoch)) break;
-                const Sched sc = sm.sched[u];
-                if (!sc.valid) break;
-                bool ok = true;
-                for (int hh = 0; hh < hs; ++hh, ++hc) {
-                    const uint32_t k = hc & 1, n = hc >> 1;
-                    if (!bwait(&sm.x_empty[k], (n & 1) ^ 1, sm, hdr, epoch)) {
-                        ok = false;
-                        break;
+            if (CONV) prefetch_tensormap(&map_xh);
+        }
+        uint32_t hc = 0;
+        int armed_x = 0;
+        uint32_t x_par[2] = {0, 0};
+        for (uint32_t v = 0;; ++v) {
+            const uint32_t u = v & 1;
+            if (!bwait(&sm.sched_full[u], (v >> 1) & 1, sm, hdr, epoch)) break;
+            const Sched sc = sm.sched[u];
+            if (!sc.valid) break;
+            bool ok = true;
+            for (int hh = 0; hh < hs; ++hh, ++hc) {
+                const uint32_t k = hc & 1, n = hc >> 1;
+                if (!bwait(&sm.x_empty[k], (n & 1) ^ 1, sm, hdr, epoch)) {
+                    ok = false;
+                    break;
+                }
+                const bool halo_tma = CONV && sc.c > 0;
+                if (CONV) {  // the head's taps and bias, read by the math warps as broadcasts
+                    const int64_t ch0 = (int64_t)(sc.h0 + hh) * kP;
+                    for (int e = lane; e < kP; e += 32) {
+                        sm.xtap[k][e] = *reinterpret_cast<const float4 *>(p.conv_w + (ch0 + e) * 4);
+                        sm.xbias[k][e] = p.conv_b ? p.conv_b[ch0 + e] : 0.f;
                     }
-                    mbar_arrive_expect_tx(&sm.x_full[k], kTile);
+                }
+                if (CONV && sc.c == 0) {  // the sequence starts here: its conv cache (or zeros) before it
+                    const IO *st = static_cast<const IO *>(p.conv_state);
+                    IO *dst = reinterpret_cast<IO *>(sm.xhalo[k]);
+                    for (int e = lane; e < 3 * kP; e += 32) {
+                        const int r = e / kP, pc = e % kP;
+                        const int64_t ch = (int64_t)(sc.h0 + hh) * kP + pc;
+                        dst[r * kP + pc] = st ? st[((int64_t)sc.s * p.x_ld + ch) * 3 + r] : from_f32<IO>(0.f);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sm.x_full[k], kTile + (halo_tma ? 3 * kP * 2 : 0));
                     tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, sc.h0 + hh, sc.row0, 0);
+                    if (halo_tma) tma_load_4d(sm.xhalo[k], &map_xh, &sm.x_full[k], 0, sc.h0 + hh, sc.row0 - 3, 0);
                     armed_x |= 1 << k;
                     x_par[k] = n & 1;
                 }
-                if (!ok) break;
             }
-            if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) {
-                for (int k = 0; k < 2; ++k)
-                    if (armed_x & (1 << k)) {
-                        const uint64_t t0 = globaltimer();
-                        while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
-                        }
+            if (!ok) break;
+        }
+        if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
+            for (int k = 0; k < 2; ++k)
+                if (armed_x & (1 << k)) {
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
                     }
-            }
+                }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -619,7 +728,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 const float cs2i = sm.cs2[u][hh][i];
                 const float xscale = ex2(sm.cs2[u][hh][kQ - 1] - cs2i) * sm.dt[u][hh][i];
-                {
+                if constexpr (CONV) {
+                    // row i of x convolved from the raw rows i-3 .. i (rows before the chunk from the halo), then,
+                    // once every row has been read, written back as fp16 together with X_s
+                    uint32_t xo[kP / 2], so[kP / 2];
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) {
+                        uint4 rr[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int r = i - 3 + j;
+                            rr[j] = r >= 0 ? lds128(sm.x[k] + r * 128 + ((lc ^ (r & 7)) << 4))
+                                           : lds128(sm.xhalo[k] + (r + 3) * 128 + lc * 16);
+                        }
+                        const float4 bb0 = reinterpret_cast<const float4 *>(sm.xbias[k])[2 * lc];
+                        const float4 bb1 = reinterpret_cast<const float4 *>(sm.xbias[k])[2 * lc + 1];
+                        const float bias8[8] = {bb0.x, bb0.y, bb0.z, bb0.w, bb1.x, bb1.y, bb1.z, bb1.w};
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {  // channel pairs of this 16-byte chunk
+                            float o[2];
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2) {
+                                const int e = 2 * e2 + c2;
+                                const float4 tw = sm.xtap[k][8 * lc + e];
+                                float in[4];
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t wv = reinterpret_cast<const uint32_t *>(&rr[j])[e2];
+                                    const float2 f = unpack_io<IO>(wv);
+                                    in[j] = c2 ? f.y : f.x;
+                                }
+                                float acc = fmaf(tw.w, in[3], fmaf(tw.z, in[2], fmaf(tw.y, in[1], fmaf(tw.x, in[0], bias8[e]))));
+                                o[c2] = p.conv_silu ? silu_fast(acc) : acc;
+                            }
+                            xo[4 * lc + e2] = pack_f16(o[0], o[1]);
+                            so[4 * lc + e2] = pack_f16(o[0] * xscale, o[1] * xscale);
+                        }
+                    }
+                    bar_sync(kBarMath, 128);  // every thread has read its raw rows: the tile may be overwritten
+                    uint8_t *xr = sm.x[k] + i * 128;
+                    uint8_t *sr = sm.xs[k] + i * 128;
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) {
+                        const int off = (lc ^ (i & 7)) << 4;
+                        sts128(xr + off, make_uint4(xo[4 * lc], xo[4 * lc + 1], xo[4 * lc + 2], xo[4 * lc + 3]));
+                        sts128(sr + off, make_uint4(so[4 * lc], so[4 * lc + 1], so[4 * lc + 2], so[4 * lc + 3]));
+                    }
+                } else {
                     uint8_t *xr = sm.x[k] + i * 128;
                     uint8_t *sr = sm.xs[k] + i * 128;
                     uint4 w[8];
@@ -990,7 +1145,7 @@ EncodeTiledFn encode_fn() {
 // box = [1, box_rows, 1, 64 inner], 128B swizzle. Rows past T read as zeros; a chunk's rows past its own
 // sequence read the next sequence and are masked by dt = 0.
 bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t T, int64_t ld,
-              uint32_t box_rows) {
+              uint32_t box_rows, bool swizzle = true) {
     const int64_t L = T, batch = 1;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
@@ -1001,24 +1156,26 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename IO, typename ST>
+template <typename IO, typename ST, bool CONV>
 cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
-    CUtensorMap mx, mb, mc, my;
+    CUtensorMap mx, mb, mc, my, mxh;
     const bool bf = !std::is_same<IO, __half>::value;
     const int64_t T = p.batch * p.L;
     if (!make_map(&mx, p.x, bf, kP, p.H, T, p.x_ld, kQ) || !make_map(&mb, p.B, bf, kN, p.G, T, p.bc_ld, kQ) ||
         !make_map(&mc, p.C, bf, kN, p.G, T, p.bc_ld, kQ) || !make_map(&my, p.y, bf, kP, p.H, T, p.H * kP, 32))
         return cudaErrorInvalidValue;
+    if (CONV ? !make_map(&mxh, p.x, bf, kP, p.H, T, p.x_ld, 3, false) : false) return cudaErrorInvalidValue;
+    if (!CONV) mxh = mx;
     const size_t smem = sizeof(Smem) + 1024;
-    auto k = tc_kernel<IO, ST>;
+    auto k = tc_kernel<IO, ST, CONV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.ctab ? (int64_t)sms : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
-    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, my, hs);
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, mx, mb, mc, my, mxh, hs);
     return cudaGetLastError();
 }
 
@@ -1057,11 +1214,18 @@ int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms) 
     return 1;
 }
 
-cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
+template <bool CONV>
+cudaError_t launch_any(const Params &p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
     if (io_dtype == 1)
-        return state_dtype == 0 ? launch_t<__nv_bfloat16, float>(p, hs, sms, stream)
-                                : launch_t<__nv_bfloat16, __half>(p, hs, sms, stream);
-    return state_dtype == 0 ? launch_t<__half, float>(p, hs, sms, stream) : launch_t<__half, __half>(p, hs, sms, stream);
+        return state_dtype == 0 ? launch_t<__nv_bfloat16, float, CONV>(p, hs, sms, stream)
+                                : launch_t<__nv_bfloat16, __half, CONV>(p, hs, sms, stream);
+    return state_dtype == 0 ? launch_t<__half, float, CONV>(p, hs, sms, stream)
+                            : launch_t<__half, __half, CONV>(p, hs, sms, stream);
+}
+
+cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
+    return p.conv_w ? launch_any<true>(p, io_dtype, state_dtype, hs, sms, stream)
+                    : launch_any<false>(p, io_dtype, state_dtype, hs, sms, stream);
 }
 
 }  // namespace ssd

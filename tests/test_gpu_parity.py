@@ -403,10 +403,12 @@ def test_varlen_bad_offsets_reported_then_recovers():
 from mamba_ssd_prefill_gb300.inputs import make_conv_inputs  # noqa: E402
 
 CONV = [
-    ("tc", "m130-bf16", dict(batch=2, seqlen=333, nheads=4, ngroups=2), 4, "silu"),
-    ("tc", "m130-bf16", dict(batch=1, seqlen=700, nheads=8, io="f16", state="f16", init="none"), 3, "none"),
-    ("simt", "tiny-fp32", dict(batch=2, seqlen=200, nheads=2, init="normal"), 4, "silu"),
-    ("auto", "m130-bf16", dict(batch=3, seqlen=1, nheads=4), 4, "silu"),               # decode step with the cache
+    ("tc", "m130-bf16", dict(batch=2, seqlen=333, nheads=4, ngroups=2), 4, "silu", True),   # fused, ragged, 2 seqs
+    ("tc", "m130-bf16", dict(batch=2, seqlen=333, nheads=4, ngroups=2), 4, "silu", False),  # the same, unfused
+    ("tc", "m130-bf16", dict(batch=3, seqlen=260, nheads=8, io="f16", state="f16"), 4, "none", True),
+    ("tc", "m130-bf16", dict(batch=1, seqlen=700, nheads=8, io="f16", state="f16", init="none"), 3, "none", True),
+    ("simt", "tiny-fp32", dict(batch=2, seqlen=200, nheads=2, init="normal"), 4, "silu", True),
+    ("auto", "m130-bf16", dict(batch=3, seqlen=1, nheads=4), 4, "silu", True),               # decode step, cache
 ]
 
 
@@ -418,22 +420,25 @@ def conv_reference(w, inp, width, act):
                                      None if inp["conv_state"] is None else inp["conv_state"].cpu(), act)
 
 
-@pytest.mark.parametrize("kernel,name,over,width,act", CONV, ids=[f"{c[0]}-{i}" for i, c in enumerate(CONV)])
-def test_conv_then_ssd_parity(kernel, name, over, width, act):
+@pytest.mark.parametrize("kernel,name,over,width,act,fuse", CONV, ids=[f"{c[0]}-{i}" for i, c in enumerate(CONV)])
+def test_conv_then_ssd_parity(kernel, name, over, width, act, fuse):
     w = WORKLOADS[name].with_(**over)
-    inp = make_conv_inputs(w, width, device="cuda", seed=61)
+    inp = make_conv_inputs(w, width, device="cuda", seed=61, conv_state=w.batch != 3)
     ws = m.Workspace("cuda")
     y, fin, cs, xo = m.ssd_fwd_conv(**inp, nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate,
                                     activation=act, chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel=kernel,
-                                    workspace=ws)
+                                    workspace=ws, fuse=fuse)
     m.check(ws)
+    # fused exactly where the tensor-core kernel runs with width 4 (no activation buffer then)
+    assert (xo is None) == (fuse and width == 4 and kernel == "tc")
     yr, fr, csr = conv_reference(w, inp, width, act)
-    assert_parity(w, y, fin, yr, fr, f"conv {kernel} {over}")
+    assert_parity(w, y, fin, yr, fr, f"conv {kernel} {over} fuse={fuse}")
     assert np.array_equal(cs.double().cpu().numpy(), csr)  # the cache holds the raw inputs exactly
-    xr, _ = oracle.conv1d_reference(inp["xbc"].cpu(), inp["conv_weight"].cpu(), inp["conv_bias"].cpu(),
-                                    None if inp["conv_state"] is None else inp["conv_state"].cpu(), act)
-    ok, s = gate_y(xo.double().cpu().numpy(), xr, w.io)  # the convolved rows, rounded once to the I/O dtype
-    assert ok, s
+    if xo is not None:
+        xr, _ = oracle.conv1d_reference(inp["xbc"].cpu(), inp["conv_weight"].cpu(), inp["conv_bias"].cpu(),
+                                        None if inp["conv_state"] is None else inp["conv_state"].cpu(), act)
+        ok, s = gate_y(xo.double().cpu().numpy(), xr, w.io)  # the convolved rows, rounded once to the I/O dtype
+        assert ok, s
 
 
 def test_conv_prefill_then_decode_continues_both_caches():
