@@ -459,3 +459,48 @@ def test_conv_prefill_then_decode_continues_both_caches():
         ys.append(yt)
     assert_parity(w, torch.cat(ys, dim=1), state, yr, fr, "conv prefill + decode")
     assert np.array_equal(cache.double().cpu().numpy(), csr)
+
+
+# ----------------------------------------------------------------------------- CUDA graphs
+def test_cuda_graph_prefill_and_decode_loop():
+    """A prefill call and a loop of eight decode steps (state updated in place) are each captured once in a CUDA
+    graph and replayed: the launches only read their workspace's epoch on the device, so replays need no host
+    work, and they match eager execution bit for bit and the oracle over the whole sequence."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=264, nheads=8, seed=97)
+    inp = make_inputs(w, device="cuda")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    T0, steps = 256, 8
+    pre = dict(inp, **{k: inp[k][:, :T0].contiguous() for k in ("x", "dt_raw", "B", "C")})
+    toks = [dict(inp, **{k: inp[k][:, t:t + 1].contiguous() for k in ("x", "dt_raw", "B", "C")})
+            for t in range(T0, T0 + steps)]
+    wp, wd = w.with_(seqlen=T0), w.with_(seqlen=1)
+    # eager reference run
+    y_e, st_e = run_gpu(wp, pre)
+    ys_e = []
+    for tok in toks:
+        yt, st_e = run_gpu(wd, dict(tok, init_states=st_e), final_states=st_e)
+        ys_e.append(yt)
+    # captured: workspaces and outputs allocated (and the library loaded) before capture
+    ws_p, ws_d = m.Workspace("cuda"), m.Workspace("cuda")
+    ws_p.get(m.workspace_size(m.make_problem(2, T0, 8, 64, 128, 1, 128)))
+    ws_d.get(m.workspace_size(m.make_problem(2, 1, 8, 64, 128, 1, 128)))
+    y_g = torch.empty_like(pre["x"])
+    st_g = torch.empty_like(st_e)
+    ys_g = [torch.empty_like(t["x"]) for t in toks]
+    m.ssd_fwd(**pre, workspace=ws_p, y=y_g, final_states=st_g)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        m.ssd_fwd(**pre, workspace=ws_p, y=y_g, final_states=st_g)
+    with torch.cuda.graph(g2):
+        for tok, yo in zip(toks, ys_g):
+            m.ssd_fwd(**dict(tok, init_states=st_g), workspace=ws_d, y=yo, final_states=st_g)
+    for _ in range(2):  # replays are repeatable: the prefill rewrites the state the decode loop advances
+        g1.replay()
+        g2.replay()
+        torch.cuda.synchronize()
+        m.check(ws_p)
+        m.check(ws_d)
+        assert torch.equal(y_g, y_e) and torch.equal(st_g, st_e)
+        assert all(torch.equal(a, b) for a, b in zip(ys_g, ys_e))
+    assert_parity(w, torch.cat([y_g] + ys_g, dim=1), st_g, yr, fr, "graph replay")
