@@ -41,6 +41,7 @@ struct Plan {
     int64_t nseq = 0;        // sequences: batch (regular) or the cu_seqlens count (variable-length)
     bool varlen = false;
     int heads_per_unit = 1;  // TC only
+    bool late_ticket = false;  // TC only: next ticket taken when the unit before it nears its end
     uint32_t total_units = 0;
     size_t flags_off = 0, ring_off = 0, tab_off = 0, bytes = 0;
 };
@@ -115,6 +116,11 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
             if (hs >= 1 && hs <= 8 && (pr->nheads / pr->ngroups) % hs == 0) pl.heads_per_unit = hs;
         }
         units = (double)pairs * (double)(pr->nheads / pl.heads_per_unit);
+        pl.late_ticket = ssd::tc_late_ticket(pl.nseq * (pr->nheads / pl.heads_per_unit), std::max(1, sm_count()));
+        // test knob: force early (0) or late (1) tickets
+        if (const char *env = getenv("SSD_TC_LATE_TICKET")) {
+            if (env[0] == '0' || env[0] == '1') pl.late_ticket = env[0] == '1';
+        }
     } else {
         units = (double)(varlen ? pl.nc + pl.nseq : pl.nc * pr->batch) * (double)pr->nheads;
     }
@@ -197,6 +203,7 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.heads_per_group = pr.nheads / pr.ngroups;
     p.total_units = pl.total_units;
     p.nseq = pl.nseq;
+    p.tc_late_ticket = pl.late_ticket ? 1 : 0;
     p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
     p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
     if (conv) {  // convolution fused into the tensor-core kernel: x, B, C are slices of the raw rows

@@ -78,6 +78,7 @@ struct Params {
     const int32_t *cu;     // variable-length: token offsets [nseq + 1]; null for a regular batch
     const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
+    int tc_late_ticket;    // tensor-core kernel: take each next ticket only when the unit before it nears its end
 };
 
 // Causal depthwise convolution over the packed token axis (nseq sequences of L tokens, D channels).

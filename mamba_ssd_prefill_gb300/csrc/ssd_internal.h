@@ -31,6 +31,7 @@ size_t tc_flag_bytes(int64_t chains);
 size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype);
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int heads_per_unit);
 int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms);
+bool tc_late_ticket(int64_t units_per_chunk, int sms);  // ticket order = finishing order (chain-bound problems)
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int heads_per_unit, int sms, cudaStream_t stream);
 
 }  // namespace ssd

@@ -67,7 +67,7 @@ struct __align__(1024) Smem {
     float wt[2][kMaxHs][kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
     float dskip[2][kMaxHs];    // D of the unit's heads (0 when absent)
     Sched sched[2];
-    uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty;
+    uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty, unit_go;
     uint64_t x_full[2], x_empty[2], p_full[2], mma1[2], s_free[2], sin_full[2], mma2[2], drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.mma2[i], 1);
         }
         mbar_init(&sm.cb_full, 1);
+        mbar_init(&sm.unit_go, 1);
         mbar_init(&sm.cb_empty, 1);
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
@@ -331,10 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ unit loader
-        // Per unit: ticket (fetched one unit ahead), dt_raw rows, B/C tiles by TMA; and, for the unit
-        // requested one iteration earlier (so its TMA latency is already behind it), the bf16 -> fp16
-        // conversion of B/C in place (same 16-bit positions, same swizzle) and the chunk cumsum
-        // tables of its heads.
+        // Per unit: ticket, dt_raw rows, B/C tiles by TMA; and, for the unit requested one iteration earlier
+        // (so its TMA latency is already behind it), the bf16 -> fp16 conversion of B/C in place (same 16-bit
+        // positions, same swizzle) and the chunk cumsum tables of its heads. Tickets are fetched one unit ahead,
+        // or, when the state chain bounds the launch (few units per chunk index), only once the unit before is
+        // three heads from its end: a ticket taken early sits on a CTA that is busy for a whole unit more, and
+        // the chain reaching that chunk waits for it; late tickets follow the order in which CTAs free up.
         if (lane == 0) {
             prefetch_tensormap(&map_b);
             prefetch_tensormap(&map_c);
@@ -347,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         t = __shfl_sync(0xffffffffu, t, 0);
         Sched prev{0, 0, 0, 0, 0, 0, 0, 0};
         const uint32_t total = total_units(p, (uint32_t)(p.G * slices));
+        const bool late = p.tc_late_ticket != 0;
         bool ok = true;
         // conversion + tables of the unit in stage uu (whose tiles were requested earlier)
         auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
@@ -430,10 +434,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t v = 0; ok; ++v) {
             const uint32_t u = v & 1, nn = v >> 1;
             uint32_t t_next = 0;
-            if (lane == 0 && t < total) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
+            if (!late && lane == 0 && t < total) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
             // the previous unit first: the MMA issuer frees stage u (unit v-2's last C.S) only after it
             // has seen unit v-1 converted
             if (v > 0 && !finish(v - 1, prev)) break;
+            if (late && v > 0) {  // the ticket only now that the unit before it is three heads from its end
+                if (!bwait(&sm.unit_go, (v - 1) & 1, sm, hdr, epoch)) break;
+                if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
+                t = __shfl_sync(0xffffffffu, t, 0);
+            }
             if (t >= total) {
                 if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
                 if (lane == 0) {
@@ -483,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bc_par[u] = nn & 1;
             }
             prev = cur;
-            t = __shfl_sync(0xffffffffu, t_next, 0);
+            if (!late) t = __shfl_sync(0xffffffffu, t_next, 0);
         }
         // teardown: make sure no TMA write into this CTA's shared memory is still in flight
         if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
@@ -886,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader) {
                     mbar_arrive(&sm.p_full[k]);
                     if (hh == hs - 1) mbar_arrive(&sm.cb_empty);
+                    if (hh == (hs > 3 ? hs - 3 : 0)) mbar_arrive(&sm.unit_go);  // late tickets: the next unit
                     TRACE(2, (3u << 24) | hc);
                 }
                 if (pend && !epilogue()) {
@@ -1197,6 +1207,11 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
     (void)state_dtype;
     return (size_t)chains * 2 * (size_t)(P * N) * 4;
 }
+
+// Late tickets pay where few units share a chunk index, so that the state chain bounds the launch (measured on
+// GB300: -13 % at L = 256K and -6 % at L = 16K with 10-16 units per chunk index; +17-24 % at batch 8-32, where
+// the loads then exposed at every unit boundary cost more than the chain).
+bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 8 <= sms; }
 
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {
     (void)G;

@@ -185,6 +185,23 @@ def test_tc_heads_per_unit(hs, monkeypatch):
     assert_parity(w, y, fin, yr, fr, f"tc hs={hs}")
 
 
+@pytest.mark.parametrize("late", ["0", "1"], ids=["early-tickets", "late-tickets"])
+@pytest.mark.parametrize("hs", [1, 2, 8])
+def test_tc_ticket_order(late, hs, monkeypatch):
+    """Work units taken one unit ahead or only when the unit before nears its end (every head count, so the
+    signal comes from the first, a middle and a late head of a unit): same results, and bit for bit the same."""
+    monkeypatch.setenv("SSD_TC_LATE_TICKET", late)
+    monkeypatch.setenv("SSD_TC_HEADS_PER_UNIT", str(hs))
+    w = WORKLOADS["m130-bf16"].with_(batch=3, seqlen=1100, nheads=16, seed=70 + hs)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp, kernel="tc")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"tc late={late} hs={hs}")
+    monkeypatch.setenv("SSD_TC_LATE_TICKET", "1" if late == "0" else "0")
+    y2, f2 = run_gpu(w, inp, kernel="tc")
+    assert torch.equal(y, y2) and torch.equal(fin, f2)
+
+
 def test_tc_no_D_alias_and_determinism():
     w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=600, nheads=8)
     inp = make_inputs(w, device="cuda")
