@@ -197,6 +197,35 @@ SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob, const voi
                                             const float *D, const void *init_states, void *y, void *final_states,
                                             void *stream);
 
+/* The forward pass on host-resident tensors, streamed through the GPU in
+ * pieces so that the host<->device copies overlap the computation (no
+ * counterpart on the pages; a library convenience for batches that live in
+ * host memory).
+ *  pieces       number of pieces (0: the library's choice, 8; at most one
+ *               per chunk). The batch is cut along its tokens at multiples of
+ *               chunk_size, each piece holding the same token range of every
+ *               sequence; the states leaving one piece enter the next (the
+ *               same chunks, in the same order and precision, as one call).
+ *  x, dt_raw, B, C, init_states (optional): host inputs, and y, final_states
+ *               (optional): host outputs, in the layouts of ssd_fwd. Page-locked
+ *               memory lets the copies overlap; pageable memory also works,
+ *               without the overlap.
+ *  dt_bias, A, D   device pointers, as for ssd_fwd.
+ *  scratch      device memory of ssd_fwd_host_scratch_size(prob, pieces)
+ *               bytes, 256-byte aligned, zero-filled once before its first use;
+ *               it begins with the workspace that ssd_fwd_check reads.
+ * The computation runs on `stream`; the copies run on two streams the library
+ * creates once per device and keeps, ordered after the work queued on `stream`
+ * before the call, and `stream` waits for all of them before any later work:
+ * once `stream` is synchronised the outputs are in host memory. The host
+ * buffers must stay valid until then. Problem checks and errors: those of
+ * ssd_fwd. */
+SSD_API ssd_status_t ssd_fwd_host_scratch_size(const ssd_problem_t *prob, int32_t pieces, size_t *bytes);
+SSD_API ssd_status_t ssd_fwd_host(const ssd_problem_t *prob, int32_t pieces, const void *x, const void *dt_raw,
+                                  const float *dt_bias, const float *A, const void *B, const void *C, const float *D,
+                                  const void *init_states, void *y, void *final_states, void *scratch,
+                                  size_t scratch_bytes, void *stream);
+
 /* Which kernel ssd_fwd would run for `prob` (SSD_KERNEL_SIMT or _TC), or a
  * negative ssd_status_t if the problem is rejected. */
 SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob);

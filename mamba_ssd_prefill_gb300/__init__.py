@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["ssd_fwd", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
+__all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
@@ -66,6 +66,10 @@ def lib():
             L.ssd_fwd_varlen.restype = ctypes.c_int
             L.ssd_fwd_conv.argtypes = [pp, ctypes.c_int32, ctypes.c_int32] + [vp] * 14 + [sz, vp]
             L.ssd_fwd_conv.restype = ctypes.c_int
+            L.ssd_fwd_host_scratch_size.restype = ctypes.c_int
+            L.ssd_fwd_host_scratch_size.argtypes = [pp, ctypes.c_int32, ctypes.POINTER(sz)]
+            L.ssd_fwd_host.restype = ctypes.c_int
+            L.ssd_fwd_host.argtypes = [pp, ctypes.c_int32] + [vp] * 10 + [vp, sz, vp]
             L.ssd_fwd_check.argtypes = [vp, vp]
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
@@ -169,6 +173,59 @@ def ssd_fwd(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chunk_size=12
                        _stream_ptr(stream, dev))
     if st:
         raise SsdError(st, "ssd_fwd")
+    return y, final_states
+
+
+def ssd_fwd_host(x, dt_raw, dt_bias, A, B, C, D=None, init_states=None, chunk_size=128, state_dtype=None, *,
+                 pieces=0, y=None, final_states=None, return_final_states=True, scratch=None, kernel="auto",
+                 stream=None):
+    """The forward pass on host-resident tensors, streamed through the GPU in token pieces of the whole batch (the
+    copies of one piece overlap the computation of another; pieces=0 lets the library choose). x, dt_raw, B, C, init_states and the outputs are CPU tensors (page-locked
+    for the overlap: the outputs are allocated page-locked when not given); dt_bias, A, D are CUDA tensors and
+    choose the device. `scratch` is a Workspace (its buffer starts with the workspace that check() reads). The call
+    is asynchronous on `stream`: synchronise it before reading y and the final states."""
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = dt_bias.device
+    if dev.type != "cuda":
+        raise ValueError("ssd_fwd_host: dt_bias, A, D are CUDA tensors (the computation runs on that GPU)")
+    io = x.dtype
+    if state_dtype is None:
+        state_dtype = init_states.dtype if init_states is not None else torch.float32
+    for name, t, shape, dt in (("x", x, (b, L, H, P), io), ("dt_raw", dt_raw, (b, L, H), io),
+                               ("B", B, (b, L, G, N), io), ("C", C, (b, L, G, N), io)):
+        if tuple(t.shape) != shape or t.dtype != dt or t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous CPU {dt} {shape}, got {t.dtype} {tuple(t.shape)} "
+                             f"on {t.device}")
+    for name, t in (("dt_bias", dt_bias), ("A", A), ("D", D)):
+        if t is not None and (tuple(t.shape) != (H,) or t.dtype != torch.float32 or t.device != dev
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name}: expected a contiguous fp32 [H] tensor on {dev}")
+    if init_states is not None and (tuple(init_states.shape) != (b, H, P, N) or init_states.dtype != state_dtype
+                                    or init_states.device.type != "cpu" or not init_states.is_contiguous()):
+        raise ValueError("init_states: expected a contiguous CPU [b, H, P, N] tensor in the state dtype")
+    prob = make_problem(b, L, H, P, N, G, chunk_size, io, state_dtype, kernel)
+    n = ctypes.c_size_t(0)
+    st = lib().ssd_fwd_host_scratch_size(ctypes.byref(prob), int(pieces), ctypes.byref(n))
+    if st:
+        raise SsdError(st, "ssd_fwd_host_scratch_size")
+    if y is None:
+        y = torch.empty(x.shape, dtype=io, pin_memory=True)
+    if final_states is None and return_final_states:
+        final_states = torch.empty(b, H, P, N, dtype=state_dtype, pin_memory=True)
+    for name, t in (("y", y), ("final_states", final_states)):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError(f"{name}: expected a contiguous CPU tensor")
+    if scratch is None:
+        key = ("host", dev.index, torch.cuda.current_stream(dev).cuda_stream if stream is None else stream.cuda_stream)
+        scratch = _default_ws.setdefault(key, Workspace(dev))
+    buf = scratch.get(n.value) if isinstance(scratch, Workspace) else scratch
+    with torch.cuda.device(dev):
+        st = lib().ssd_fwd_host(ctypes.byref(prob), int(pieces), _ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A),
+                                _ptr(B), _ptr(C), _ptr(D), _ptr(init_states), _ptr(y), _ptr(final_states), _ptr(buf),
+                                buf.numel() * buf.element_size(), _stream_ptr(stream, dev))
+    if st:
+        raise SsdError(st, "ssd_fwd_host")
     return y, final_states
 
 

@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libmamba_ssd.so")
-SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_step.cu", "ssd_varlen.cu", "ssd_conv.cu", "ssd_noalloc.cu"]
+SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_step.cu", "ssd_varlen.cu", "ssd_conv.cu", "ssd_noalloc.cu", "ssd_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

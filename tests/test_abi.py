@@ -137,3 +137,33 @@ def test_new_entry_points_reject_bad_arguments_before_any_cuda_call(lib):
     assert lib.ssd_fwd_varlen(ctypes.byref(prob(batch=2)), None, 3, *([None] * 10), None, 0, None) == 1  # batch != 1
     n = ctypes.c_size_t()
     assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(prob(batch=1)), 4, ctypes.byref(n)) == 0 and n.value > 256
+
+
+def test_host_streaming_plan_and_argument_checks(lib):
+    """ssd_fwd_host: the scratch holds the workspace of a piece, two slots of a piece's inputs and outputs and
+    the states carried from piece to piece, so more pieces need less of it; argument errors return before any
+    CUDA call."""
+    n1, n4, n8 = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    p = prob(batch=3, seqlen=1024)
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), 1, ctypes.byref(n1)) == 0
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), 4, ctypes.byref(n4)) == 0
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), 8, ctypes.byref(n8)) == 0
+    assert n1.value > n4.value > n8.value > 0
+    # 4 pieces of 256 tokens: the workspace of [3, 256], three slots (x, y, dt_raw, B, C), the [3, H, P, N] states
+    ws = ctypes.c_size_t()
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(prob(batch=3, seqlen=256)), ctypes.byref(ws)) == 0
+    tok = 3 * 256
+    slot = 2 * tok * 8 * 64 * 2 + tok * 8 * 2 + 2 * tok * 1 * 128 * 2
+    assert n4.value >= ws.value + 3 * slot + 3 * 8 * 64 * 128 * 4
+    # no more pieces than chunks
+    n9, n99 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(prob(batch=1, seqlen=1000)), 8, ctypes.byref(n9)) == 0
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(prob(batch=1, seqlen=1000)), 99, ctypes.byref(n99)) == 0
+    assert n9.value == n99.value
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), -1, ctypes.byref(n1)) == 1      # negative piece count
+    assert lib.ssd_fwd_host(ctypes.byref(p), -1, *([None] * 10), None, 0, None) == 1
+    assert lib.ssd_fwd_host(ctypes.byref(p), 0, *([None] * 10), None, 0, None) == 3       # no scratch
+    bad = prob(batch=2, seqlen=64)
+    bad.nheads = 3                                                                        # not a multiple of G
+    bad.ngroups = 2
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(bad), 0, ctypes.byref(n1)) == 1

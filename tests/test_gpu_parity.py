@@ -521,3 +521,54 @@ def test_cuda_graph_prefill_and_decode_loop():
         assert torch.equal(y_g, y_e) and torch.equal(st_g, st_e)
         assert all(torch.equal(a, b) for a, b in zip(ys_g, ys_e))
     assert_parity(w, torch.cat([y_g] + ys_g, dim=1), st_g, yr, fr, "graph replay")
+
+
+# ----------------------------------------------------------------------------- host-resident batches
+def _pinned(t):
+    return None if t is None else t.cpu().pin_memory()
+
+
+@pytest.mark.parametrize("case", ["batch-5", "one-sequence", "f16-states", "simt-fp32", "pageable"])
+def test_host_streaming_matches_device_call(case):
+    """ssd_fwd_host streams host tensors through the GPU in token pieces of the whole batch, the states running
+    from piece to piece: the same chunks in the same order and precision as one device call, so y and the final
+    states are bit for bit those of ssd_fwd, and within the parity gate of the oracle."""
+    over = {"batch-5": dict(batch=5, seqlen=700, nheads=8),
+            "one-sequence": dict(batch=1, seqlen=1100, nheads=8),
+            "f16-states": dict(batch=2, seqlen=1000, nheads=6, state="f16"),
+            "simt-fp32": dict(batch=2, seqlen=900, nheads=4, io="f32", chunk=64),
+            "pageable": dict(batch=3, seqlen=300, nheads=4)}[case]
+    w = WORKLOADS["m130-bf16"].with_(seed=300 + len(case), **over)
+    inp = make_inputs(w, device="cuda")
+    st = DTYPES[w.state]
+    y_d, f_d = m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=st)
+    host = {k: (v if k in ("dt_bias", "A", "D") else (v.cpu() if case == "pageable" else _pinned(v)))
+            for k, v in inp.items()}
+    scratch = m.Workspace("cuda")
+    y_h, f_h = m.ssd_fwd_host(**host, chunk_size=w.chunk, state_dtype=st, pieces=3 if case == "one-sequence" else 0,
+                              scratch=scratch)
+    torch.cuda.synchronize()
+    m.check(scratch)
+    assert torch.equal(y_h, y_d.cpu()) and torch.equal(f_h, f_d.cpu())
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y_h, f_h, yr, fr, f"host {case}")
+
+
+def test_host_streaming_piece_counts_and_empty():
+    """Every piece count from one to more pieces than there are chunks gives the same result; a sequence of
+    length 0 returns the initial states as the final ones."""
+    w = WORKLOADS["m130-bf16"].with_(batch=1, seqlen=520, nheads=4, seed=333)
+    inp = make_inputs(w, device="cuda")
+    host = {k: (v if k in ("dt_bias", "A", "D") else _pinned(v)) for k, v in inp.items()}
+    y_d, f_d = m.ssd_fwd(**inp, chunk_size=w.chunk)
+    scratch = m.Workspace("cuda")
+    for pieces in (1, 2, 4, 5, 9):
+        y_h, f_h = m.ssd_fwd_host(**host, chunk_size=w.chunk, pieces=pieces, scratch=scratch)
+        torch.cuda.synchronize()
+        assert torch.equal(y_h, y_d.cpu()) and torch.equal(f_h, f_d.cpu()), pieces
+    e = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=0, nheads=4, seed=334)
+    ie = make_inputs(e, device="cuda")
+    he = {k: (v if k in ("dt_bias", "A", "D") else _pinned(v)) for k, v in ie.items()}
+    y0, f0 = m.ssd_fwd_host(**he, chunk_size=e.chunk, scratch=scratch)
+    torch.cuda.synchronize()
+    assert y0.numel() == 0 and torch.equal(f0, he["init_states"])
