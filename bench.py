@@ -48,6 +48,9 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
 def algorithmic(w):
     """Algorithmic bytes and causal MMA flops of one call (on-chip intermediates not counted)."""
     T = w.batch * w.seqlen
@@ -346,7 +349,14 @@ def run_gpu(args, w):
             "traffic": traffic_for(w.name), "peak_kind": kind,
             "roofline_time_us": max(t_mem, t_tc) * 1e6, "algorithmic_bytes": nbytes, "causal_flops": flops}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    if bound == "hbm":  # beside the measured peak: the fraction of the nominal 7.9 TB/s of HBM3e (the stricter one)
+        roof["frac_of_nominal_7900_gbs"] = achieved / NOMINAL_HBM_GBS
     cfg = workload_config(w)
+    # the per-token dt the inputs realise (softplus of dt_raw + dt_bias), outside any timed region
+    with torch.no_grad():
+        dtv = torch.nn.functional.softplus(inp["dt_raw"].float() + inp["dt_bias"].float())
+        cfg["dt_realised"] = [float(dtv.min()), float(dtv.max())]
+        del dtv
     cfg.update({"kernel": kernel, "l2": f"{FLUSH_BYTES >> 20} MiB buffer written before every step, outside the events",
                 "wall_s_timed_region": round(wall, 3)})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
