@@ -1209,23 +1209,25 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
 }
 
 // Late tickets pay where few units share a chunk index, so that the state chain bounds the launch (measured on
-// GB300: -13 % at L = 256K and -6 % at L = 16K with 10-16 units per chunk index; +17-24 % at batch 8-32, where
-// the loads then exposed at every unit boundary cost more than the chain).
-bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 8 <= sms; }
+// GB300: -13 % at L = 256K and -6 % at L = 16K with 10-16 units per chunk index, -7 % on the 130M-shaped batch
+// with 32; +17-24 % at batch 8-32 with 80 and more, where the loads then exposed at every unit boundary cost more
+// than the chain).
+bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 4 <= sms; }
 
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {
     (void)G;
     return (uint32_t)(nc * batch * (H / hs));
 }
 
-// Heads per work unit: the largest divisor of heads-per-group (<= 8) that still leaves at least five units per
+// Heads per work unit: the largest divisor of heads-per-group (<= 8) that still leaves at least six units per
 // SM; small problems fall back to 1. More heads per unit share one C.B^T and one B/C load; more units spread the
-// chunk-serial state chain over more SMs (measured on GB300: 4 heads beat 8 by 8-9 % where 8 left 2.5-4 units per
-// SM, 8 beat 4 by 8 % at 33 units per SM).
+// chunk-serial state chain over more SMs (measured on GB300: the 130M-shaped batch runs 3 heads per unit 7-9 %
+// faster than 4 with late tickets; 4 beat 8 by 8-9 % where 8 left 2.5-4 units per SM; 8 beat 4 by 8 % at 33 units
+// per SM).
 int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms) {
     const int64_t hpg = H / G;
     for (int d = kMaxHs; d >= 1; --d)
-        if (hpg % d == 0 && nc * batch * (H / d) >= 5 * (int64_t)sms) return d;
+        if (hpg % d == 0 && nc * batch * (H / d) >= 6 * (int64_t)sms) return d;
     return 1;
 }
 
