@@ -26,8 +26,10 @@
  *   page, section 2.2)
  *
  * Ownership: the caller owns every buffer, including the workspace; the
- * library allocates no device memory and keeps no per-call global state.
- * All pointers except the workspace and the stream are device pointers.
+ * library allocates no device memory and keeps no per-call global state
+ * (ssd_fwd_host keeps two copy streams per device for the process's life).
+ * Tensor pointers are device pointers, except the host tensors of
+ * ssd_fwd_host.
  *
  * Errors: argument errors are detected on the host, return immediately and
  * launch nothing. The launch itself is asynchronous on `stream`; a device-side
