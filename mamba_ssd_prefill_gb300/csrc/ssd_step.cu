@@ -16,6 +16,7 @@
 // grid-stride loop over chains. No workspace and no inter-CTA ordering.
 #include <type_traits>
 
+#include "sm100_ptx.cuh"
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -118,8 +119,188 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
     }
 }
 
+// Staged form for rows of 128, 256 or 512 bytes: persistent CTAs (2 per SM with fp32 states, 4 with fp16 ones)
+// keep several chains' states in flight in shared memory. Thread 0 loads a chain's state (P x N, contiguous)
+// together with its B and C rows and its x by plain bulk copies onto one mbarrier, `stages - 1` chains ahead;
+// the warps update the state in place (a lane owns a 16-byte vector of a row, LPR lanes a row), write y, and
+// thread 0 sends the state back by one bulk store. The bytes in flight are the stages', not registers', and the
+// CTAs of an SM overlap each other's per-chain latencies (measured on GB300: 64 x 80 fp32 states 0.068 -> 0.061
+// ms, 256 x 80 fp16 states 0.205 -> 0.121 ms against the register-only form).
+constexpr int kBulkThreads = 256;
+template <typename ST> constexpr int bulk_ctas() { return sizeof(ST) == 4 ? 2 : 4; }
+template <typename ST> constexpr uint32_t bulk_smem() { return 200u * 1024u / bulk_ctas<ST>(); }  // per CTA
+
+__device__ __noinline__ void step_pipe_error(WsHeader *hdr) {
+    if (atomicCAS(&hdr->status, 0u, (uint32_t)DEV_PIPE) == 0u) hdr->err_where = WAIT_PIPE;
+}
+
+template <typename IO, typename ST, int LPR>
+__global__ void __launch_bounds__(kBulkThreads, bulk_ctas<ST>()) step_bulk_kernel(Params p, int stages, uint32_t stride) {
+    using namespace sm100;
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int V = 16 / (int)sizeof(ST), RPW = 32 / LPR, kWarpsB = kBulkThreads / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane / LPR, l = lane % LPR;
+    const IO *x = static_cast<const IO *>(p.x);
+    const IO *dtr = static_cast<const IO *>(p.dt_raw);
+    const IO *Bm = static_cast<const IO *>(p.B);
+    const IO *Cm = static_cast<const IO *>(p.C);
+    const ST *hin = static_cast<const ST *>(p.init);
+    ST *hout = static_cast<ST *>(p.final_states);
+    IO *y = static_cast<IO *>(p.y);
+    const uint32_t SB = (uint32_t)(p.P * p.N * sizeof(ST)), BB = (uint32_t)(p.N * sizeof(IO));
+    const uint32_t XB = (uint32_t)(p.P * sizeof(IO));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stride);
+    const int64_t chains = p.batch * p.H;
+    const int64_t mine = blockIdx.x < chains ? (chains - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // thread 0: chain j's state, B and C rows and x into stage j % stages
+    auto issue = [&](int64_t j) {
+        const int st = (int)(j % stages);
+        const int64_t ch = blockIdx.x + j * gridDim.x;
+        const int64_t b = ch / p.H, h = ch % p.H, g = h / p.heads_per_group;
+        uint8_t *base = smem + (size_t)st * stride;
+        mbar_arrive_expect_tx(&full[st], (hin ? SB : 0u) + 2 * BB + XB);
+        if (hin) bulk_load(base, hin + ch * p.P * p.N, SB, &full[st]);
+        bulk_load(base + SB, Bm + b * p.bc_ld + g * p.N, BB, &full[st]);
+        bulk_load(base + SB + BB, Cm + b * p.bc_ld + g * p.N, BB, &full[st]);
+        bulk_load(base + SB + 2 * BB, x + b * p.x_ld + h * p.P, XB, &full[st]);
+    };
+    int64_t issued = 0;
+    if (tid == 0)
+        for (; issued < stages - 1 && issued < mine; ++issued) issue(issued);
+    bool failed = false;
+    int64_t j = 0;
+    for (; j < mine; ++j) {
+        const int st = (int)(j % stages);
+        const int64_t ch = blockIdx.x + j * gridDim.x;
+        const int64_t h = ch % p.H;
+        // bounded wait for the stage (every thread; the outcome is made uniform below)
+        if (!mbar_try_wait(&full[st], (uint32_t)((j / stages) & 1))) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&full[st], (uint32_t)((j / stages) & 1)))
+                if (globaltimer() - t0 > kDefaultTimeoutNs) {
+                    failed = true;
+                    break;
+                }
+        }
+        if (!failed) {
+            const float dt = softplus_f32(to_f32(dtr[ch]) + p.dt_bias[h]);
+            const float a = expf(dt * p.A[h]);
+            const float Dh = p.D ? p.D[h] : 0.f;
+            uint8_t *base = smem + (size_t)st * stride;
+            ST *S = reinterpret_cast<ST *>(base);
+            const IO *Bs = reinterpret_cast<const IO *>(base + SB);
+            const IO *Cs = Bs + p.N;
+            const IO *xs = reinterpret_cast<const IO *>(base + SB + 2 * BB);
+            float bv[V], cv[V];
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                bv[i] = to_f32(Bs[l * V + i]);
+                cv[i] = to_f32(Cs[l * V + i]);
+            }
+            for (int r = warp * RPW + sub; r < p.P; r += kWarpsB * RPW) {
+                const float xv = to_f32(xs[r]);
+                float hv[V];
+                ST *row = S + (int64_t)r * p.N + l * V;
+                if (hin) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(row);
+                    const ST *e = reinterpret_cast<const ST *>(&u);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) hv[i] = to_f32(e[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < V; ++i) hv[i] = 0.f;
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    hv[i] = fmaf(a, hv[i], dt * xv * bv[i]);
+                    acc = fmaf(cv[i], hv[i], acc);
+                }
+                if (hout) {
+                    uint4 u;
+                    ST *e = reinterpret_cast<ST *>(&u);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) e[i] = from_f32<ST>(hv[i]);
+                    *reinterpret_cast<uint4 *>(row) = u;
+                }
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (l == 0) y[ch * p.P + r] = from_f32<IO>(fmaf(Dh, xv, acc));
+            }
+            if (hout) fence_proxy_async_smem();  // the updated rows, for the bulk store
+        }
+        if (__syncthreads_or(failed)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            if (hout) {
+                bulk_store(hout + ch * p.P * p.N, smem + (size_t)st * stride, SB);
+                bulk_commit();
+            }
+            // refill the stage of chain j - 1 (its store has been issued one chain ago) with chain j + stages - 1
+            if (issued < mine) {
+                if (hout) bulk_wait_read1();
+                issue(issued);
+                ++issued;
+            }
+        }
+    }
+    if (tid == 0) {
+        if (failed) {  // record it, and let the loads still in flight land before the shared memory is released
+            step_pipe_error(p.hdr);
+            for (int64_t k = j; k < issued; ++k) {
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&full[k % stages], (uint32_t)((k / stages) & 1)) &&
+                       globaltimer() - t0 < 100000000ull) {
+                }
+            }
+        }
+        bulk_wait0();  // every state store has completed
+    }
+}
+
+template <typename IO, typename ST, int LPR>
+cudaError_t launch_bulk(const Params &p, int sms, cudaStream_t stream) {
+    const uint32_t SB = (uint32_t)(p.P * p.N * sizeof(ST)), BB = (uint32_t)(p.N * sizeof(IO));
+    const uint32_t XB = (uint32_t)(p.P * sizeof(IO));
+    const uint32_t stride = (SB + 2 * BB + XB + 127) / 128 * 128;
+    const int stages = (int)std::min<uint32_t>(8u, bulk_smem<ST>() / stride);
+    const size_t smem = (size_t)stages * stride + 8 * (size_t)stages;
+    auto k = step_bulk_kernel<IO, ST, LPR>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(p.batch * p.H, (int64_t)sms * bulk_ctas<ST>());
+    k<<<(unsigned)grid, kBulkThreads, smem, stream>>>(p, stages, stride);
+    return cudaGetLastError();
+}
+
+// The staged kernel takes rows of 128, 256 or 512 bytes whose state, B, C and x rows all start on 16 bytes and
+// at least two stages of them fit in a CTA's share of shared memory.
+template <typename IO, typename ST>
+bool bulk_ok(const Params &p) {
+    const int64_t row = p.N * (int64_t)sizeof(ST), es = sizeof(IO);
+    const uint64_t stride = ((uint64_t)(p.P * p.N * sizeof(ST) + 2 * p.N * es + p.P * es) + 127) / 128 * 128;
+    const bool al = ((reinterpret_cast<uintptr_t>(p.init) | reinterpret_cast<uintptr_t>(p.final_states) |
+                      reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.B) |
+                      reinterpret_cast<uintptr_t>(p.C)) % 16) == 0;
+    return al && (row == 128 || row == 256 || row == 512) && (p.N * es) % 16 == 0 && (p.P * es) % 16 == 0 &&
+           (p.bc_ld * es) % 16 == 0 && (p.x_ld * es) % 16 == 0 && 2 * stride <= bulk_smem<ST>() && p.P <= (1 << 20);
+}
+
 template <typename IO, typename ST>
 cudaError_t launch_t(const Params &p, int sms, cudaStream_t stream) {
+    if (bulk_ok<IO, ST>(p)) {
+        const int64_t lpr = p.N * (int64_t)sizeof(ST) / 16;
+        if (lpr == 32) return launch_bulk<IO, ST, 32>(p, sms, stream);
+        if (lpr == 16) return launch_bulk<IO, ST, 16>(p, sms, stream);
+        return launch_bulk<IO, ST, 8>(p, sms, stream);
+    }
     const int64_t chains = p.batch * p.H;
     const int64_t grid = std::min<int64_t>(chains, (int64_t)sms * 16);
     // 16-byte state vectors (8-byte for short rows) need the row length to be a multiple of the vector and aligned

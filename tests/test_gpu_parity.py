@@ -296,6 +296,9 @@ STEP = [
     ("tiny-fp32", dict(batch=2, nheads=3, ngroups=3, init="normal")),                  # fp32, N = 64
     ("m130-bf16", dict(batch=2, nheads=2, headdim=24, dstate=100)),                    # N % 4 != 0: element-wise
     ("m130-bf16", dict(batch=64, nheads=80, init="none")),                             # no cached state yet
+    ("m130-bf16", dict(batch=3, nheads=4, dstate=32)),                                 # 128-byte fp32 rows
+    ("m130-bf16", dict(batch=2, nheads=4, dstate=64, state="f16")),                    # 128-byte fp16 rows
+    ("m130-bf16", dict(batch=700, nheads=5, headdim=32, dstate=64, ngroups=5)),        # many chains per CTA
 ]
 
 
@@ -319,6 +322,16 @@ def test_step_in_place_without_D():
     y, fin = run_gpu(w, dict(inp, init_states=state), final_states=state)
     assert fin.data_ptr() == state.data_ptr()
     assert_parity(w, y, fin, yr, fr)
+
+
+@pytest.mark.parametrize("state", ["f32", "f16"])
+def test_step_without_final_states(state):
+    """A step that returns y only (no state written) gives the same y as one that also writes the state."""
+    w = WORKLOADS["m130-bf16"].with_(batch=9, seqlen=1, nheads=8, state=state, seed=95)
+    inp = make_inputs(w, device="cuda")
+    y_full, _ = run_gpu(w, inp)
+    y_only, fin = run_gpu(w, inp, return_final_states=False)
+    assert fin is None and torch.equal(y_only, y_full)
 
 
 @pytest.mark.parametrize("state", ["f32", "f16"])
