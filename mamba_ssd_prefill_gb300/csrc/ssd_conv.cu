@@ -9,10 +9,11 @@
 // or SiLU, v * sigmoid(v). The channels are the x | B | C concatenation of the
 // SSD inputs, so the SSD reads x, B and C as column slices of the output.
 //
-// HBM-bound: a thread walks 32 tokens of one 16-byte vector of channels with
-// the taps and the last k - 1 inputs in registers, so every input is read once;
-// fp32 arithmetic. A second kernel writes the cache for continuing each
-// sequence.
+// HBM-bound: tiles of 64 tokens x 512 bytes of channels, with the k - 1 rows before them, go through shared
+// memory in a 3-stage pipeline of 16-byte asynchronous copies (rows outside the sequence zero-filled), two
+// CTAs per SM; a thread walks 32 tokens of one 4-byte column of the tile (two 16-bit channels or one fp32 one)
+// with the taps and the last k - 1 inputs in registers, fp32 arithmetic, and stores rows coalesced. A second
+// kernel writes the cache for continuing each sequence.
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -20,85 +21,146 @@ namespace ssd {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTileT = 64;      // tokens per tile
+constexpr int kTileB = 512;     // bytes of channels per tile row
+constexpr int kStages = 3;
+constexpr int kCols = kTileB / 4;  // 4-byte columns per tile row (one per thread, two token halves)
 
-template <typename IO> __device__ __forceinline__ void load_vec(const IO *p, float (&f)[16 / sizeof(IO)]) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(p);
-    const IO *e = reinterpret_cast<const IO *>(&u);
-#pragma unroll
-    for (int i = 0; i < (int)(16 / sizeof(IO)); ++i) f[i] = to_f32(e[i]);
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-constexpr int kTokens = 32;  // tokens per thread: the taps and the window of the last k - 1 inputs stay in registers
-
-// Inputs before token tt of sequence s for window slot j (token tt - 1 - j): from the rows, else the cache, else 0.
-template <typename IO, int V>
-__device__ __forceinline__ void load_before(const ConvParams &c, const IO *in, const IO *state, int64_t s, int64_t tt,
-                                            int64_t c0, int j, float (&v)[V]) {
-    const int64_t tp = tt - 1 - j;
-    if (tp >= 0) {
-        load_vec<IO>(in + (s * c.L + tp) * c.D + c0, v);
-    } else {
-#pragma unroll
-        for (int i = 0; i < V; ++i) v[i] = state ? to_f32(state[((s * c.D) + c0 + i) * (c.k - 1) + (c.k - 1 + tp)]) : 0.f;
+template <typename IO> struct Col;  // a 4-byte column: two 16-bit channels or one fp32 channel
+template <> struct Col<float> {
+    static constexpr int C = 1;
+    __device__ static void load(const uint8_t *p, float (&v)[1]) { v[0] = *reinterpret_cast<const float *>(p); }
+    __device__ static uint32_t pack(const float (&v)[1]) { return __float_as_uint(v[0]); }
+};
+template <> struct Col<__nv_bfloat16> {
+    static constexpr int C = 2;
+    __device__ static void load(const uint8_t *p, float (&v)[2]) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+        v[0] = f.x;
+        v[1] = f.y;
     }
-}
+    __device__ static uint32_t pack(const float (&v)[2]) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+template <> struct Col<__half> {
+    static constexpr int C = 2;
+    __device__ static void load(const uint8_t *p, float (&v)[2]) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(p));
+        v[0] = f.x;
+        v[1] = f.y;
+    }
+    __device__ static uint32_t pack(const float (&v)[2]) {
+        __half2 h = __floats2half2_rn(v[0], v[1]);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
 
-// One thread: a 16-byte vector of channels over kTokens consecutive tokens (a warp covers 512 contiguous bytes of
-// each token's row). The window restarts at a sequence start.
 template <typename IO, int K>
-__global__ void __launch_bounds__(kThreads) conv_kernel(ConvParams c) {
-    constexpr int V = 16 / sizeof(IO);
-    const IO *in = static_cast<const IO *>(c.in);
+__global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int R = kTileT + K - 1;  // rows per stage: the tile and the k - 1 before it
+    constexpr int STAGE = R * kTileB;
+    constexpr int NC = Col<IO>::C;
+    const int tid = threadIdx.x;
+    const int64_t rowb = c.D * (int64_t)sizeof(IO);  // bytes of one token row
+    const int64_t ctiles = (rowb + kTileB - 1) / kTileB, ttiles = (c.L + kTileT - 1) / kTileT;
+    const int64_t items = c.nseq * ttiles * ctiles;
+    const uint8_t *in = static_cast<const uint8_t *>(c.in);
     const IO *state = static_cast<const IO *>(c.state);
-    IO *out = static_cast<IO *>(c.out);
-    const int64_t groups = c.D / V, blocks = (c.T + kTokens - 1) / kTokens, total = blocks * groups;
-    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < total; e += (int64_t)gridDim.x * kThreads) {
-        const int64_t t0 = (e / groups) * kTokens, c0 = (e % groups) * V;
-        float w[K][V], bias[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            bias[i] = c.bias ? c.bias[c0 + i] : 0.f;
-#pragma unroll
-            for (int j = 0; j < K; ++j) w[j][i] = c.w[(c0 + i) * K + j];
+    uint8_t *out = static_cast<uint8_t *>(c.out);
+    // item -> (sequence, token tile, channel tile), channel tiles fastest
+    auto load = [&](int64_t it, int st) {
+        const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
+        const int64_t t0 = tt * kTileT - (K - 1), cbyte = cb * kTileB;
+        uint8_t *dst = smem + st * STAGE;
+        const uint8_t *src = in + sq * c.L * rowb + cbyte;
+        for (int q = tid; q < R * (kTileB / 16); q += kThreads) {
+            const int r = q / (kTileB / 16), off = (q % (kTileB / 16)) * 16;
+            const int64_t t = t0 + r;
+            const bool valid = t >= 0 && t < c.L && cbyte + off < rowb;
+            cp_async16(dst + r * kTileB + off, valid ? src + t * rowb + off : in, valid ? 16u : 0u);
         }
-        float hist[K > 1 ? K - 1 : 1][V];  // hist[j] = input of token t - 1 - j
-        int64_t s = t0 / c.L, tt = t0 % c.L;
+    };
+    const int col = tid % kCols, half = tid / kCols;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    for (int k = 0; k < kStages - 1; ++k) {
+        if (first + k * step < items) load(first + k * step, k);
+        cp_async_commit();
+    }
+    for (int64_t n = 0;; ++n) {
+        const int64_t it = first + n * step;
+        if (it >= items) break;
+        cp_async_wait<kStages - 2>();  // this thread's copies of item n have landed
+        __syncthreads();               // everyone's; and stage (n - 1) % kStages has been read by everyone
+        {
+            const int64_t nx = first + (n + kStages - 1) * step;
+            if (nx < items) load(nx, (int)((n + kStages - 1) % kStages));
+            cp_async_commit();
+        }
+        const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
+        const int64_t cbyte = cb * kTileB + col * 4;
+        if (cbyte >= rowb) continue;  // past the last channel
+        const int64_t ch0 = cbyte / (int64_t)sizeof(IO);
+        const uint8_t *tile = smem + (int)(n % kStages) * STAGE + col * 4;
+        const int64_t tb = tt * kTileT + half * (kTileT / 2);  // first token of this thread's half
+        const int64_t te = tb + kTileT / 2 < c.L ? tb + kTileT / 2 : c.L;
+        if (tb >= te) continue;
+        float w[K][NC], bias[NC];
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) load_before<IO, V>(c, in, state, s, tt, c0, j, hist[j]);
-        const int64_t t1 = t0 + kTokens < c.T ? t0 + kTokens : c.T;
-#pragma unroll 4
-        for (int64_t t = t0; t < t1; ++t) {
-            if (t != t0 && tt == 0) {  // a new sequence starts: its window comes from its cache
+        for (int i = 0; i < NC; ++i) {
+            bias[i] = c.bias ? c.bias[ch0 + i] : 0.f;
 #pragma unroll
-                for (int j = 0; j < K - 1; ++j) load_before<IO, V>(c, in, state, s, 0, c0, j, hist[j]);
+            for (int j = 0; j < K; ++j) w[j][i] = c.w[(ch0 + i) * K + j];
+        }
+        // hist[j] = input of token t - 1 - j: from the tile (rows before the sequence are zeros there), or the cache
+        float hist[K > 1 ? K - 1 : 1][NC];
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int64_t tp = tb - 1 - j;
+            if (tp >= 0 || !state) {
+                Col<IO>::load(tile + (int)(tp - (tt * kTileT - (K - 1))) * kTileB, hist[j]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < NC; ++i) hist[j][i] = to_f32(state[((sq * c.D) + ch0 + i) * (K - 1) + (K - 1 + tp)]);
             }
-            float v[V], acc[V];
-            load_vec<IO>(in + t * c.D + c0, v);
+        }
+        uint8_t *orow = out + (sq * c.L + tb) * rowb + cbyte;
+        const uint8_t *irow = tile + (int)(tb - (tt * kTileT - (K - 1))) * kTileB;
+#pragma unroll 4
+        for (int64_t t = tb; t < te; ++t) {
+            float v[NC], acc[NC];
+            Col<IO>::load(irow, v);
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
+            for (int i = 0; i < NC; ++i) {
                 acc[i] = fmaf(w[K - 1][i], v[i], bias[i]);
 #pragma unroll
                 for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
+                if (c.silu) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
             }
-            uint4 o;
-            IO *oe = reinterpret_cast<IO *>(&o);
-#pragma unroll
-            for (int i = 0; i < V; ++i) oe[i] = from_f32<IO>(c.silu ? __fdividef(acc[i], 1.f + __expf(-acc[i])) : acc[i]);
-            *reinterpret_cast<uint4 *>(out + t * c.D + c0) = o;
+            *reinterpret_cast<uint32_t *>(orow) = Col<IO>::pack(acc);
 #pragma unroll
             for (int j = K - 2; j > 0; --j)
 #pragma unroll
-                for (int i = 0; i < V; ++i) hist[j][i] = hist[j - 1][i];
+                for (int i = 0; i < NC; ++i) hist[j][i] = hist[j - 1][i];
             if (K > 1) {
 #pragma unroll
-                for (int i = 0; i < V; ++i) hist[0][i] = v[i];
+                for (int i = 0; i < NC; ++i) hist[0][i] = v[i];
             }
-            if (++tt == c.L) {
-                tt = 0;
-                ++s;
-            }
+            irow += kTileB;
+            orow += rowb;
         }
     }
+    cp_async_wait<0>();
 }
 
 // The cache for continuing each sequence: its last k - 1 inputs per channel (from the cache given on entry where the
@@ -124,24 +186,34 @@ __global__ void __launch_bounds__(kThreads) conv_state_kernel(ConvParams c) {
     }
 }
 
+template <typename IO, int K>
+cudaError_t launch_k(const ConvParams &c, int sms, cudaStream_t stream) {
+    const size_t smem = (size_t)kStages * (kTileT + K - 1) * kTileB;
+    auto k = conv_kernel<IO, K>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t rowb = c.D * (int64_t)sizeof(IO);
+    const int64_t items = c.nseq * ((c.L + kTileT - 1) / kTileT) * ((rowb + kTileB - 1) / kTileB);
+    const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(c);
+    return cudaGetLastError();
+}
+
 template <typename IO>
 cudaError_t launch_t(const ConvParams &c, int sms, cudaStream_t stream) {
-    constexpr int V = 16 / sizeof(IO);
-    const int64_t total = (c.T + kTokens - 1) / kTokens * (c.D / V);
-    if (total > 0) {
-        const int64_t grid = std::min<int64_t>((total + kThreads - 1) / kThreads, (int64_t)sms * 16);
+    if (c.T > 0) {
+        cudaError_t e;
         switch (c.k) {
-            case 1: conv_kernel<IO, 1><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 2: conv_kernel<IO, 2><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 3: conv_kernel<IO, 3><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 4: conv_kernel<IO, 4><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 5: conv_kernel<IO, 5><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 6: conv_kernel<IO, 6><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 7: conv_kernel<IO, 7><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
-            case 8: conv_kernel<IO, 8><<<(unsigned)grid, kThreads, 0, stream>>>(c); break;
+            case 1: e = launch_k<IO, 1>(c, sms, stream); break;
+            case 2: e = launch_k<IO, 2>(c, sms, stream); break;
+            case 3: e = launch_k<IO, 3>(c, sms, stream); break;
+            case 4: e = launch_k<IO, 4>(c, sms, stream); break;
+            case 5: e = launch_k<IO, 5>(c, sms, stream); break;
+            case 6: e = launch_k<IO, 6>(c, sms, stream); break;
+            case 7: e = launch_k<IO, 7>(c, sms, stream); break;
+            case 8: e = launch_k<IO, 8>(c, sms, stream); break;
             default: return cudaErrorInvalidValue;
         }
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (c.state_out && c.k > 1 && c.nseq * c.D > 0) {
