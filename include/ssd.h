@@ -171,7 +171,16 @@ SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);
  *  timeout_ns     limit of every device-side wait (0 restores the 2 s default)
  *  skip_publish   chunk index whose state publish is skipped, so that the next
  *                 chunk's wait runs out (-1 disables). Host-armed fault
- *                 injection: no memory fault, no trap, the kernel returns. */
+ *                 injection: no memory fault, no trap, the kernel returns.
+ *                 -2 instead arms the probe of the bounds-checked debug build
+ *                 (compiled with SSD_BOUNDS_CHECK): the tensor-core kernel's
+ *                 dt_raw indices are planted one extent past the end, the
+ *                 check redirects them to the buffer's start and records the
+ *                 violation, and ssd_fwd_check returns SSD_ERR_DEVICE; release
+ *                 builds ignore it.
+ * In the bounds-checked build every kernel compares its global indices with
+ * the buffers' extents; an index outside is never used (the access goes to
+ * the buffer's first element) and ssd_fwd_check reports SSD_ERR_DEVICE. */
 SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream);
 
 /* ssd_fwd without a workspace argument, for callers that cannot allocate

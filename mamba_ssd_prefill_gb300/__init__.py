@@ -18,7 +18,8 @@ import torch
 __all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
+# MAMBA_SSD_LIB selects another build of the library (the bounds-checked debug build, libmamba_ssd_checked.so)
+LIB_PATH = os.environ.get("MAMBA_SSD_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba_ssd.so")
 
 _DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 _KERNEL = {"auto": 0, "simt": 1, "tc": 2, "step": 3}

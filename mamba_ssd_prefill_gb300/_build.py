@@ -10,6 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libmamba_ssd.so")
+LIB_CHECKED = os.path.join(PKG, "libmamba_ssd_checked.so")  # debug build: every kernel's global indices range-checked
 SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_step.cu", "ssd_varlen.cu", "ssd_conv.cu", "ssd_noalloc.cu", "ssd_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -24,11 +25,15 @@ def flags(extra=()):
             "-I", os.path.join(ROOT, "include"), *extra]
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every translation unit in parallel and link libmamba_ssd.so."""
-    objdir = os.path.join(PKG, "_build")
+def build(verbose: bool = False, ptxas_info: bool = False, checked: bool = False) -> str:
+    """Compile every translation unit in parallel and link libmamba_ssd.so (checked: the bounds-checked debug
+    library libmamba_ssd_checked.so, in which an out-of-range global index is reported instead of used)."""
+    objdir = os.path.join(PKG, "_build_checked" if checked else "_build")
     os.makedirs(objdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if checked:
+        extra.append("-DSSD_BOUNDS_CHECK")
+    out = LIB_CHECKED if checked else LIB
 
     def compile_one(src):
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
@@ -42,13 +47,13 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -203,6 +203,8 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.heads_per_group = pr.nheads / pr.ngroups;
     p.total_units = pl.total_units;
     p.nseq = pl.nseq;
+    p.ring_bytes = (int64_t)(pl.tab_off - pl.ring_off);
+    p.flag_count = (int64_t)((pl.ring_off - pl.flags_off) / sizeof(uint64_t));
     p.tc_late_ticket = pl.late_ticket ? 1 : 0;
     p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
     p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
@@ -304,6 +306,8 @@ SSD_API ssd_status_t ssd_fwd_conv(const ssd_problem_t *prob, int32_t conv_width,
     const int sms = sm_count();
     if (sms <= 0) return SSD_ERR_CUDA;
     ssd::ConvParams c;
+    memset(&c, 0, sizeof(c));
+    c.hdr = static_cast<WsHeader *>(workspace);
     c.in = xbc;
     c.w = conv_weight;
     c.bias = conv_bias;
@@ -353,7 +357,7 @@ SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream) {
     if (cudaMemset(&hdr->status, 0, sizeof(status)) != cudaSuccess) return SSD_ERR_CUDA;
     if (status == ssd::DEV_TIMEOUT) return SSD_ERR_TIMEOUT;
     if (status == ssd::DEV_BAD_SEQLENS) return SSD_ERR_INVALID_ARG;
-    return SSD_ERR_DEVICE;
+    return SSD_ERR_DEVICE;  // DEV_PIPE, or DEV_BOUNDS from a bounds-checked build
 }
 
 SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream) {
@@ -364,6 +368,9 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
         return SSD_ERR_CUDA;
     const int64_t stored = skip_publish < 0 ? 0 : skip_publish + 1;  // 0 = off (zero-filled workspace)
     if (cudaMemcpy(&hdr->skip_publish, &stored, sizeof(stored), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    const uint32_t probe = skip_publish == -2 ? 1u : 0u;  // bounds-checked builds: plant one index past its end
+    if (cudaMemcpy(&hdr->bounds_probe, &probe, sizeof(probe), cudaMemcpyHostToDevice) != cudaSuccess)
         return SSD_ERR_CUDA;
     return SSD_OK;
 }

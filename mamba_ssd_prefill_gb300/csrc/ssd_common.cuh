@@ -29,7 +29,9 @@ struct WsHeader {
     uint32_t err_where;   // which wait gave up (WAIT_* below)
     uint64_t timeout_ns;  // limit of every device wait, 0 = default
     int64_t skip_publish; // test hook: 1 + chunk whose publish is skipped (0 = off, the zero-filled state)
-    uint32_t pad[52];
+    uint32_t bounds_probe;  // test hook of bounds-checked builds: 1 = one checked index is planted one past its end
+    uint32_t err_index_lo, err_index_hi;  // bounds-checked builds: the first rejected index
+    uint32_t pad[49];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -41,7 +43,16 @@ enum WaitSite : uint32_t {
     WAIT_PIPE = 2,    // intra-CTA mbarrier (tensor-core kernel)
 };
 
-enum DevStatus : uint32_t { DEV_OK = 0, DEV_BAD_SEQLENS = 1, DEV_TIMEOUT = 5, DEV_PIPE = 6 };
+enum DevStatus : uint32_t { DEV_OK = 0, DEV_BAD_SEQLENS = 1, DEV_TIMEOUT = 5, DEV_PIPE = 6, DEV_BOUNDS = 7 };
+
+// Access sites of the bounds-checked builds (recorded in err_where with DEV_BOUNDS).
+enum BoundsSite : uint32_t {
+    SITE_TC_DT = 101, SITE_TC_Y = 102, SITE_TC_INIT = 103, SITE_TC_FINAL = 104, SITE_TC_RING = 105, SITE_TC_FLAG = 106,
+    SITE_SIMT_IN = 111, SITE_SIMT_Y = 112, SITE_SIMT_INIT = 113, SITE_SIMT_FINAL = 114, SITE_SIMT_RING = 115,
+    SITE_SIMT_FLAG = 116,
+    SITE_STEP_IN = 121, SITE_STEP_Y = 122, SITE_STEP_STATE = 123,
+    SITE_CONV_IN = 131, SITE_CONV_OUT = 132, SITE_CONV_STATE = 133,
+};
 
 // Parameters common to the kernels. Element strides are implied by the packed
 // layouts documented in ssd.h. Tokens are addressed on one packed axis: a
@@ -79,6 +90,7 @@ struct Params {
     const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
     int tc_late_ticket;    // tensor-core kernel: take each next ticket only when the unit before it nears its end
+    int64_t ring_bytes, flag_count;  // extents of the ring and the flags (bounds-checked builds compare with them)
 };
 
 // Causal depthwise convolution over the packed token axis (nseq sequences of L tokens, D channels).
@@ -91,6 +103,7 @@ struct ConvParams {
     void *state_out;      // [nseq, D, k - 1] the last k - 1 inputs of each sequence, or null; may alias state
     int64_t T, L, D, nseq;
     int k, silu;
+    WsHeader *hdr;        // for the bounds-checked builds' reports (may be null: not checked)
 };
 
 // Chunk pair cp (one chunk of one sequence) in chunk-major order -> sequence, chunk, first token, length.
@@ -174,6 +187,32 @@ __device__ __forceinline__ void report_error(WsHeader *hdr, uint32_t epoch, uint
 __device__ __forceinline__ bool aborted(const WsHeader *hdr, uint32_t epoch) {
     return ld_relaxed_gpu(&hdr->abort) == epoch;
 }
+
+// Bounds-checked builds (-DSSD_BOUNDS_CHECK), the stand-in for a memory checker: a checked access goes through
+// chk(), which compares the element index and the access's span with the buffer's extent. Outside it, the first
+// such access records DEV_BOUNDS, the site and the index in the workspace header, and the access is redirected to
+// the buffer's first element, so nothing outside the buffers is touched and ssd_fwd_check reports it. Release
+// builds compile chk() to the plain address.
+#ifdef SSD_BOUNDS_CHECK
+static __device__ __noinline__ void bounds_hit(WsHeader *hdr, uint32_t site, int64_t idx) {
+    if (hdr && atomicCAS(&hdr->status, 0u, (uint32_t)DEV_BOUNDS) == 0u) {
+        hdr->err_where = site;
+        hdr->err_index_lo = (uint32_t)idx;
+        hdr->err_index_hi = (uint32_t)((uint64_t)idx >> 32);
+    }
+}
+template <typename T>
+__device__ __forceinline__ T *chk(T *base, int64_t idx, int64_t span, int64_t n, WsHeader *hdr, uint32_t site) {
+    if (idx >= 0 && idx + span <= n) return base + idx;
+    bounds_hit(hdr, site, idx);
+    return base;
+}
+#else
+template <typename T>
+__device__ __forceinline__ T *chk(T *base, int64_t idx, int64_t, int64_t, WsHeader *, uint32_t) {
+    return base + idx;
+}
+#endif
 
 // Bounded wait until *tag == want (acquire). Returns false (after recording
 // a timeout) when the limit passes or another CTA aborted the launch.

@@ -83,12 +83,14 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
         const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
         const int64_t t0 = tt * kTileT - (K - 1), cbyte = cb * kTileB;
         uint8_t *dst = smem + st * STAGE;
-        const uint8_t *src = in + sq * c.L * rowb + cbyte;
         for (int q = tid; q < R * (kTileB / 16); q += kThreads) {
             const int r = q / (kTileB / 16), off = (q % (kTileB / 16)) * 16;
             const int64_t t = t0 + r;
             const bool valid = t >= 0 && t < c.L && cbyte + off < rowb;
-            cp_async16(dst + r * kTileB + off, valid ? src + t * rowb + off : in, valid ? 16u : 0u);
+            cp_async16(dst + r * kTileB + off,
+                       valid ? chk(in, (sq * c.L + t) * rowb + cbyte + off, 16, c.nseq * c.L * rowb, c.hdr, SITE_CONV_IN)
+                             : in,
+                       valid ? 16u : 0u);
         }
     };
     const int col = tid % kCols, half = tid / kCols;
@@ -131,10 +133,14 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
                 Col<IO>::load(tile + (int)(tp - (tt * kTileT - (K - 1))) * kTileB, hist[j]);
             } else {
 #pragma unroll
-                for (int i = 0; i < NC; ++i) hist[j][i] = to_f32(state[((sq * c.D) + ch0 + i) * (K - 1) + (K - 1 + tp)]);
+                for (int i = 0; i < NC; ++i)
+                    hist[j][i] = to_f32(*chk(state, ((sq * c.D) + ch0 + i) * (K - 1) + (K - 1 + tp), 1,
+                                             c.nseq * c.D * (K - 1), c.hdr, SITE_CONV_STATE));
             }
         }
-        uint8_t *orow = out + (sq * c.L + tb) * rowb + cbyte;
+        int64_t oidx = (sq * c.L + tb) * rowb + cbyte;  // byte index of this thread's output column
+        const int64_t nout = c.nseq * c.L * rowb;
+        (void)nout;
         const uint8_t *irow = tile + (int)(tb - (tt * kTileT - (K - 1))) * kTileB;
 #pragma unroll 4
         for (int64_t t = tb; t < te; ++t) {
@@ -147,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
                 for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
                 if (c.silu) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
             }
-            *reinterpret_cast<uint32_t *>(orow) = Col<IO>::pack(acc);
+            *reinterpret_cast<uint32_t *>(chk(out, oidx, 4, nout, c.hdr, SITE_CONV_OUT)) = Col<IO>::pack(acc);
 #pragma unroll
             for (int j = K - 2; j > 0; --j)
 #pragma unroll
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
                 for (int i = 0; i < NC; ++i) hist[0][i] = v[i];
             }
             irow += kTileB;
-            orow += rowb;
+            oidx += rowb;
         }
     }
     cp_async_wait<0>();
@@ -178,10 +184,10 @@ __global__ void __launch_bounds__(kThreads) conv_state_kernel(ConvParams c) {
             const int64_t tp = c.L - (c.k - 1) + j;
             IO v = from_f32<IO>(0.f);
             if (tp >= 0)
-                v = in[(s * c.L + tp) * c.D + ch];
+                v = *chk(in, (s * c.L + tp) * c.D + ch, 1, c.nseq * c.L * c.D, c.hdr, SITE_CONV_IN);
             else if (state)
-                v = state[e * (c.k - 1) + (c.k - 1 + tp)];
-            sout[e * (c.k - 1) + j] = v;
+                v = *chk(state, e * (c.k - 1) + (c.k - 1 + tp), 1, total * (c.k - 1), c.hdr, SITE_CONV_STATE);
+            *chk(sout, e * (c.k - 1) + j, 1, total * (c.k - 1), c.hdr, SITE_CONV_STATE) = v;
         }
     }
 }

@@ -64,22 +64,27 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
         const int64_t chain = sq.s * p.H + h;
         const bool last = c == (sq.len + p.Q - 1) / p.Q - 1;
         const float Ah = p.A[h], bias = p.dt_bias[h], Dh = p.D ? p.D[h] : 0.f;
+        // extents of the checked accesses (bounds-checked builds)
+        const int64_t Tt = p.batch * p.L, nstate = p.nseq * p.H * P * N;
+        (void)Tt;
+        (void)nstate;
 
         // ---- state entering chunk c
         if (tid == 0)
             s_ok = aborted(hdr, epoch) ? 0
-                                       : (c == 0 ? 1 : (int)wait_flag(&p.flags[chain * 2 + (c & 1)], chain_tag(epoch, c),
+                                       : (c == 0 ? 1 : (int)wait_flag(chk(p.flags, chain * 2 + (c & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG), chain_tag(epoch, c),
                                                                       epoch, hdr, limit, t, (uint32_t)c));
         __syncthreads();
         if (!s_ok) continue;  // launch aborted: drain the remaining tickets
         if (c == 0) {
             for (int e = tid; e < N * P; e += kThreads) {
                 const int n = e / P, q = e % P;
-                S[e] = init ? to_f32(init[(chain * P + q) * N + n]) : 0.f;
+                S[e] = init ? to_f32(*chk(init, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_INIT)) : 0.f;
             }
         } else {
-            const ST *slot = ring + (chain * 2 + (c & 1)) * (int64_t)(N * P);
-            for (int e = tid; e < N * P; e += kThreads) S[e] = to_f32(__ldcg(slot + e));
+            const int64_t slot = (chain * 2 + (c & 1)) * (int64_t)(N * P);
+            for (int e = tid; e < N * P; e += kThreads)
+                S[e] = to_f32(__ldcg(chk(ring, slot + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING)));
         }
         __syncthreads();
 
@@ -90,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             // step 1: dt = softplus(dt_raw + bias), inclusive cumsum of dt*A (rows >= T: dt = 0)
             if (tid < 32) {
                 float dtv = 0.f;
-                if (tid < T) dtv = softplus_f32(to_f32(dtr[(s0 + tid) * p.H + h]) + bias);
+                if (tid < T) dtv = softplus_f32(to_f32(*chk(dtr, (s0 + tid) * p.H + h, 1, Tt * p.H, hdr, SITE_SIMT_IN)) + bias);
                 float sc = dtv * Ah;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -105,13 +110,13 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             }
             for (int e = tid; e < kSub * P; e += kThreads) {
                 const int r = e / P, q = e % P;
-                xs[e] = r < T ? to_f32(x[(s0 + r) * p.x_ld + h * P + q]) : 0.f;
+                xs[e] = r < T ? to_f32(*chk(x, (s0 + r) * p.x_ld + h * P + q, 1, Tt * p.x_ld, hdr, SITE_SIMT_IN)) : 0.f;
             }
             for (int e = tid; e < kSub * N; e += kThreads) {
                 const int r = e / N, q = e % N;
                 const int64_t off = (s0 + r) * p.bc_ld + g * N + q;
-                Bs[r * NB + q] = r < T ? to_f32(Bg[off]) : 0.f;
-                Cs[r * NB + q] = r < T ? to_f32(Cg[off]) : 0.f;
+                Bs[r * NB + q] = r < T ? to_f32(*chk(Bg, off, 1, Tt * p.bc_ld, hdr, SITE_SIMT_IN)) : 0.f;
+                Cs[r * NB + q] = r < T ? to_f32(*chk(Cg, off, 1, Tt * p.bc_ld, hdr, SITE_SIMT_IN)) : 0.f;
             }
             __syncthreads();
             // step 2 (BMM) with the segsum decay mask: Pm[i][j] = (C_i.B_j) exp(cs_i - cs_j) dt_j, j <= i
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
                 for (int j = 0; j <= i; ++j) a1 = fmaf(Pm[i * kSub + j], xs[j * P + q], a1);
                 for (int n = 0; n < N; ++n) a2 = fmaf(Cs[i * NB + n], S[n * P + q], a2);
                 const float v = a1 + ecs[i] * a2 + Dh * xs[i * P + q];
-                y[((s0 + i) * p.H + h) * P + q] = from_f32<IO>(v);
+                *chk(y, ((s0 + i) * p.H + h) * P + q, 1, Tt * p.H * P, hdr, SITE_SIMT_Y) = from_f32<IO>(v);
             }
             __syncthreads();
             // steps 3 + 4 (chunk state, state passing): S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
@@ -152,14 +157,17 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
             if (fin)
                 for (int e = tid; e < N * P; e += kThreads) {
                     const int q = e / N, n = e % N;
-                    fin[(chain * P + q) * N + n] = from_f32<ST>(S[n * P + q]);
+                    *chk(fin, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_FINAL) = from_f32<ST>(S[n * P + q]);
                 }
         } else if (c != skip) {
-            ST *slot = ring + (chain * 2 + ((c + 1) & 1)) * (int64_t)(N * P);
-            for (int e = tid; e < N * P; e += kThreads) __stcg(slot + e, from_f32<ST>(S[e]));
+            const int64_t slot = (chain * 2 + ((c + 1) & 1)) * (int64_t)(N * P);
+            for (int e = tid; e < N * P; e += kThreads)
+                __stcg(chk(ring, slot + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING), from_f32<ST>(S[e]));
             __threadfence();
             __syncthreads();
-            if (tid == 0) st_release_u64(&p.flags[chain * 2 + ((c + 1) & 1)], chain_tag(epoch, c + 1));
+            if (tid == 0)
+                st_release_u64(chk(p.flags, chain * 2 + ((c + 1) & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG),
+                               chain_tag(epoch, c + 1));
         }
         __syncthreads();
     }

@@ -70,15 +70,23 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
     ST *hout = static_cast<ST *>(p.final_states);
     IO *y = static_cast<IO *>(p.y);
     const int64_t chains = p.batch * p.H;
+    // extents of the checked accesses (bounds-checked builds)
+    const int64_t nst = chains * p.P * p.N, nbc = p.batch * p.bc_ld, nx = p.batch * p.x_ld;
+    (void)nst;
+    (void)nbc;
+    (void)nx;
     for (int64_t ch = blockIdx.x; ch < chains; ch += gridDim.x) {
         const int64_t b = ch / p.H, h = ch % p.H, g = h / p.heads_per_group;
-        const float dt = softplus_f32(to_f32(dtr[ch]) + p.dt_bias[h]);
+        const float dt = softplus_f32(to_f32(*chk(dtr, ch, 1, chains, p.hdr, SITE_STEP_IN)) + p.dt_bias[h]);
         const float a = expf(dt * p.A[h]);
         const float Dh = p.D ? p.D[h] : 0.f;
-        const IO *Bg = Bm + b * p.bc_ld + g * p.N;
-        const IO *Cg = Cm + b * p.bc_ld + g * p.N;
-        const IO *xh = x + b * p.x_ld + h * p.P;  // this chain's token
+        const IO *Bg = chk(Bm, b * p.bc_ld + g * p.N, p.N, nbc, p.hdr, SITE_STEP_IN);
+        const IO *Cg = chk(Cm, b * p.bc_ld + g * p.N, p.N, nbc, p.hdr, SITE_STEP_IN);
+        const IO *xh = chk(x, b * p.x_ld + h * p.P, p.P, nx, p.hdr, SITE_STEP_IN);  // this chain's token
         const int64_t base = ch * p.P * p.N;
+        const ST *hin_c = hin ? chk(hin, base, p.P * p.N, nst, p.hdr, SITE_STEP_STATE) : nullptr;
+        ST *hout_c = hout ? chk(hout, base, p.P * p.N, nst, p.hdr, SITE_STEP_STATE) : nullptr;
+        IO *y_c = chk(y, ch * p.P, p.P, chains * p.P, p.hdr, SITE_STEP_Y);
         for (int64_t r0 = (int64_t)warp * ROWS; r0 < p.P; r0 += (int64_t)kWarps * ROWS) {
             const int64_t p0 = r0 + sub, p1 = r0 + SUBS + sub;
             const bool one = p0 < p.P, two = p1 < p.P;
@@ -89,8 +97,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
 #pragma unroll
                 for (int i = 0; i < K; ++i) h0[i] = h1[i] = 0.f;
                 if (hin) {
-                    if (one) load_k<ST, K>(hin + base + p0 * p.N + n0, h0);
-                    if (two) load_k<ST, K>(hin + base + p1 * p.N + n0, h1);
+                    if (one) load_k<ST, K>(hin_c + p0 * p.N + n0, h0);
+                    if (two) load_k<ST, K>(hin_c + p1 * p.N + n0, h1);
                 }
                 load_k<IO, K>(Bg + n0, bv);
                 load_k<IO, K>(Cg + n0, cv);
@@ -102,8 +110,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
                     acc1 = fmaf(cv[i], h1[i], acc1);
                 }
                 if (hout) {
-                    if (one) store_k<ST, K>(hout + base + p0 * p.N + n0, h0);
-                    if (two) store_k<ST, K>(hout + base + p1 * p.N + n0, h1);
+                    if (one) store_k<ST, K>(hout_c + p0 * p.N + n0, h0);
+                    if (two) store_k<ST, K>(hout_c + p1 * p.N + n0, h1);
                 }
             }
 #pragma unroll
@@ -112,8 +120,8 @@ __global__ void __launch_bounds__(kThreads) step_kernel(Params p) {
                 acc1 += __shfl_xor_sync(0xffffffffu, acc1, o);
             }
             if (l == 0) {
-                if (one) y[ch * p.P + p0] = from_f32<IO>(fmaf(Dh, x0, acc0));
-                if (two) y[ch * p.P + p1] = from_f32<IO>(fmaf(Dh, x1, acc1));
+                if (one) y_c[p0] = from_f32<IO>(fmaf(Dh, x0, acc0));
+                if (two) y_c[p1] = from_f32<IO>(fmaf(Dh, x1, acc1));
             }
         }
     }
@@ -164,10 +172,10 @@ __global__ void __launch_bounds__(kBulkThreads, bulk_ctas<ST>()) step_bulk_kerne
         const int64_t b = ch / p.H, h = ch % p.H, g = h / p.heads_per_group;
         uint8_t *base = smem + (size_t)st * stride;
         mbar_arrive_expect_tx(&full[st], (hin ? SB : 0u) + 2 * BB + XB);
-        if (hin) bulk_load(base, hin + ch * p.P * p.N, SB, &full[st]);
-        bulk_load(base + SB, Bm + b * p.bc_ld + g * p.N, BB, &full[st]);
-        bulk_load(base + SB + BB, Cm + b * p.bc_ld + g * p.N, BB, &full[st]);
-        bulk_load(base + SB + 2 * BB, x + b * p.x_ld + h * p.P, XB, &full[st]);
+        if (hin) bulk_load(base, chk(hin, ch * p.P * p.N, p.P * p.N, chains * p.P * p.N, p.hdr, SITE_STEP_STATE), SB, &full[st]);
+        bulk_load(base + SB, chk(Bm, b * p.bc_ld + g * p.N, p.N, p.batch * p.bc_ld, p.hdr, SITE_STEP_IN), BB, &full[st]);
+        bulk_load(base + SB + BB, chk(Cm, b * p.bc_ld + g * p.N, p.N, p.batch * p.bc_ld, p.hdr, SITE_STEP_IN), BB, &full[st]);
+        bulk_load(base + SB + 2 * BB, chk(x, b * p.x_ld + h * p.P, p.P, p.batch * p.x_ld, p.hdr, SITE_STEP_IN), XB, &full[st]);
     };
     int64_t issued = 0;
     if (tid == 0)
@@ -188,10 +196,11 @@ __global__ void __launch_bounds__(kBulkThreads, bulk_ctas<ST>()) step_bulk_kerne
                 }
         }
         if (!failed) {
-            const float dt = softplus_f32(to_f32(dtr[ch]) + p.dt_bias[h]);
+            const float dt = softplus_f32(to_f32(*chk(dtr, ch, 1, chains, p.hdr, SITE_STEP_IN)) + p.dt_bias[h]);
             const float a = expf(dt * p.A[h]);
             const float Dh = p.D ? p.D[h] : 0.f;
             uint8_t *base = smem + (size_t)st * stride;
+            IO *y_c = chk(y, ch * p.P, p.P, chains * p.P, p.hdr, SITE_STEP_Y);
             ST *S = reinterpret_cast<ST *>(base);
             const IO *Bs = reinterpret_cast<const IO *>(base + SB);
             const IO *Cs = Bs + p.N;
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(kBulkThreads, bulk_ctas<ST>()) step_bulk_kerne
                 }
 #pragma unroll
                 for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (l == 0) y[ch * p.P + r] = from_f32<IO>(fmaf(Dh, xv, acc));
+                if (l == 0) y_c[r] = from_f32<IO>(fmaf(Dh, xv, acc));
             }
             if (hout) fence_proxy_async_smem();  // the updated rows, for the bulk store
         }
@@ -240,7 +249,8 @@ __global__ void __launch_bounds__(kBulkThreads, bulk_ctas<ST>()) step_bulk_kerne
         }
         if (tid == 0) {
             if (hout) {
-                bulk_store(hout + ch * p.P * p.N, smem + (size_t)st * stride, SB);
+                bulk_store(chk(hout, ch * p.P * p.N, p.P * p.N, chains * p.P * p.N, p.hdr, SITE_STEP_STATE),
+                           smem + (size_t)st * stride, SB);
                 bulk_commit();
             }
             // refill the stage of chain j - 1 (its store has been issued one chain ago) with chain j + stages - 1

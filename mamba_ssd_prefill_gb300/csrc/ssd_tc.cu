@@ -151,16 +151,20 @@ __device__ __forceinline__ void conv_halo(const Params &p, int64_t s, int64_t to
                                           float (&h)[3][2]) {
     const IO *xraw = static_cast<const IO *>(p.x);
     const IO *st = static_cast<const IO *>(p.conv_state);
+    const int64_t nx = p.batch * p.L * p.x_ld, nst = p.nseq * p.x_ld * 3;  // extents (bounds-checked builds)
+    (void)nx;
+    (void)nst;
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int64_t tok = row0 - 3 + j;
         if (tok >= tok0) {
-            const float2 f = unpack_io<IO>(*reinterpret_cast<const uint32_t *>(xraw + tok * p.x_ld + ch));
+            const float2 f = unpack_io<IO>(
+                *reinterpret_cast<const uint32_t *>(chk(xraw, tok * p.x_ld + ch, 2, nx, p.hdr, SITE_CONV_IN)));
             h[j][0] = f.x;
             h[j][1] = f.y;
         } else if (st) {
-            h[j][0] = to_f32(st[(s * p.x_ld + ch) * 3 + 3 + (tok - tok0)]);
-            h[j][1] = to_f32(st[(s * p.x_ld + ch + 1) * 3 + 3 + (tok - tok0)]);
+            h[j][0] = to_f32(*chk(st, (s * p.x_ld + ch) * 3 + 3 + (tok - tok0), 1, nst, p.hdr, SITE_CONV_STATE));
+            h[j][1] = to_f32(*chk(st, (s * p.x_ld + ch + 1) * 3 + 3 + (tok - tok0), 1, nst, p.hdr, SITE_CONV_STATE));
         } else {
             h[j][0] = h[j][1] = 0.f;
         }
@@ -351,6 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         Sched prev{0, 0, 0, 0, 0, 0, 0, 0};
         const uint32_t total = total_units(p, (uint32_t)(p.G * slices));
         const bool late = p.tc_late_ticket != 0;
+        const int64_t ndt = p.batch * p.L * p.H;  // dt_raw extent (bounds-checked builds)
+#ifdef SSD_BOUNDS_CHECK
+        const int64_t probe = hdr->bounds_probe ? ndt : 0;  // test hook: plant the dt rows one extent further
+#else
+        const int64_t probe = 0;
+#endif
         bool ok = true;
         // conversion + tables of the unit in stage uu (whose tiles were requested earlier)
         auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
@@ -470,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < kMaxHs; ++hh) {
                     raw[jj][hh] = 0.f;
-                    if (hh < hs && i < rows) raw[jj][hh] = to_f32(dtr[(row0 + i) * p.H + h0 + hh]);
+                    if (hh < hs && i < rows)
+                        raw[jj][hh] = to_f32(*chk(dtr, (row0 + i) * p.H + h0 + hh + probe, 1, ndt, hdr, SITE_TC_DT));
                 }
             }
 #pragma unroll
@@ -541,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = lane; e < 3 * kP; e += 32) {
                         const int r = e / kP, pc = e % kP;
                         const int64_t ch = (int64_t)(sc.h0 + hh) * kP + pc;
-                        dst[r * kP + pc] = st ? st[((int64_t)sc.s * p.x_ld + ch) * 3 + r] : from_f32<IO>(0.f);
+                        dst[r * kP + pc] = st ? *chk(st, ((int64_t)sc.s * p.x_ld + ch) * 3 + r, 1, p.nseq * p.x_ld * 3, hdr,
+                                                     SITE_CONV_STATE)
+                                              : from_f32<IO>(0.f);
                     }
                 }
                 __syncwarp();
@@ -707,7 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
             } else if (lane < pvr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
-                uint4 *dst = reinterpret_cast<uint4 *>(yg + ((int64_t)(prow + lane) * p.H + ph) * kP);
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    chk(yg, ((int64_t)(prow + lane) * p.H + ph) * kP, kP, p.batch * p.L * p.H * kP, hdr, SITE_TC_Y));
 #pragma unroll
                 for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(yrow + ((lc ^ (i & 7)) << 4));
             }
@@ -931,7 +945,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t skip = hdr->skip_publish - 1;
         const ST *init = static_cast<const ST *>(p.init);
         ST *fin = static_cast<ST *>(p.final_states);
-        ST *ring = static_cast<ST *>(p.ring);
         uint64_t *tags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]
         constexpr bool kTagged = sizeof(ST) == 2;
         float S[kP];          // entering state of the current head (fp32)
@@ -946,7 +959,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             return sc.valid != 0;
         };
         ulonglong2 *ringv = static_cast<ulonglong2 *>(p.ring);  // fp16: [chain][slot][P / 4 vectors][row]
-        auto vrow_of = [&](int64_t chain, int c) { return ringv + (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow; };
+        const int64_t nvec = p.ring_bytes / 16, nstate = p.nseq * p.H * kP * kN;  // extents (bounds-checked builds)
+        // row nrow of a slot: 16 vectors kN apart (checked as one span)
+        auto vrow_of = [&](int64_t chain, int c) {
+            return chk(ringv, (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1, nvec, hdr,
+                       SITE_TC_RING);
+        };
         auto vtag = [&](int c) { return epoch * 4096u + (uint32_t)(c & 4095); };
         // fp16: the tagged row of chunk c as loaded, and whether any of its words is stale
         uint64_t raw[kTagged ? kP / 2 : 1];
@@ -967,12 +985,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // Row nrow of the state entering chunk c > 0 of `chain`, from the ring (the caller has seen its tag).
         auto load_ring = [&](int64_t chain, int c) {
-            const ST *slot = ring + (chain * 2 + (c & 1)) * (int64_t)(kP * kN);
             if (sizeof(ST) == 4) {
-                const float4 *src = reinterpret_cast<const float4 *>(slot);
+                const float4 *src = chk(reinterpret_cast<const float4 *>(p.ring),
+                                        (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
+                                        nvec, hdr, SITE_TC_RING);
 #pragma unroll
                 for (int m = 0; m < kP / 4; ++m) {
-                    const float4 f = __ldcg(src + m * kN + nrow);
+                    const float4 f = __ldcg(src + m * kN);
                     S[4 * m] = f.x;
                     S[4 * m + 1] = f.y;
                     S[4 * m + 2] = f.z;
@@ -980,7 +999,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        auto tag_of = [&](int64_t chain, int c) { return tags + (chain * 2 + (c & 1)) * kN + nrow; };
+        auto tag_of = [&](int64_t chain, int c) {
+            return chk(tags, (chain * 2 + (c & 1)) * kN + nrow, 1, p.flag_count, hdr, SITE_TC_FLAG);
+        };
         auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
         // Prefetch (fp32 states): load the entering state now when its producer's tag is already visible.
         auto prefetch = [&](int64_t chain, int c) -> bool {
@@ -1003,7 +1024,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!have_S) {
                     if (c == 0) {
 #pragma unroll
-                        for (int pp = 0; pp < kP; ++pp) S[pp] = init ? to_f32(init[(chain * kP + pp) * kN + nrow]) : 0.f;
+                        for (int pp = 0; pp < kP; ++pp)
+                            S[pp] = init ? to_f32(*chk(init, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_INIT)) : 0.f;
                     } else if (kTagged) {
                         const uint32_t want = vtag(c);
                         issue_tagged(chain, c);
@@ -1064,15 +1086,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sc.last) {
                 if (fin) {
 #pragma unroll
-                    for (int pp = 0; pp < kP; ++pp) fin[(chain * kP + pp) * kN + nrow] = from_f32<ST>(s[pp]);
+                    for (int pp = 0; pp < kP; ++pp)
+                        *chk(fin, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_FINAL) = from_f32<ST>(s[pp]);
                 }
             } else if (publish) {
-                ST *slot = ring + (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP * kN);
                 if (sizeof(ST) == 4) {
-                    float4 *dst = reinterpret_cast<float4 *>(slot);
+                    float4 *dst = chk(reinterpret_cast<float4 *>(p.ring),
+                                      (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
+                                      nvec, hdr, SITE_TC_RING);
 #pragma unroll
                     for (int m = 0; m < kP / 4; ++m)
-                        __stcg(dst + m * kN + nrow, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
+                        __stcg(dst + m * kN, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
                 } else {  // tagged words, the last vector last
                     ulonglong2 *dst = vrow_of(chain, c + 1);
                     const uint64_t tg = (uint64_t)vtag(c + 1) << 32;

@@ -1,5 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -585,3 +586,25 @@ def test_host_streaming_piece_counts_and_empty():
     y0, f0 = m.ssd_fwd_host(**he, chunk_size=e.chunk, scratch=scratch)
     torch.cuda.synchronize()
     assert y0.numel() == 0 and torch.equal(f0, he["init_states"])
+
+
+# ----------------------------------------------------------------------------- bounds-checked debug build
+def test_bounds_checked_build_reports_no_violation_and_catches_the_probe():
+    """The debug build compares every kernel's global indices with the buffers' extents (an index outside is never
+    used and is reported). Every entry point on edge-case shapes runs clean under it; the planted probe (the
+    tensor-core kernel's dt_raw indices one extent too far) is caught and reported, and the workspace works again
+    after it."""
+    import subprocess
+    import sys
+
+    from mamba_ssd_prefill_gb300 import _build
+
+    lib_path = _build.build(checked=True)
+    env = dict(os.environ, MAMBA_SSD_LIB=lib_path)
+    r = subprocess.run([sys.executable, os.path.join(os.path.dirname(__file__), "bounds_cases.py")], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    results = dict(line.split() for line in r.stdout.strip().splitlines())
+    assert len(results) == 16, results
+    assert results.pop("probe") == "6", r.stdout
+    assert all(v == "0" for v in results.values()), results
