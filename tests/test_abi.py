@@ -167,3 +167,14 @@ def test_host_streaming_plan_and_argument_checks(lib):
     bad.nheads = 3                                                                        # not a multiple of G
     bad.ngroups = 2
     assert lib.ssd_fwd_host_scratch_size(ctypes.byref(bad), 0, ctypes.byref(n1)) == 1
+
+
+def test_bounds_checked_build_compiles_and_exports_every_symbol():
+    """The bounds-checked debug library (SSD_BOUNDS_CHECK) builds from the same sources and exports the same C ABI;
+    the GPU test runs it."""
+    from mamba_ssd_prefill_gb300 import _build
+
+    path = _build.build(checked=True)
+    L = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(L, name), name
