@@ -608,3 +608,28 @@ def test_bounds_checked_build_reports_no_violation_and_catches_the_probe():
     assert len(results) == 16, results
     assert results.pop("probe") == "6", r.stdout
     assert all(v == "0" for v in results.values()), results
+
+
+def test_host_streaming_in_a_cuda_graph():
+    """ssd_fwd_host captured once in a CUDA graph (its copy streams join the capture through the events on the
+    caller's stream) and replayed: the replays give the same y and final states as the eager call."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=520, nheads=4, seed=341)
+    inp = make_inputs(w, device="cuda")
+    host = {k: (v if k in ("dt_bias", "A", "D") else _pinned(v)) for k, v in inp.items()}
+    scratch = m.Workspace("cuda")
+    y_e, f_e = m.ssd_fwd_host(**host, chunk_size=w.chunk, pieces=3, scratch=scratch)
+    torch.cuda.synchronize()
+    y_g = torch.zeros_like(y_e).pin_memory()
+    f_g = torch.zeros_like(f_e).pin_memory()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        m.ssd_fwd_host(**host, chunk_size=w.chunk, pieces=3, scratch=scratch, y=y_g, final_states=f_g,
+                       stream=stream)
+    for _ in range(2):
+        y_g.zero_()
+        f_g.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        m.check(scratch)
+        assert torch.equal(y_g, y_e) and torch.equal(f_g, f_e)
