@@ -59,6 +59,11 @@ WORKLOADS = {
     "m2p7-L8k-b32": Workload("m2p7-L8k-b32", 32, 8192, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal", seed=1004),
     "long-L256k-g8": Workload("long-L256k-g8", 1, 262144, 80, 64, 128, 8, 128, io="bf16", state="f32", init="none",
                               dt_lo=1e-4, seed=1005),
+    # the fp16-state variants of the fp32-state workloads above (states passed and returned in fp16)
+    "long-L256k-g8-f16": Workload("long-L256k-g8-f16", 1, 262144, 80, 64, 128, 8, 128, io="bf16", state="f16",
+                                  init="none", dt_lo=1e-4, seed=1005),
+    "m130-bf16-f16": Workload("m130-bf16-f16", 4, 4096, 24, 64, 128, 1, 128, io="bf16", state="f16", init="normal",
+                              seed=1002),
     # decode: one token per sequence advances the cached state (2.7B layer shape, 64 / 256 sequences)
     "decode-2p7-b64": Workload("decode-2p7-b64", 64, 1, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal",
                                seed=1006),

@@ -248,7 +248,7 @@ def test_tc_matches_simt_kernel():
 
 # full-size workloads, in the launch configuration the benchmark times; the oracle checks sampled chains
 FULL = ["m130-bf16", "m2p7-L16k-q128", "m2p7-L16k-q256", "m2p7-L8k-b1", "m2p7-L8k-b8", "m2p7-L8k-b32",
-        "long-L256k-g8"]
+        "long-L256k-g8", "m130-bf16-f16", "long-L256k-g8-f16"]
 
 
 def sampled_chains(w, n):
