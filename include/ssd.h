@@ -224,7 +224,11 @@ SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob, const voi
  *  dt_bias, A, D   device pointers, as for ssd_fwd.
  *  scratch      device memory of ssd_fwd_host_scratch_size(prob, pieces)
  *               bytes, 256-byte aligned, zero-filled once before its first use;
- *               it begins with the workspace that ssd_fwd_check reads.
+ *               it begins with the workspace that ssd_fwd_check reads. Calls
+ *               on one stream may reuse it back to back; calls that may overlap
+ *               (other streams, other host threads) need separate scratch.
+ *               Such calls share the device's two copy streams, so their
+ *               copies queue behind each other.
  * The computation runs on `stream`; the copies run on two streams the library
  * creates once per device and keeps, ordered after the work queued on `stream`
  * before the call, and `stream` waits for all of them before any later work:
