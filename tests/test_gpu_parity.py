@@ -26,7 +26,7 @@ def run_gpu(w, inp, kernel="auto", ws=None, **kw):
 
 
 def assert_parity(w, y, fin, yr, fr, label=""):
-    ok, s = gate_y(y.double().cpu().numpy(), yr, w.io)
+    ok, s = gate_y(y.double().cpu().numpy(), yr, w.io, w.state)
     assert ok, f"{label} y parity failed: {s}"
     okf, sf = gate_final(fin.double().cpu().numpy(), fr, w.io, w.state)
     assert okf, f"{label} final-state parity failed: {sf}"
@@ -284,7 +284,7 @@ def test_tc_full_size_sampled(name):
     yr, fr = oracle.ssd_chains(sub["x"][:, :, 0], sub["dt_raw"][:, :, 0], inp["dt_bias"].cpu()[hs],
                                inp["A"].cpu()[hs], sub["B"][:, :, 0], sub["C"][:, :, 0], inp["D"].cpu()[hs],
                                None if init is None else init.cpu())
-    ok, s = gate_y(ys, yr, w.io)
+    ok, s = gate_y(ys, yr, w.io, w.state)
     assert ok, f"{name}: {s}"
     okf, sf = gate_final(fs, fr, w.io, w.state)
     assert okf, f"{name} final: {sf}"
@@ -633,3 +633,32 @@ def test_host_streaming_in_a_cuda_graph():
         torch.cuda.synchronize()
         m.check(scratch)
         assert torch.equal(y_g, y_e) and torch.equal(f_g, f_e)
+
+
+# ----------------------------------------------------------------------------- randomised shapes
+def _random_cases(n=24, seed=2024):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        tc = i % 2 == 0  # alternate shapes the tensor-core kernel takes and shapes only the SIMT kernel takes
+        H = int(rng.choice([2, 4, 6, 8]))
+        G = int(rng.choice([g for g in (1, 2, 3, 4, 6, 8) if H % g == 0]))
+        io = str(rng.choice(["bf16", "f16"])) if tc else str(rng.choice(["f32", "bf16", "f16"]))
+        over = dict(batch=int(rng.integers(1, 4)), seqlen=int(rng.integers(1, 1300)), nheads=H, ngroups=G, io=io,
+                    headdim=64 if tc else int(rng.choice([16, 32, 64])),
+                    dstate=128 if tc else int(rng.choice([16, 32, 64, 128])),
+                    chunk=int(rng.choice([128, 256])) if tc else int(rng.choice([32, 64, 128])),
+                    state=str(rng.choice(["f32", "f16"])), init=str(rng.choice(["none", "normal"])), seed=5000 + i)
+        cases.append(over)
+    return cases
+
+
+@pytest.mark.parametrize("over", _random_cases(), ids=[f"rand{i}" for i in range(24)])
+def test_random_shapes_against_the_oracle(over):
+    """Seeded random problems across both prefill kernels (and the decode step when a length of 1 comes up):
+    batch, odd lengths, groups, head and state sizes, chunk sizes, dtypes, with and without initial states."""
+    w = WORKLOADS["m130-bf16"].with_(**over)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp)
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"random {over}")
