@@ -662,3 +662,60 @@ def test_random_shapes_against_the_oracle(over):
     y, fin = run_gpu(w, inp)
     yr, fr = oracle.ssd_reference(**cpu(inp))
     assert_parity(w, y, fin, yr, fr, f"random {over}")
+
+
+def _random_varlen_cases(n=10, seed=2025):
+    """Length mixes with empty, one-token, chunk-edge and long sequences, on both prefill kernels."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        tc = i % 2 == 0
+        H = int(rng.choice([2, 4, 8]))
+        G = int(rng.choice([g for g in (1, 2, 4) if H % g == 0]))
+        chunk = int(rng.choice([128, 256])) if tc else int(rng.choice([32, 64]))
+        pool = [0, 1, chunk - 1, chunk, chunk + 1] + [int(v) for v in rng.integers(2, 900, size=3)]
+        lengths = [int(rng.choice(pool)) for _ in range(int(rng.integers(1, 7)))]
+        over = dict(nheads=H, ngroups=G, chunk=chunk, io=str(rng.choice(["bf16", "f16"])),
+                    state=str(rng.choice(["f32", "f16"])), init=str(rng.choice(["none", "normal"])),
+                    headdim=64 if tc else int(rng.choice([32, 64])), dstate=128 if tc else int(rng.choice([32, 128])))
+        cases.append(("tc" if tc else "simt", over, lengths, 7000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("kernel,over,lengths,seed", _random_varlen_cases(), ids=[f"rvar{i}" for i in range(10)])
+def test_random_varlen_against_the_oracle(kernel, over, lengths, seed):
+    w = WORKLOADS["m130-bf16"].with_(**over)
+    inp = make_varlen_inputs(w, lengths, device="cuda", seed=seed)
+    ws = m.Workspace("cuda")
+    y, fin = m.ssd_fwd_varlen(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel=kernel, workspace=ws)
+    m.check(ws)
+    yr, fr = oracle.ssd_varlen_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"random varlen {kernel} {over} {lengths}")
+
+
+def _random_conv_cases(n=8, seed=2026):
+    """Conv widths 1 .. 8, both activations, with and without a cache, fused and unfused, prefill and one token."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        H = int(rng.choice([2, 4]))
+        over = dict(batch=int(rng.integers(1, 4)), seqlen=int(rng.choice([1, int(rng.integers(2, 600))])), nheads=H,
+                    ngroups=int(rng.choice([1, 2])), io=str(rng.choice(["bf16", "f16"])),
+                    state=str(rng.choice(["f32", "f16"])), init=str(rng.choice(["none", "normal"])), seed=8000 + i)
+        cases.append((over, int(rng.integers(1, 9)), str(rng.choice(["silu", "none"])), bool(rng.integers(0, 2)),
+                      bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("over,width,act,cache,fuse", _random_conv_cases(), ids=[f"rconv{i}" for i in range(8)])
+def test_random_conv_against_the_oracle(over, width, act, cache, fuse):
+    w = WORKLOADS["m130-bf16"].with_(**over)
+    inp = make_conv_inputs(w, width, device="cuda", seed=w.seed, conv_state=cache)
+    ws = m.Workspace("cuda")
+    y, fin, cs, _ = m.ssd_fwd_conv(**inp, nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate,
+                                   activation=act, chunk_size=w.chunk, state_dtype=DTYPES[w.state], workspace=ws,
+                                   fuse=fuse)
+    m.check(ws)
+    yr, fr, csr = conv_reference(w, inp, width, act)
+    assert_parity(w, y, fin, yr, fr, f"random conv {over} k={width} {act} cache={cache} fuse={fuse}")
+    assert np.array_equal(cs.double().cpu().numpy(), csr)
