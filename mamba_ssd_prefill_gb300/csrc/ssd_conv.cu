@@ -12,8 +12,9 @@
 // HBM-bound: tiles of 64 tokens x 512 bytes of channels, with the k - 1 rows before them, go through shared
 // memory in a 3-stage pipeline of 16-byte asynchronous copies (rows outside the sequence zero-filled), two
 // CTAs per SM; a thread walks 32 tokens of one 4-byte column of the tile (two 16-bit channels or one fp32 one)
-// with the taps and the last k - 1 inputs in registers, fp32 arithmetic, and stores rows coalesced. A second
-// kernel writes the cache for continuing each sequence.
+// with the taps and the last k - 1 inputs in registers, fp32 arithmetic (a 16-bit column's two channels in packed
+// f32x2 fused multiply-adds), SiLU as h + h tanh(h) with h = v / 2 (one special-function op per channel), and
+// stores rows coalesced. A second kernel writes the cache for continuing each sequence.
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -33,6 +34,21 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Two fp32 fused multiply-adds in one packed instruction, each rounded like a scalar fmaf.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float tanh_approx(float v) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
 
 template <typename IO> struct Col;  // a 4-byte column: two 16-bit channels or one fp32 channel
 template <> struct Col<float> {
@@ -146,12 +162,31 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
         for (int64_t t = tb; t < te; ++t) {
             float v[NC], acc[NC];
             Col<IO>::load(irow, v);
+            if constexpr (NC == 2) {  // the column's two channels side by side
+                float2 a2 = fma2(make_float2(w[K - 1][0], w[K - 1][1]), make_float2(v[0], v[1]),
+                                 make_float2(bias[0], bias[1]));
 #pragma unroll
-            for (int i = 0; i < NC; ++i) {
-                acc[i] = fmaf(w[K - 1][i], v[i], bias[i]);
+                for (int j = 0; j < K - 1; ++j)
+                    a2 = fma2(make_float2(w[K - 2 - j][0], w[K - 2 - j][1]), make_float2(hist[j][0], hist[j][1]), a2);
+                acc[0] = a2.x;
+                acc[NC - 1] = a2.y;
+                if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
+                    const float2 hv = make_float2(0.5f * a2.x, 0.5f * a2.y);
+                    const float2 r = fma2(hv, make_float2(tanh_approx(hv.x), tanh_approx(hv.y)), hv);
+                    acc[0] = r.x;
+                    acc[NC - 1] = r.y;
+                }
+            } else {
 #pragma unroll
-                for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
-                if (c.silu) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
+                for (int i = 0; i < NC; ++i) {
+                    acc[i] = fmaf(w[K - 1][i], v[i], bias[i]);
+#pragma unroll
+                    for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
+                    if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
+                        const float hv = 0.5f * acc[i];
+                        acc[i] = fmaf(hv, tanh_approx(hv), hv);
+                    }
+                }
             }
             *reinterpret_cast<uint32_t *>(chk(out, oidx, 4, nout, c.hdr, SITE_CONV_OUT)) = Col<IO>::pack(acc);
 #pragma unroll
