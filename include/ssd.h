@@ -217,6 +217,9 @@ SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob, const voi
  *               chunk_size, each piece holding the same token range of every
  *               sequence; the states leaving one piece enter the next (the
  *               same chunks, in the same order and precision, as one call).
+ *               From 8 pieces on, the first and the last piece are a quarter
+ *               of an even piece's size (a shorter pipeline fill and drain)
+ *               and the others share the rest evenly.
  *  x, dt_raw, B, C, init_states (optional): host inputs, and y, final_states
  *               (optional): host outputs, in the layouts of ssd_fwd. Page-locked
  *               memory lets the copies overlap; pageable memory also works,

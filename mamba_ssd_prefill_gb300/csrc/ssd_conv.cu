@@ -10,16 +10,25 @@
 // SSD inputs, so the SSD reads x, B and C as column slices of the output.
 //
 // HBM-bound: tiles of 64 tokens x 512 bytes of channels, with the k - 1 rows before them, go through shared
-// memory in a 3-stage pipeline of 16-byte asynchronous copies (rows outside the sequence zero-filled), two
-// CTAs per SM; a thread walks 32 tokens of one 4-byte column of the tile (two 16-bit channels or one fp32 one)
+// memory in a 3-stage pipeline, two CTAs per SM: one TMA box per tile from a 3-D map over [sequence, token,
+// channel] (rows outside the sequence and channels past the last read as zeros), or, where the rows are not
+// 16-byte multiples, 16-byte asynchronous copies with the same zero fill. A thread walks 32 tokens of one
+// 4-byte column of the tile (two 16-bit channels or one fp32 one)
 // with the taps and the last k - 1 inputs in registers, fp32 arithmetic (a 16-bit column's two channels in packed
 // f32x2 fused multiply-adds), SiLU as h + h tanh(h) with h = v / 2 (one special-function op per channel), and
 // stores rows coalesced. A second kernel writes the cache for continuing each sequence.
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "sm100_ptx.cuh"
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
 namespace {
+
+using namespace sm100;
 
 constexpr int kThreads = 256;
 constexpr int kTileT = 64;      // tokens per tile
@@ -48,6 +57,14 @@ __device__ __forceinline__ float tanh_approx(float v) {
     float r;
     asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
     return r;
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
 }
 
 template <typename IO> struct Col;  // a 4-byte column: two 16-bit channels or one fp32 channel
@@ -81,19 +98,103 @@ template <> struct Col<__half> {
     }
 };
 
+// Item `it` (sequence, token tile, channel tile; channel tiles fastest) from its staged rows: this thread's 4-byte
+// column of the output, tokens [tb, tb + 32) of the tile.
+template <typename IO, int K>
+__device__ __forceinline__ void conv_item(const ConvParams &c, const uint8_t *stage, int64_t it, int64_t ctiles,
+                                          int64_t ttiles, int tid) {
+    constexpr int NC = Col<IO>::C;
+    const int64_t rowb = c.D * (int64_t)sizeof(IO);
+    const IO *state = static_cast<const IO *>(c.state);
+    uint8_t *out = static_cast<uint8_t *>(c.out);
+    const int col = tid % kCols, half = tid / kCols;
+    const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
+    const int64_t cbyte = cb * kTileB + col * 4;
+    if (cbyte >= rowb) return;  // past the last channel
+    const int64_t ch0 = cbyte / (int64_t)sizeof(IO);
+    const uint8_t *tile = stage + col * 4;
+    const int64_t tb = tt * kTileT + half * (kTileT / 2);  // first token of this thread's half
+    const int64_t te = tb + kTileT / 2 < c.L ? tb + kTileT / 2 : c.L;
+    if (tb >= te) return;
+    float w[K][NC], bias[NC];
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        bias[i] = c.bias ? c.bias[ch0 + i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[j][i] = c.w[(ch0 + i) * K + j];
+    }
+    // hist[j] = input of token t - 1 - j: from the tile (rows before the sequence are zeros there), or the cache
+    float hist[K > 1 ? K - 1 : 1][NC];
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j) {
+        const int64_t tp = tb - 1 - j;
+        if (tp >= 0 || !state) {
+            Col<IO>::load(tile + (int)(tp - (tt * kTileT - (K - 1))) * kTileB, hist[j]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+                hist[j][i] = to_f32(*chk(state, ((sq * c.D) + ch0 + i) * (K - 1) + (K - 1 + tp), 1,
+                                         c.nseq * c.D * (K - 1), c.hdr, SITE_CONV_STATE));
+        }
+    }
+    int64_t oidx = (sq * c.L + tb) * rowb + cbyte;  // byte index of this thread's output column
+    const int64_t nout = c.nseq * c.L * rowb;
+    (void)nout;
+    const uint8_t *irow = tile + (int)(tb - (tt * kTileT - (K - 1))) * kTileB;
+#pragma unroll 4
+    for (int64_t t = tb; t < te; ++t) {
+        float v[NC], acc[NC];
+        Col<IO>::load(irow, v);
+        if constexpr (NC == 2) {  // the column's two channels side by side
+            float2 a2 = fma2(make_float2(w[K - 1][0], w[K - 1][1]), make_float2(v[0], v[1]),
+                             make_float2(bias[0], bias[1]));
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j)
+                a2 = fma2(make_float2(w[K - 2 - j][0], w[K - 2 - j][1]), make_float2(hist[j][0], hist[j][1]), a2);
+            acc[0] = a2.x;
+            acc[NC - 1] = a2.y;
+            if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
+                const float2 hv = make_float2(0.5f * a2.x, 0.5f * a2.y);
+                const float2 r = fma2(hv, make_float2(tanh_approx(hv.x), tanh_approx(hv.y)), hv);
+                acc[0] = r.x;
+                acc[NC - 1] = r.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NC; ++i) {
+                acc[i] = fmaf(w[K - 1][i], v[i], bias[i]);
+#pragma unroll
+                for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
+                if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
+                    const float hv = 0.5f * acc[i];
+                    acc[i] = fmaf(hv, tanh_approx(hv), hv);
+                }
+            }
+        }
+        *reinterpret_cast<uint32_t *>(chk(out, oidx, 4, nout, c.hdr, SITE_CONV_OUT)) = Col<IO>::pack(acc);
+#pragma unroll
+        for (int j = K - 2; j > 0; --j)
+#pragma unroll
+            for (int i = 0; i < NC; ++i) hist[j][i] = hist[j - 1][i];
+        if (K > 1) {
+#pragma unroll
+            for (int i = 0; i < NC; ++i) hist[0][i] = v[i];
+        }
+        irow += kTileB;
+        oidx += rowb;
+    }
+    }
+
 template <typename IO, int K>
 __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int R = kTileT + K - 1;  // rows per stage: the tile and the k - 1 before it
     constexpr int STAGE = R * kTileB;
-    constexpr int NC = Col<IO>::C;
     const int tid = threadIdx.x;
     const int64_t rowb = c.D * (int64_t)sizeof(IO);  // bytes of one token row
     const int64_t ctiles = (rowb + kTileB - 1) / kTileB, ttiles = (c.L + kTileT - 1) / kTileT;
     const int64_t items = c.nseq * ttiles * ctiles;
     const uint8_t *in = static_cast<const uint8_t *>(c.in);
-    const IO *state = static_cast<const IO *>(c.state);
-    uint8_t *out = static_cast<uint8_t *>(c.out);
     // item -> (sequence, token tile, channel tile), channel tiles fastest
     auto load = [&](int64_t it, int st) {
         const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
@@ -109,7 +210,6 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
                        valid ? 16u : 0u);
         }
     };
-    const int col = tid % kCols, half = tid / kCols;
     const int64_t first = blockIdx.x, step = gridDim.x;
     for (int k = 0; k < kStages - 1; ++k) {
         if (first + k * step < items) load(first + k * step, k);
@@ -125,83 +225,76 @@ __global__ void __launch_bounds__(kThreads, 2) conv_kernel(ConvParams c) {
             if (nx < items) load(nx, (int)((n + kStages - 1) % kStages));
             cp_async_commit();
         }
-        const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
-        const int64_t cbyte = cb * kTileB + col * 4;
-        if (cbyte >= rowb) continue;  // past the last channel
-        const int64_t ch0 = cbyte / (int64_t)sizeof(IO);
-        const uint8_t *tile = smem + (int)(n % kStages) * STAGE + col * 4;
-        const int64_t tb = tt * kTileT + half * (kTileT / 2);  // first token of this thread's half
-        const int64_t te = tb + kTileT / 2 < c.L ? tb + kTileT / 2 : c.L;
-        if (tb >= te) continue;
-        float w[K][NC], bias[NC];
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-            bias[i] = c.bias ? c.bias[ch0 + i] : 0.f;
-#pragma unroll
-            for (int j = 0; j < K; ++j) w[j][i] = c.w[(ch0 + i) * K + j];
-        }
-        // hist[j] = input of token t - 1 - j: from the tile (rows before the sequence are zeros there), or the cache
-        float hist[K > 1 ? K - 1 : 1][NC];
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) {
-            const int64_t tp = tb - 1 - j;
-            if (tp >= 0 || !state) {
-                Col<IO>::load(tile + (int)(tp - (tt * kTileT - (K - 1))) * kTileB, hist[j]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < NC; ++i)
-                    hist[j][i] = to_f32(*chk(state, ((sq * c.D) + ch0 + i) * (K - 1) + (K - 1 + tp), 1,
-                                             c.nseq * c.D * (K - 1), c.hdr, SITE_CONV_STATE));
-            }
-        }
-        int64_t oidx = (sq * c.L + tb) * rowb + cbyte;  // byte index of this thread's output column
-        const int64_t nout = c.nseq * c.L * rowb;
-        (void)nout;
-        const uint8_t *irow = tile + (int)(tb - (tt * kTileT - (K - 1))) * kTileB;
-#pragma unroll 4
-        for (int64_t t = tb; t < te; ++t) {
-            float v[NC], acc[NC];
-            Col<IO>::load(irow, v);
-            if constexpr (NC == 2) {  // the column's two channels side by side
-                float2 a2 = fma2(make_float2(w[K - 1][0], w[K - 1][1]), make_float2(v[0], v[1]),
-                                 make_float2(bias[0], bias[1]));
-#pragma unroll
-                for (int j = 0; j < K - 1; ++j)
-                    a2 = fma2(make_float2(w[K - 2 - j][0], w[K - 2 - j][1]), make_float2(hist[j][0], hist[j][1]), a2);
-                acc[0] = a2.x;
-                acc[NC - 1] = a2.y;
-                if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
-                    const float2 hv = make_float2(0.5f * a2.x, 0.5f * a2.y);
-                    const float2 r = fma2(hv, make_float2(tanh_approx(hv.x), tanh_approx(hv.y)), hv);
-                    acc[0] = r.x;
-                    acc[NC - 1] = r.y;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NC; ++i) {
-                    acc[i] = fmaf(w[K - 1][i], v[i], bias[i]);
-#pragma unroll
-                    for (int j = 0; j < K - 1; ++j) acc[i] = fmaf(w[K - 2 - j][i], hist[j][i], acc[i]);
-                    if (c.silu) {  // v sigmoid(v) = h + h tanh(h), h = v / 2
-                        const float hv = 0.5f * acc[i];
-                        acc[i] = fmaf(hv, tanh_approx(hv), hv);
-                    }
-                }
-            }
-            *reinterpret_cast<uint32_t *>(chk(out, oidx, 4, nout, c.hdr, SITE_CONV_OUT)) = Col<IO>::pack(acc);
-#pragma unroll
-            for (int j = K - 2; j > 0; --j)
-#pragma unroll
-                for (int i = 0; i < NC; ++i) hist[j][i] = hist[j - 1][i];
-            if (K > 1) {
-#pragma unroll
-                for (int i = 0; i < NC; ++i) hist[0][i] = v[i];
-            }
-            irow += kTileB;
-            oidx += rowb;
-        }
+        conv_item<IO, K>(c, smem + (int)(n % kStages) * STAGE, it, ctiles, ttiles, tid);
     }
     cp_async_wait<0>();
+}
+
+// Bounded wait on a stage's mbarrier phase (the TMA that fills it); false after about 2 s.
+__device__ __noinline__ bool stage_wait_slow(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0; i < kMaxSpinIters; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && globaltimer() - t0 > kDefaultTimeoutNs) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ bool stage_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity) || stage_wait_slow(bar, parity);
+}
+
+// The same pipeline with one TMA box per stage ([1 sequence, R tokens, 512 bytes of channels] of a 3-D map over
+// [nseq, L, D]; rows before or past the sequence and channels past D read as zeros), issued by one thread and
+// counted on the stage's mbarrier, so no thread spends instructions on addresses. A stage is refilled only after
+// the barrier that follows everyone's use of it. A wait that runs out records SSD_ERR_DEVICE and the CTA stops
+// (after waiting, bounded, for its copies still in flight).
+template <typename IO, int K>
+__global__ void __launch_bounds__(kThreads, 2) conv_tma_kernel(ConvParams c, const __grid_constant__ CUtensorMap map) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full[kStages];
+    constexpr int R = kTileT + K - 1;
+    constexpr int STAGE = R * kTileB;
+    const int tid = threadIdx.x;
+    const int64_t rowb = c.D * (int64_t)sizeof(IO);
+    const int64_t ctiles = (rowb + kTileB - 1) / kTileB, ttiles = (c.L + kTileT - 1) / kTileT;
+    const int64_t items = c.nseq * ttiles * ctiles;
+    if (tid == 0) {
+        prefetch_tensormap(&map);
+        for (int st = 0; st < kStages; ++st) mbar_init(&full[st], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t it, int st) {  // thread 0
+        const int64_t cb = it % ctiles, rest = it / ctiles, tt = rest % ttiles, sq = rest / ttiles;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)STAGE);
+        tma_load_3d(smem + st * STAGE, &map, &full[st], (int)(cb * (kTileB / (int)sizeof(IO))),
+                    (int)(tt * kTileT - (K - 1)), (int)sq);
+    };
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    int64_t issued = 0;  // items issued so far (thread 0)
+    if (tid == 0)
+        for (int k = 0; k < kStages - 1 && first + k * step < items; ++k, ++issued) issue(first + k * step, k);
+    int64_t n = 0;
+    for (;; ++n) {
+        const int64_t it = first + n * step;
+        if (it >= items) break;
+        const int st = (int)(n % kStages);
+        const bool ok = stage_wait(&full[st], (uint32_t)((n / kStages) & 1));
+        if (__syncthreads_or(!ok)) {  // also: everyone is done with stage (n - 1) % kStages
+            if (!ok && c.hdr && atomicCAS(&c.hdr->status, 0u, (uint32_t)DEV_PIPE) == 0u) c.hdr->err_where = WAIT_PIPE;
+            break;
+        }
+        if (tid == 0) {
+            const int64_t nx = first + (n + kStages - 1) * step;
+            if (nx < items) {
+                issue(nx, (int)((n + kStages - 1) % kStages));
+                ++issued;
+            }
+        }
+        conv_item<IO, K>(c, smem + st * STAGE, it, ctiles, ttiles, tid);
+    }
+    if (tid == 0)  // only after a stop: the copies issued but not waited for land before the CTA exits
+        for (int64_t m = n; m < issued; ++m) stage_wait(&full[(int)(m % kStages)], (uint32_t)((m / kStages) & 1));
 }
 
 // The cache for continuing each sequence: its last k - 1 inputs per channel (from the cache given on entry where the
@@ -227,15 +320,60 @@ __global__ void __launch_bounds__(kThreads) conv_state_kernel(ConvParams c) {
     }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 3-D map over the raw rows [nseq, L, D], box [1, R, 512 bytes of channels], no swizzle, zeros outside. Needs a
+// 16-byte aligned base and rows a multiple of 16 bytes (else the cp.async kernel runs).
+template <typename IO>
+bool conv_map(CUtensorMap *m, const ConvParams &c, int R) {
+    const int64_t es = (int64_t)sizeof(IO), rowb = c.D * es;
+    if ((reinterpret_cast<uintptr_t>(c.in) & 15) || (rowb & 15) || c.L > INT32_MAX || c.nseq > INT32_MAX) return false;
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)c.D, (cuuint64_t)c.L, (cuuint64_t)c.nseq};
+    const cuuint64_t strides[2] = {(cuuint64_t)rowb, (cuuint64_t)(rowb * c.L)};
+    const cuuint32_t box[3] = {(cuuint32_t)(kTileB / es), (cuuint32_t)R, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : std::is_same<IO, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(m, dt, 3, const_cast<void *>(c.in), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename IO, int K>
 cudaError_t launch_k(const ConvParams &c, int sms, cudaStream_t stream) {
     const size_t smem = (size_t)kStages * (kTileT + K - 1) * kTileB;
-    auto k = conv_kernel<IO, K>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int64_t rowb = c.D * (int64_t)sizeof(IO);
     const int64_t items = c.nseq * ((c.L + kTileT - 1) / kTileT) * ((rowb + kTileB - 1) / kTileB);
     const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
+    CUtensorMap map;
+    if (conv_map<IO>(&map, c, kTileT + K - 1)) {
+        auto k = conv_tma_kernel<IO, K>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k<<<(unsigned)grid, kThreads, smem, stream>>>(c, map);
+        return cudaGetLastError();
+    }
+    auto k = conv_kernel<IO, K>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     k<<<(unsigned)grid, kThreads, smem, stream>>>(c);
     return cudaGetLastError();
 }

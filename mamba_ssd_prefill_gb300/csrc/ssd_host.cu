@@ -62,11 +62,17 @@ bool copy_streams(cudaStream_t *up, cudaStream_t *down) {
     return true;
 }
 
-// How a problem is cut and where the pieces live in the scratch.
+// How a problem is cut and where the pieces live in the scratch. Piece k holds chunks [first(k), first(k + 1)) of
+// every sequence: the first and the last piece `edge` chunks, the ones between `mid` chunks (the last of them
+// possibly fewer). Short end pieces shorten the pipeline's fill (the first upload, before any computation) and
+// drain (the last computation and download, after every other copy).
 struct HostPlan {
-    int64_t per = 0;      // tokens per piece (a multiple of chunk_size)
+    int64_t nc = 0;       // chunks per sequence
+    int64_t edge = 0;     // chunks of the first and the last piece
+    int64_t mid = 0;      // chunks of each piece between them
     int64_t pieces = 0;
-    ssd_problem_t sub{};  // the largest piece: [batch, per]
+    int64_t chunk = 0;    // tokens per chunk
+    ssd_problem_t sub{};  // the largest piece: [batch, tokens of `mid` chunks]
     size_t ws = 0;        // workspace bytes of the largest piece (at offset 0 of the scratch)
     size_t bx = 0, bdt = 0, bbc = 0;  // per-slot bytes of x (and y), dt_raw, B (and C)
     size_t slot = 0;      // bytes of one slot (kSlots of them)
@@ -91,10 +97,23 @@ ssd_status_t host_plan(const ssd_problem_t *prob, int32_t pieces, HostPlan *out)
     const int64_t want = pieces ? pieces : kDefaultPieces;
     const int64_t nc = (pr.seqlen + pr.chunk_size - 1) / pr.chunk_size;
     const int64_t n = want < nc ? want : nc;
-    hp.per = (nc + n - 1) / n * pr.chunk_size;
-    hp.pieces = (pr.seqlen + hp.per - 1) / hp.per;
+    const int64_t even = (nc + n - 1) / n;  // chunks per piece of an even cut
+    hp.nc = nc;
+    hp.chunk = pr.chunk_size;
+    hp.edge = hp.mid = even;
+    // From 8 pieces on, end pieces of a quarter of the even size and the rest shared out evenly (measured on GB300
+    // at 8 pieces: 3 % faster on the 130M-shaped batch, equal at L = 16K and batch 8; with 4 pieces the two middle
+    // pieces grew too large to overlap, up to 10 % slower, so fewer pieces are cut evenly).
+    if (n >= 8 && even >= 4) {
+        hp.edge = even / 4;
+        hp.mid = (nc - 2 * hp.edge + n - 3) / (n - 2);
+        hp.pieces = 2 + (nc - 2 * hp.edge + hp.mid - 1) / hp.mid;
+    } else {
+        hp.pieces = (nc + even - 1) / even;
+    }
+    const int64_t big = (hp.mid > hp.edge ? hp.mid : hp.edge) * pr.chunk_size;
     hp.sub = pr;
-    hp.sub.seqlen = hp.per < pr.seqlen ? hp.per : pr.seqlen;
+    hp.sub.seqlen = big < pr.seqlen ? big : pr.seqlen;
     st = ssd_fwd_workspace_size(&hp.sub, &hp.ws);
     if (st != SSD_OK) return st;
     const int64_t T = hp.sub.batch * hp.sub.seqlen;  // tokens of the largest piece
@@ -107,6 +126,15 @@ ssd_status_t host_plan(const ssd_problem_t *prob, int32_t pieces, HostPlan *out)
     hp.bytes = hp.state_off + states;
     *out = hp;
     return SSD_OK;
+}
+
+// First chunk of piece k (k = pieces: the end).
+int64_t piece_first(const HostPlan &hp, int64_t k) {
+    if (k <= 0) return 0;
+    if (k >= hp.pieces) return hp.nc;
+    if (hp.edge == hp.mid) return k * hp.mid;
+    if (k == hp.pieces - 1) return hp.nc - hp.edge;
+    return hp.edge + (k - 1) * hp.mid;
 }
 
 }  // namespace
@@ -180,8 +208,9 @@ SSD_API ssd_status_t ssd_fwd_host(const ssd_problem_t *prob, int32_t pieces, con
         const int u = (int)(k % kSlots);
         char *slot = sc + hp.ws + (size_t)u * hp.slot;
         char *dx = slot, *dy = dx + hp.bx, *ddt = dy + hp.bx, *dB = ddt + hp.bdt, *dC = dB + hp.bbc;
-        const size_t t0 = (size_t)(k * hp.per);
-        const size_t n = (L - t0) < (size_t)hp.per ? (L - t0) : (size_t)hp.per;  // tokens of the piece
+        const size_t t0 = (size_t)(piece_first(hp, k) * hp.chunk);
+        const size_t t1 = (size_t)(piece_first(hp, k + 1) * hp.chunk);
+        const size_t n = (t1 < L ? t1 : L) - t0;  // tokens of the piece
         ssd_problem_t sub = pr;
         sub.seqlen = (int64_t)n;
         // inputs of piece k into slot u, once piece k - kSlots (same slot) has been computed: per sequence, rows

@@ -160,6 +160,18 @@ def test_host_streaming_plan_and_argument_checks(lib):
     assert lib.ssd_fwd_host_scratch_size(ctypes.byref(prob(batch=1, seqlen=1000)), 8, ctypes.byref(n9)) == 0
     assert lib.ssd_fwd_host_scratch_size(ctypes.byref(prob(batch=1, seqlen=1000)), 99, ctypes.byref(n99)) == 0
     assert n9.value == n99.value
+    # from 8 pieces on the end pieces are short: 32 chunks in 8 pieces are 1, 5, 5, 5, 5, 5, 5, 1 chunks, so a slot
+    # holds 5 chunks (640 tokens), between the even cuts into 8 (4 chunks) and 4 (8 chunks) pieces
+    t8, t6, t4, ws5 = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    long = prob(batch=1, seqlen=32 * 128)
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(long), 8, ctypes.byref(t8)) == 0
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(long), 6, ctypes.byref(t6)) == 0
+    assert lib.ssd_fwd_host_scratch_size(ctypes.byref(long), 4, ctypes.byref(t4)) == 0
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(prob(batch=1, seqlen=640)), ctypes.byref(ws5)) == 0
+    tok = 640
+    slot5 = 2 * tok * 8 * 64 * 2 + tok * 8 * 2 + 2 * tok * 1 * 128 * 2
+    assert t8.value >= ws5.value + 3 * slot5 + 8 * 64 * 128 * 4
+    assert t6.value > t8.value and t4.value > t8.value  # 6 pieces: an even cut of 6 chunks each
     assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), -1, ctypes.byref(n1)) == 1      # negative piece count
     assert lib.ssd_fwd_host(ctypes.byref(p), -1, *([None] * 10), None, 0, None) == 1
     assert lib.ssd_fwd_host(ctypes.byref(p), 0, *([None] * 10), None, 0, None) == 3       # no scratch

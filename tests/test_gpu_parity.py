@@ -580,6 +580,15 @@ def test_host_streaming_piece_counts_and_empty():
         y_h, f_h = m.ssd_fwd_host(**host, chunk_size=w.chunk, pieces=pieces, scratch=scratch)
         torch.cuda.synchronize()
         assert torch.equal(y_h, y_d.cpu()) and torch.equal(f_h, f_d.cpu()), pieces
+    # from 8 pieces on, short first and last pieces (33 chunks, the last ragged: 1, 5, ..., 5, 2 or 1, 3, ..., 1)
+    w2 = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=4100, nheads=4, seed=335)
+    inp2 = make_inputs(w2, device="cuda")
+    host2 = {k: (v if k in ("dt_bias", "A", "D") else _pinned(v)) for k, v in inp2.items()}
+    y_d2, f_d2 = m.ssd_fwd(**inp2, chunk_size=w2.chunk)
+    for pieces in (0, 8, 12):
+        y_h, f_h = m.ssd_fwd_host(**host2, chunk_size=w2.chunk, pieces=pieces, scratch=scratch)
+        torch.cuda.synchronize()
+        assert torch.equal(y_h, y_d2.cpu()) and torch.equal(f_h, f_d2.cpu()), pieces
     e = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=0, nheads=4, seed=334)
     ie = make_inputs(e, device="cuda")
     he = {k: (v if k in ("dt_bias", "A", "D") else _pinned(v)) for k, v in ie.items()}
