@@ -19,6 +19,8 @@
 // stores rows coalesced. A second kernel writes the cache for continuing each sequence.
 #include <cuda.h>
 
+#include <stdlib.h>
+
 #include <type_traits>
 
 #include "sm100_ptx.cuh"
@@ -364,7 +366,10 @@ cudaError_t launch_k(const ConvParams &c, int sms, cudaStream_t stream) {
     const int64_t items = c.nseq * ((c.L + kTileT - 1) / kTileT) * ((rowb + kTileB - 1) / kTileB);
     const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
     CUtensorMap map;
-    if (conv_map<IO>(&map, c, kTileT + K - 1)) {
+    // test knob: SSD_CONV_TMA=0 runs the cp.async kernel on any rows (it serves rows that are not 16-byte multiples)
+    const char *env = getenv("SSD_CONV_TMA");
+    const bool tma_allowed = !(env && env[0] == '0');
+    if (tma_allowed && conv_map<IO>(&map, c, kTileT + K - 1)) {
         auto k = conv_tma_kernel<IO, K>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -472,6 +472,30 @@ def test_conv_then_ssd_parity(kernel, name, over, width, act, fuse):
         assert ok, s
 
 
+@pytest.mark.parametrize("io,width,act", [("bf16", 4, "silu"), ("f16", 7, "none"), ("f32", 3, "silu")])
+def test_conv_copy_pipeline_matches_tma_pipeline(io, width, act, monkeypatch):
+    """The conv kernel's two tile pipelines (one TMA box per tile, or 16-byte asynchronous copies, the form for rows
+    that are not 16-byte multiples) convolve the same staged rows with the same arithmetic: bit-identical outputs
+    and caches, and the oracle's values (ragged tiles: 333 tokens, a cache on entry)."""
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=333, nheads=4, ngroups=2, io=io, seed=64,
+                                     **({"state": "f32", "chunk": 64} if io == "f32" else {}))
+    inp = make_conv_inputs(w, width, device="cuda")
+    kw = dict(nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate, activation=act,
+              chunk_size=w.chunk, state_dtype=DTYPES[w.state])
+    outs = []
+    for tma in ("1", "0"):
+        monkeypatch.setenv("SSD_CONV_TMA", tma)
+        ws = m.Workspace("cuda")
+        outs.append(m.ssd_fwd_conv(**inp, **kw, workspace=ws, fuse=False))
+        m.check(ws)
+    (y1, f1, c1, x1), (y0, f0, c0, x0) = outs
+    assert torch.equal(x1, x0) and torch.equal(c1, c0) and torch.equal(y1, y0) and torch.equal(f1, f0)
+    xr, _ = oracle.conv1d_reference(inp["xbc"].cpu(), inp["conv_weight"].cpu(), inp["conv_bias"].cpu(),
+                                    inp["conv_state"].cpu(), act)
+    ok, s = gate_y(x0.double().cpu().numpy(), xr, w.io)
+    assert ok, s
+
+
 def test_conv_prefill_then_decode_continues_both_caches():
     """Prefill 250 tokens, then 3 single-token steps carrying the SSD state and the conv cache in place: every y and
     both final caches match the oracle over the whole 253-token sequence."""
