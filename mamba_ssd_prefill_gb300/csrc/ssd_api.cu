@@ -10,6 +10,23 @@
 #include "../../include/ssd.h"
 #include "ssd_internal.h"
 
+namespace ssd {
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;  // benign race: every caller stores the same pointer
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+}  // namespace ssd
+
 namespace {
 
 using ssd::Params;

@@ -1,6 +1,7 @@
 // Host-side interfaces between the C ABI (ssd_api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -10,6 +11,13 @@
 #include "ssd_common.cuh"
 
 namespace ssd {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry points (ssd_api.cu); null when the
+// driver has none
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 // fp32 SIMT kernel (ssd_simt.cu)
 size_t simt_smem_bytes(int64_t P, int64_t N);

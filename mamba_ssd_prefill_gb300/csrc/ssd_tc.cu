@@ -130,18 +130,13 @@ template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t 
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
 
 // ---------------------------------------------------------------- fused depthwise convolution (width 4)
-// SiLU with one special-function op: e = 2^(-v log2 e) on the SFU, then 1 / (1 + e) by Newton-Raphson steps
-// r <- r (2 - d r) from the exponent-reflection estimate (bit pattern 0x7EF311C3 - bits(d), relative error below
-// 0.13); each step squares the error, so three leave it near 1e-7, far below what the fp16 result keeps. v is
-// clamped at -80, where SiLU is 0 in fp16.
+// SiLU with one special-function op: v sigmoid(v) = h + h tanh(h) with h = v / 2, tanh by tanh.approx.f32 (the
+// form of the separate conv kernel, so both paths round alike).
 __device__ __forceinline__ float silu_fast(float v) {
-    v = fmaxf(v, -80.f);
-    const float d = 1.f + ex2(-v * kLog2e);
-    float r = __int_as_float(0x7EF311C3 - __float_as_int(d));
-    r = r * fmaf(-d, r, 2.f);
-    r = r * fmaf(-d, r, 2.f);
-    r = r * fmaf(-d, r, 2.f);
-    return v * r;
+    const float h = 0.5f * v;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
 }
 
 // The 3 raw inputs before token row0 of channels ch, ch + 1 (h[j] = token row0 - 3 + j): the rows themselves inside
@@ -1158,30 +1153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------- host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
 // 4-D map over a [1, T, mid, inner] 16-bit tensor (all sequences on one packed token axis of T tokens),
 // box = [1, box_rows, 1, 64 inner], 128B swizzle. Rows past T read as zeros; a chunk's rows past its own
 // sequence read the next sequence and are masked by dt = 0.
 bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_t mid, int64_t T, int64_t ld,
               uint32_t box_rows, bool swizzle = true) {
     const int64_t L = T, batch = 1;
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)L, (cuuint64_t)batch};
     // ld: elements from one token to the next (inner * mid when packed, more when a slice of wider rows)
