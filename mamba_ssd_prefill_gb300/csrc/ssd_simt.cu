@@ -11,6 +11,14 @@
 // in shared memory, doing the five SSD steps of "Accelerating Mamba2 with
 // Kernel Fusion" (chunk cumsum, BMM, chunk state, state passing, chunk scan)
 // at sub-chunk granularity, then publish the state leaving chunk c.
+//
+// With few chains (fewer than the resident CTAs) the chain's hops bound the launch, and each hop
+// would carry the whole chunk's work. There the unit runs in two passes: first the chunk state from
+// a zero state, s_c, and the chunk's decay a (no wait needed), then the wait, S_out = a S_in + s_c
+// published at once, and only then the pass that produces y from S_in. A hop then costs the wait,
+// one multiply-add per state element and the publish.
+#include <stdlib.h>
+
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -21,7 +29,7 @@ constexpr int kThreads = 256;
 constexpr int kSub = 32;  // tokens per sub-chunk (one warp-wide cumsum)
 
 template <typename IO, typename ST>
-__global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads) simt_kernel(Params p, int two_pass) {
     extern __shared__ float4 smem_f4[];
     float *smem = reinterpret_cast<float *>(smem_f4);
     const int P = (int)p.P, N = (int)p.N, NB = N + 1;  // padded B/C rows avoid bank conflicts
@@ -69,30 +77,11 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
         (void)Tt;
         (void)nstate;
 
-        // ---- state entering chunk c
-        if (tid == 0)
-            s_ok = aborted(hdr, epoch) ? 0
-                                       : (c == 0 ? 1 : (int)wait_flag(chk(p.flags, chain * 2 + (c & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG), chain_tag(epoch, c),
-                                                                      epoch, hdr, limit, t, (uint32_t)c));
-        __syncthreads();
-        if (!s_ok) continue;  // launch aborted: drain the remaining tickets
-        if (c == 0) {
-            for (int e = tid; e < N * P; e += kThreads) {
-                const int n = e / P, q = e % P;
-                S[e] = init ? to_f32(*chk(init, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_INIT)) : 0.f;
-            }
-        } else {
-            const int64_t slot = (chain * 2 + (c & 1)) * (int64_t)(N * P);
-            for (int e = tid; e < N * P; e += kThreads)
-                S[e] = to_f32(__ldcg(chk(ring, slot + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING)));
-        }
-        __syncthreads();
-
         // tokens [c0, c1) of the packed token axis
         const int64_t c0 = sq.tok0 + c * p.Q, end = sq.tok0 + sq.len, c1 = (c0 + p.Q < end) ? c0 + p.Q : end;
-        for (int64_t s0 = c0; s0 < c1; s0 += kSub) {
-            const int T = (int)((c1 - s0) < kSub ? (c1 - s0) : kSub);
-            // step 1: dt = softplus(dt_raw + bias), inclusive cumsum of dt*A (rows >= T: dt = 0)
+        // step 1 of a sub-chunk (dt = softplus(dt_raw + bias), inclusive cumsum of dt*A; rows >= T: dt = 0) and
+        // its x and B rows (and C rows when y is computed)
+        auto load_sub = [&](int64_t s0, int T, bool with_c) {
             if (tid < 32) {
                 float dtv = 0.f;
                 if (tid < T) dtv = softplus_f32(to_f32(*chk(dtr, (s0 + tid) * p.H + h, 1, Tt * p.H, hdr, SITE_SIMT_IN)) + bias);
@@ -116,9 +105,76 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
                 const int r = e / N, q = e % N;
                 const int64_t off = (s0 + r) * p.bc_ld + g * N + q;
                 Bs[r * NB + q] = r < T ? to_f32(*chk(Bg, off, 1, Tt * p.bc_ld, hdr, SITE_SIMT_IN)) : 0.f;
-                Cs[r * NB + q] = r < T ? to_f32(*chk(Cg, off, 1, Tt * p.bc_ld, hdr, SITE_SIMT_IN)) : 0.f;
+                if (with_c) Cs[r * NB + q] = r < T ? to_f32(*chk(Cg, off, 1, Tt * p.bc_ld, hdr, SITE_SIMT_IN)) : 0.f;
             }
             __syncthreads();
+        };
+        // steps 3 + 4 (chunk state, state passing) over a sub-chunk: S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
+        auto advance = [&](int T) {
+            const float decay = ecs[kSub - 1];
+            for (int e = tid; e < N * P; e += kThreads) {
+                const int n = e / P, q = e % P;
+                float acc = 0.f;
+                for (int j = 0; j < T; ++j) acc = fmaf(wj[j] * xs[j * P + q], Bs[j * NB + n], acc);
+                S[e] = fmaf(decay, S[e], acc);
+            }
+            __syncthreads();
+        };
+
+        // ---- two passes: the chunk state from a zero state (s_c) and the log of the chunk's decay
+        float log_a = 0.f;
+        if (two_pass) {
+            for (int e = tid; e < N * P; e += kThreads) S[e] = 0.f;
+            for (int64_t s0 = c0; s0 < c1; s0 += kSub) {
+                const int T = (int)((c1 - s0) < kSub ? (c1 - s0) : kSub);
+                load_sub(s0, T, false);
+                log_a += cs[kSub - 1];
+                advance(T);
+            }
+        }
+
+        // ---- state entering chunk c
+        if (tid == 0)
+            s_ok = aborted(hdr, epoch) ? 0
+                                       : (c == 0 ? 1 : (int)wait_flag(chk(p.flags, chain * 2 + (c & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG), chain_tag(epoch, c),
+                                                                      epoch, hdr, limit, t, (uint32_t)c));
+        __syncthreads();
+        if (!s_ok) continue;  // launch aborted: drain the remaining tickets
+        const bool publish = !last && c != skip;
+        const int64_t slot_in = (chain * 2 + (c & 1)) * (int64_t)(N * P), slot_out = (chain * 2 + ((c + 1) & 1)) * (int64_t)(N * P);
+        const float a_c = expf(log_a);  // the chunk's decay (two passes)
+        for (int e = tid; e < N * P; e += kThreads) {
+            float s_in;
+            if (c == 0) {
+                const int n = e / P, q = e % P;
+                s_in = init ? to_f32(*chk(init, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_INIT)) : 0.f;
+            } else {
+                s_in = to_f32(__ldcg(chk(ring, slot_in + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING)));
+            }
+            if (two_pass) {  // the state leaving the chunk, right away
+                const float sout = fmaf(a_c, s_in, S[e]);
+                if (publish)
+                    __stcg(chk(ring, slot_out + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING), from_f32<ST>(sout));
+                else if (last && fin) {
+                    const int n = e / P, q = e % P;
+                    *chk(fin, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_FINAL) = from_f32<ST>(sout);
+                }
+            }
+            S[e] = s_in;
+        }
+        if (two_pass && publish) {
+            __threadfence();
+            __syncthreads();
+            if (tid == 0)
+                st_release_u64(chk(p.flags, chain * 2 + ((c + 1) & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG),
+                               chain_tag(epoch, c + 1));
+        }
+        __syncthreads();
+
+        // ---- y over the chunk, the running state from S_in
+        for (int64_t s0 = c0; s0 < c1; s0 += kSub) {
+            const int T = (int)((c1 - s0) < kSub ? (c1 - s0) : kSub);
+            load_sub(s0, T, true);
             // step 2 (BMM) with the segsum decay mask: Pm[i][j] = (C_i.B_j) exp(cs_i - cs_j) dt_j, j <= i
             for (int e = tid; e < kSub * kSub; e += kThreads) {
                 const int i = e / kSub, j = e % kSub;
@@ -141,33 +197,27 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p) {
                 *chk(y, ((s0 + i) * p.H + h) * P + q, 1, Tt * p.H * P, hdr, SITE_SIMT_Y) = from_f32<IO>(v);
             }
             __syncthreads();
-            // steps 3 + 4 (chunk state, state passing): S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
-            const float decay = ecs[kSub - 1];
-            for (int e = tid; e < N * P; e += kThreads) {
-                const int n = e / P, q = e % P;
-                float acc = 0.f;
-                for (int j = 0; j < T; ++j) acc = fmaf(wj[j] * xs[j * P + q], Bs[j * NB + n], acc);
-                S[e] = fmaf(decay, S[e], acc);
-            }
-            __syncthreads();
+            // the state entering the next sub-chunk (two passes: not needed after the last one)
+            if (!two_pass || s0 + kSub < c1) advance(T);
         }
 
-        // ---- publish the state leaving chunk c
-        if (last) {
-            if (fin)
-                for (int e = tid; e < N * P; e += kThreads) {
-                    const int q = e / N, n = e % N;
-                    *chk(fin, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_FINAL) = from_f32<ST>(S[n * P + q]);
-                }
-        } else if (c != skip) {
-            const int64_t slot = (chain * 2 + ((c + 1) & 1)) * (int64_t)(N * P);
-            for (int e = tid; e < N * P; e += kThreads)
-                __stcg(chk(ring, slot + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING), from_f32<ST>(S[e]));
-            __threadfence();
-            __syncthreads();
-            if (tid == 0)
-                st_release_u64(chk(p.flags, chain * 2 + ((c + 1) & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG),
-                               chain_tag(epoch, c + 1));
+        // ---- one pass: publish the state leaving chunk c
+        if (!two_pass) {
+            if (last) {
+                if (fin)
+                    for (int e = tid; e < N * P; e += kThreads) {
+                        const int q = e / N, n = e % N;
+                        *chk(fin, (chain * P + q) * N + n, 1, nstate, hdr, SITE_SIMT_FINAL) = from_f32<ST>(S[n * P + q]);
+                    }
+            } else if (c != skip) {
+                for (int e = tid; e < N * P; e += kThreads)
+                    __stcg(chk(ring, slot_out + e, 1, p.ring_bytes / (int64_t)sizeof(ST), hdr, SITE_SIMT_RING), from_f32<ST>(S[e]));
+                __threadfence();
+                __syncthreads();
+                if (tid == 0)
+                    st_release_u64(chk(p.flags, chain * 2 + ((c + 1) & 1), 1, p.flag_count, hdr, SITE_SIMT_FLAG),
+                                   chain_tag(epoch, c + 1));
+            }
         }
         __syncthreads();
     }
@@ -197,7 +247,12 @@ cudaError_t launch_t(const Params &p, int sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t grid = p.ctab ? (int64_t)sms * per_sm : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms * per_sm);
-    k<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    // two passes where the chains are fewer than the resident CTAs (the hops bound the launch); test knob
+    // SSD_SIMT_TWO_PASS=0/1 forces one form
+    int two_pass = p.nseq * p.H < (int64_t)sms * per_sm;
+    if (const char *env = getenv("SSD_SIMT_TWO_PASS"))
+        if (env[0] == '0' || env[0] == '1') two_pass = env[0] == '1';
+    k<<<(unsigned)grid, kThreads, smem, stream>>>(p, two_pass);
     return cudaGetLastError();
 }
 

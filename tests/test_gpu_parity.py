@@ -53,6 +53,24 @@ def test_simt_parity_small(name, over):
     assert_parity(w, y, fin, yr, fr, f"simt {name} {over}")
 
 
+@pytest.mark.parametrize("two_pass", ["0", "1"])
+@pytest.mark.parametrize("name,over", [
+    ("tiny-fp32", {}),
+    ("m130-bf16", dict(batch=2, seqlen=300, nheads=3, ngroups=3, chunk=64, headdim=32, dstate=64, state="f16",
+                       init="normal")),
+    ("tiny-fp32", dict(batch=3, seqlen=200, nheads=2, chunk=32, init="normal")),
+], ids=["tiny", "bf16-f16-ragged", "fp32-init"])
+def test_simt_one_and_two_passes(name, over, two_pass, monkeypatch):
+    """The SIMT kernel walks each chunk once (the entering state awaited first) or twice (the chunk state from zero
+    first, the leaving state published right after the wait, then y): both against the oracle."""
+    monkeypatch.setenv("SSD_SIMT_TWO_PASS", two_pass)
+    w = WORKLOADS[name].with_(**over)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp, kernel="simt")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"simt two_pass={two_pass} {name} {over}")
+
+
 def test_simt_no_D_no_init():
     w = WORKLOADS["m130-bf16"].with_(batch=1, seqlen=150, nheads=2, init="none")
     inp = make_inputs(w, device="cuda")
