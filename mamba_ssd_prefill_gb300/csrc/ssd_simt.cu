@@ -29,7 +29,7 @@ constexpr int kThreads = 256;
 constexpr int kSub = 32;  // tokens per sub-chunk (one warp-wide cumsum)
 
 template <typename IO, typename ST>
-__global__ void __launch_bounds__(kThreads) simt_kernel(Params p, int two_pass) {
+__global__ void __launch_bounds__(kThreads, 3) simt_kernel(Params p, int two_pass) {
     extern __shared__ float4 smem_f4[];
     float *smem = reinterpret_cast<float *>(smem_f4);
     const int P = (int)p.P, N = (int)p.N, NB = N + 1;  // padded B/C rows avoid bank conflicts
@@ -109,14 +109,42 @@ __global__ void __launch_bounds__(kThreads) simt_kernel(Params p, int two_pass) 
             }
             __syncthreads();
         };
-        // steps 3 + 4 (chunk state, state passing) over a sub-chunk: S = exp(cs_last) S + sum_j w_j x_j (outer) B_j
+        // steps 3 + 4 (chunk state, state passing) over a sub-chunk: S = exp(cs_last) S + sum_j w_j x_j (outer) B_j.
+        // Where N and P are multiples of 4, a thread owns 4 x 4 blocks of S (4 state rows n, 4 columns q): per token
+        // one 16-byte x load and 4 B loads feed 16 multiply-adds, against two loads per multiply-add otherwise.
         auto advance = [&](int T) {
             const float decay = ecs[kSub - 1];
-            for (int e = tid; e < N * P; e += kThreads) {
-                const int n = e / P, q = e % P;
-                float acc = 0.f;
-                for (int j = 0; j < T; ++j) acc = fmaf(wj[j] * xs[j * P + q], Bs[j * NB + n], acc);
-                S[e] = fmaf(decay, S[e], acc);
+            if ((N & 3) == 0 && (P & 3) == 0) {
+                const int qb_n = P / 4;
+                for (int blk = tid; blk < (N / 4) * qb_n; blk += kThreads) {
+                    const int q0 = 4 * (blk % qb_n), n0 = 4 * (blk / qb_n);
+                    float acc[4][4] = {};
+                    for (int j = 0; j < T; ++j) {
+                        const float4 xv = *reinterpret_cast<const float4 *>(xs + j * P + q0);
+                        const float w = wj[j];
+                        const float xw[4] = {w * xv.x, w * xv.y, w * xv.z, w * xv.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float b = Bs[j * NB + n0 + k];
+#pragma unroll
+                            for (int l = 0; l < 4; ++l) acc[k][l] = fmaf(xw[l], b, acc[k][l]);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float4 *row = reinterpret_cast<float4 *>(S + (n0 + k) * P + q0);
+                        const float4 sv = *row;
+                        *row = make_float4(fmaf(decay, sv.x, acc[k][0]), fmaf(decay, sv.y, acc[k][1]),
+                                           fmaf(decay, sv.z, acc[k][2]), fmaf(decay, sv.w, acc[k][3]));
+                    }
+                }
+            } else {
+                for (int e = tid; e < N * P; e += kThreads) {
+                    const int n = e / P, q = e % P;
+                    float acc = 0.f;
+                    for (int j = 0; j < T; ++j) acc = fmaf(wj[j] * xs[j * P + q], Bs[j * NB + n], acc);
+                    S[e] = fmaf(decay, S[e], acc);
+                }
             }
             __syncthreads();
         };
