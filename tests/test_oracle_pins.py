@@ -279,3 +279,27 @@ def test_conv_oracle_against_numpy_convolve_and_silu():
     o2, s2 = oracle.conv1d_reference(x[:, 4:], w, bias, s1)
     close(np.concatenate([o1, o2], axis=1), out, 1e-15)
     close(s2, st_out, 0.0)
+
+
+def test_conv_oracle_width_one_and_sequences_shorter_than_the_cache():
+    """Width 1 (no history: a per-channel scale and bias, an empty cache) and widths up to 8 on sequences shorter
+    than the cache (the cache leaving the sequence is then the tail of [cache on entry, tokens]), each against
+    numpy's convolution of [cache, tokens] with the flipped taps."""
+    rng = np.random.default_rng(11)
+    b, D = 2, 3
+    x = rng.standard_normal((b, 5, D))
+    w1 = rng.standard_normal((D, 1))
+    bias = rng.standard_normal(D)
+    out, st = oracle.conv1d_reference(x, w1, bias, None, activation="none")
+    close(out, x * w1[:, 0] + bias, 1e-15)
+    assert st.shape == (b, D, 0)
+    for k, L in ((6, 2), (8, 1), (8, 7), (5, 4)):
+        xs = rng.standard_normal((b, L, D))
+        w = rng.standard_normal((D, k))
+        cache = rng.standard_normal((b, D, k - 1))
+        out, st = oracle.conv1d_reference(xs, w, bias, cache, activation="none")
+        for bi in range(b):
+            for ch in range(D):
+                seq = np.concatenate([cache[bi, ch], xs[bi, :, ch]])
+                close(out[bi, :, ch], np.convolve(seq, w[ch, ::-1], mode="valid") + bias[ch], 1e-13)
+                close(st[bi, ch], seq[-(k - 1):], 0.0)
