@@ -215,14 +215,51 @@ __global__ void __launch_bounds__(kThreads, 3) simt_kernel(Params p, int two_pas
                 Pm[e] = v;
             }
             __syncthreads();
-            // step 5 (chunk scan): y_i = sum_j Pm_ij x_j + exp(cs_i) C_i . S + D x_i
-            for (int e = tid; e < T * P; e += kThreads) {
-                const int i = e / P, q = e % P;
-                float a1 = 0.f, a2 = 0.f;
-                for (int j = 0; j <= i; ++j) a1 = fmaf(Pm[i * kSub + j], xs[j * P + q], a1);
-                for (int n = 0; n < N; ++n) a2 = fmaf(Cs[i * NB + n], S[n * P + q], a2);
-                const float v = a1 + ecs[i] * a2 + Dh * xs[i * P + q];
-                *chk(y, ((s0 + i) * p.H + h) * P + q, 1, Tt * p.H * P, hdr, SITE_SIMT_Y) = from_f32<IO>(v);
+            // step 5 (chunk scan): y_i = sum_j Pm_ij x_j + exp(cs_i) C_i . S + D x_i. Where P is a multiple of 4, a
+            // thread owns 2 tokens x 4 columns: per step one 16-byte load of x (or S) and two of Pm (or C) feed 8
+            // multiply-adds, in the scalar loop's order (row i0's extra term j = i0 + 1 has Pm = 0: exact).
+            if ((P & 3) == 0) {
+                const int qb_n = P / 4;
+                for (int blk = tid; blk < (kSub / 2) * qb_n; blk += kThreads) {
+                    const int q0 = 4 * (blk % qb_n), i0 = 2 * (blk / qb_n);
+                    if (i0 >= T) continue;
+                    float a1[2][4] = {}, a2[2][4] = {};
+                    for (int j = 0; j <= i0 + 1; ++j) {
+                        const float4 xv = *reinterpret_cast<const float4 *>(xs + j * P + q0);
+                        const float p0 = Pm[i0 * kSub + j], p1 = Pm[(i0 + 1) * kSub + j];
+                        a1[0][0] = fmaf(p0, xv.x, a1[0][0]); a1[0][1] = fmaf(p0, xv.y, a1[0][1]);
+                        a1[0][2] = fmaf(p0, xv.z, a1[0][2]); a1[0][3] = fmaf(p0, xv.w, a1[0][3]);
+                        a1[1][0] = fmaf(p1, xv.x, a1[1][0]); a1[1][1] = fmaf(p1, xv.y, a1[1][1]);
+                        a1[1][2] = fmaf(p1, xv.z, a1[1][2]); a1[1][3] = fmaf(p1, xv.w, a1[1][3]);
+                    }
+                    for (int n = 0; n < N; ++n) {
+                        const float4 sv = *reinterpret_cast<const float4 *>(S + n * P + q0);
+                        const float c0 = Cs[i0 * NB + n], c1 = Cs[(i0 + 1) * NB + n];
+                        a2[0][0] = fmaf(c0, sv.x, a2[0][0]); a2[0][1] = fmaf(c0, sv.y, a2[0][1]);
+                        a2[0][2] = fmaf(c0, sv.z, a2[0][2]); a2[0][3] = fmaf(c0, sv.w, a2[0][3]);
+                        a2[1][0] = fmaf(c1, sv.x, a2[1][0]); a2[1][1] = fmaf(c1, sv.y, a2[1][1]);
+                        a2[1][2] = fmaf(c1, sv.z, a2[1][2]); a2[1][3] = fmaf(c1, sv.w, a2[1][3]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int i = i0 + r;
+                        if (i >= T) break;
+#pragma unroll
+                        for (int l = 0; l < 4; ++l) {
+                            const float v = a1[r][l] + ecs[i] * a2[r][l] + Dh * xs[i * P + q0 + l];
+                            *chk(y, ((s0 + i) * p.H + h) * P + q0 + l, 1, Tt * p.H * P, hdr, SITE_SIMT_Y) = from_f32<IO>(v);
+                        }
+                    }
+                }
+            } else {
+                for (int e = tid; e < T * P; e += kThreads) {
+                    const int i = e / P, q = e % P;
+                    float a1 = 0.f, a2 = 0.f;
+                    for (int j = 0; j <= i; ++j) a1 = fmaf(Pm[i * kSub + j], xs[j * P + q], a1);
+                    for (int n = 0; n < N; ++n) a2 = fmaf(Cs[i * NB + n], S[n * P + q], a2);
+                    const float v = a1 + ecs[i] * a2 + Dh * xs[i * P + q];
+                    *chk(y, ((s0 + i) * p.H + h) * P + q, 1, Tt * p.H * P, hdr, SITE_SIMT_Y) = from_f32<IO>(v);
+                }
             }
             __syncthreads();
             // the state entering the next sub-chunk (two passes: not needed after the last one)
