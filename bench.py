@@ -4,10 +4,12 @@
 
 A step is one call of the whole fused path (chunk cumsum, BMM, chunk state,
 state passing, chunk scan) over one batch of synthetic inputs. The default
-workload is the Mamba-2 130M-shaped layer (batch 4, seqlen 4096, 24 heads,
-headdim 64, d_state 128, chunk 128, bf16 I/O, fp32 states, init ~ N(0, 0.1)).
-Its 116 MB of inputs and outputs fit in L2, so a 512 MiB buffer is written
-before every step, outside the timed events.
+workload is the long-context layer (batch 1, seqlen 262144, 80 heads in 8
+groups, headdim 64, d_state 128, chunk 128, bf16 I/O, fp32 states, no initial
+state), the largest of the single-GPU workloads: its 6.5 GB of inputs and
+outputs are far larger than L2, and a 512 MiB buffer is still written before
+every step, outside the timed events (other workloads fit in L2). The step
+time is the median of the per-step CUDA-event timings.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the (batch, head) chains need no exchange); the time is the
@@ -32,11 +34,11 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs  # noqa: E402
+from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_chain_inputs, make_inputs  # noqa: E402
 
 METRIC = "SSD prefill tokens/s per layer at 1 GB300; % of roofline (HBM vs tensor)"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "m130-bf16"
+DEFAULT_WORKLOAD = "long-L256k-g8"
 FLUSH_BYTES = 512 * 1024 * 1024
 
 
@@ -186,34 +188,34 @@ def replica_throughput(world, tokens_per_rank, ms_per_step_max):
     return world * tokens_per_rank / (ms_per_step_max * 1e-3)
 
 
-def oracle_sample(w, inp_cpu, budget_s, min_reps=1):
-    """Time the oracle on whole chains of the workload for about budget_s; returns (tokens/s, sample text, threads)."""
-    import oracle
-
-    b, L, H, P = inp_cpu["x"].shape
+def device_chains(w, inp, n, rng):
+    """n random (sequence, head) chains of the device inputs, copied to the host as float64 (only those chains)."""
+    b, L, H, P = inp["x"].shape
     per = H // w.ngroups
-    # gather chains once (float64), outside the timed region
-    rng = np.random.default_rng(0)
     order = [(bi, h) for bi in range(b) for h in range(H)]
     rng.shuffle(order)
+    ch = order[:min(n, len(order))]
+    hs = np.array([h for _, h in ch])
+
+    def stack(f):
+        return torch.stack([f(bi, h) for bi, h in ch]).double().cpu().numpy()
+
+    init = None if inp["init_states"] is None else stack(lambda bi, h: inp["init_states"][bi, h])
+    return dict(x=stack(lambda bi, h: inp["x"][bi, :, h]), dt_raw=stack(lambda bi, h: inp["dt_raw"][bi, :, h]),
+                dt_bias=inp["dt_bias"].double().cpu().numpy()[hs], A=inp["A"].double().cpu().numpy()[hs],
+                B=stack(lambda bi, h: inp["B"][bi, :, h // per]), C=stack(lambda bi, h: inp["C"][bi, :, h // per]),
+                D=inp["D"].double().cpu().numpy()[hs], init=init), len(order)
+
+
+def oracle_sample(w, chains, total_chains, budget_s, min_reps=1):
+    """Time the oracle on whole chains (float64 arrays of a sample of the workload's chains) for about budget_s;
+    returns (tokens/s, sample text, threads)."""
+    import oracle
+
     threads = oracle.default_threads()
-    # size the sample: start with one chain per thread and grow
-    n = min(len(order), threads)
-    chains = order[:n]
-
-    def gather(ch):
-        x = np.stack([inp_cpu["x"][bi, :, h].double().numpy() for bi, h in ch])
-        dtr = np.stack([inp_cpu["dt_raw"][bi, :, h].double().numpy() for bi, h in ch])
-        B = np.stack([inp_cpu["B"][bi, :, h // per].double().numpy() for bi, h in ch])
-        C = np.stack([inp_cpu["C"][bi, :, h // per].double().numpy() for bi, h in ch])
-        hs = np.array([h for _, h in ch])
-        init = None
-        if inp_cpu["init_states"] is not None:
-            init = np.stack([inp_cpu["init_states"][bi, h].double().numpy() for bi, h in ch])
-        return (x, dtr, inp_cpu["dt_bias"].double().numpy()[hs], inp_cpu["A"].double().numpy()[hs], B, C,
-                inp_cpu["D"].double().numpy()[hs], init)
-
-    args = gather(chains)
+    n, L = chains["x"].shape[0], chains["x"].shape[1]
+    args = (chains["x"], chains["dt_raw"], chains["dt_bias"], chains["A"], chains["B"], chains["C"], chains["D"],
+            chains["init"])
     t0 = time.perf_counter()
     oracle.ssd_chains(*args, nthreads=threads)
     dt1 = time.perf_counter() - t0
@@ -223,9 +225,9 @@ def oracle_sample(w, inp_cpu, budget_s, min_reps=1):
     for _ in range(reps):
         oracle.ssd_chains(*args, nthreads=threads)
     el = time.perf_counter() - t0
-    chain_tokens = reps * len(chains) * L
-    tok_s = chain_tokens / H / el  # a token is one position across all heads
-    sample = (f"{len(chains)} of {b * H} (batch, head) chains x {L} tokens, {reps} repetitions, "
+    chain_tokens = reps * n * L
+    tok_s = chain_tokens / w.nheads / el  # a token is one position across all heads
+    sample = (f"{n} of {total_chains} (sequence, head) chains x {L} tokens, {reps} repetitions, "
               f"{el:.1f} s; tokens/s = chain-tokens / nheads / seconds")
     return tok_s, sample, threads
 
@@ -234,12 +236,16 @@ def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    inp = make_inputs(w, device="cpu")
+    import oracle
+
+    # only the sampled chains are drawn (the whole long-context batch would be gigabytes of host arrays)
+    chains = make_chain_inputs(w, min(w.batch * w.nheads, oracle.default_threads()))
     cfg = workload_config(w)
+    cfg["reference_inputs"] = "the sampled chains drawn directly with the workload's recipe (make_chain_inputs)"
     per_step = []
     budget = min(args.ref_budget, 150.0 / (args.warmup + args.steps))  # whole run within a few minutes
     for s in range(args.warmup + args.steps):
-        tok_s, sample, threads = oracle_sample(w, inp, budget_s=budget)
+        tok_s, sample, threads = oracle_sample(w, chains, w.batch * w.nheads, budget_s=budget)
         if s >= args.warmup:
             per_step.append(tok_s)
     v = float(np.median(per_step))
@@ -305,7 +311,7 @@ def run_gpu(args, w):
     barrier(world)
     m.check(ws)
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = max_over_ranks(float(np.mean(times)), world)
+    ms = max_over_ranks(float(np.median(times)), world)
     value = replica_throughput(world, w.tokens, ms)
 
     # end to end through the public API with host buffers: ssd_fwd_host takes the pinned host inputs and outputs
@@ -367,8 +373,10 @@ def run_gpu(args, w):
                     "path": "ssd_fwd_host: pinned host buffers streamed in 8 token pieces (copies overlap compute)"},
             "gpu_launches": args.steps, "clocks": clk.summary(wall0, wall1, load_end)}
     if world == 1 and not args.no_cpu_baseline:
-        tok_s, sample, threads = oracle_sample(w, {k: (v.cpu() if v is not None else None) for k, v in inp.items()},
-                                               budget_s=args.ref_budget)
+        import oracle
+
+        chains, total = device_chains(w, inp, oracle.default_threads(), np.random.default_rng(0))
+        tok_s, sample, threads = oracle_sample(w, chains, total, budget_s=args.ref_budget)
         line["cpu_baseline"] = {"value": tok_s, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
 

@@ -91,7 +91,9 @@ typedef struct {
 /* Bytes of workspace ssd_fwd needs for `prob` (written to *bytes). The
  * workspace must be zero-filled once before its first use; after that each
  * call leaves it ready for the next one (launches on one stream may reuse it
- * back to back; concurrent launches need separate workspaces). */
+ * back to back; concurrent launches need separate workspaces). State-passing
+ * tags carry the workspace's launch count modulo 2^30 (fp16 states) or 2^32:
+ * zero-fill a workspace again before its 2^30-th launch. */
 SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes);
 
 /* Launch the fused SSD prefill forward on `stream` (a cudaStream_t, NULL for
@@ -182,6 +184,25 @@ SSD_API ssd_status_t ssd_fwd_check(void *workspace, void *stream);
  * the buffers' extents; an index outside is never used (the access goes to
  * the buffer's first element) and ssd_fwd_check reports SSD_ERR_DEVICE. */
 SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t skip_publish, void *stream);
+
+/* Process-wide test hooks that force a kernel's launch configuration, for
+ * tests that compare each form with the default one and with the oracle. Every
+ * argument is -1 for the library's own choice (the state at load time); any
+ * other value must be valid for its field, else SSD_ERR_INVALID_ARG and
+ * nothing changes:
+ *  tc_heads_per_unit  tensor-core kernel: heads per work unit, 1 .. 8 (used only
+ *                     when it divides nheads / ngroups)
+ *  tc_late_ticket     tensor-core kernel: 0 = every next work ticket taken one
+ *                     unit ahead, 1 = only when the unit before nears its end
+ *  simt_two_pass      fp32 SIMT kernel: 0 = one pass per unit, 1 = the chunk
+ *                     state before the entering state is awaited, then y
+ *  conv_tma           depthwise convolution: 0 = the 16-byte-copy pipeline
+ *                     (the form for rows that are not 16-byte multiples),
+ *                     1 = the TMA-fed one where the rows allow it
+ * The values are read by later calls on any host thread (not by calls already
+ * queued). The library reads no environment variable. */
+SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
+                                     int32_t conv_tma);
 
 /* ssd_fwd without a workspace argument, for callers that cannot allocate
  * device memory (no counterpart on the pages; it is a library convenience).

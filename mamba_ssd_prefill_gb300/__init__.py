@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "kernel_for", "SsdError",
+__all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "debug_knobs", "kernel_for", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
 # MAMBA_SSD_LIB selects another build of the library (the bounds-checked debug build, libmamba_ssd_checked.so)
@@ -75,6 +75,8 @@ def lib():
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
             L.ssd_debug_set.restype = ctypes.c_int
+            L.ssd_debug_knobs.argtypes = [ctypes.c_int32] * 4
+            L.ssd_debug_knobs.restype = ctypes.c_int
             L.ssd_fwd_kernel_for.argtypes = [pp]
             L.ssd_fwd_kernel_for.restype = ctypes.c_int
             L.ssd_status_string.argtypes = [ctypes.c_int]
@@ -363,3 +365,10 @@ def debug_set(workspace, timeout_ns=0, skip_publish=-1, stream=None):
     st = lib().ssd_debug_set(_ptr(ws), int(timeout_ns), int(skip_publish), _stream_ptr(stream, ws.device))
     if st:
         raise SsdError(st, "ssd_debug_set")
+
+
+def debug_knobs(tc_heads_per_unit=-1, tc_late_ticket=-1, simt_two_pass=-1, conv_tma=-1):
+    """Test hook: force launch-configuration choices of later calls (-1 everywhere restores the library's own)."""
+    st = lib().ssd_debug_knobs(int(tc_heads_per_unit), int(tc_late_ticket), int(simt_two_pass), int(conv_tma))
+    if st:
+        raise SsdError(st, "ssd_debug_knobs")

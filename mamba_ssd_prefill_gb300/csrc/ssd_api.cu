@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/ssd.h"
 #include "ssd_internal.h"
@@ -25,6 +26,15 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
+namespace {
+std::atomic<int> g_knob[4] = {{-1}, {-1}, {-1}, {-1}};  // heads per unit, late ticket, SIMT two pass, conv TMA
+}  // namespace
+
+Knobs knobs() {
+    return Knobs{g_knob[0].load(std::memory_order_relaxed), g_knob[1].load(std::memory_order_relaxed),
+                 g_knob[2].load(std::memory_order_relaxed), g_knob[3].load(std::memory_order_relaxed)};
+}
+
 }  // namespace ssd
 
 namespace {
@@ -33,15 +43,18 @@ using ssd::Params;
 using ssd::WsHeader;
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];  // 0 = not queried yet (benign race: same value)
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 = not queried yet (threads that race store the same value)
 
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+    if (dev < kMaxDevices) {
+        const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < kMaxDevices) g_sm_count[dev] = n;
+    if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -127,17 +140,14 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
         // for a variable-length batch the chunk count is only bounded here (pairs <= nc + nseq); it sizes the units
         const int64_t pairs = varlen ? pl.nc + pl.nseq : pl.nc * pr->batch;
         pl.heads_per_unit = ssd::tc_heads_per_unit(1, pr->nheads, pr->ngroups, pairs, std::max(1, sm_count()));
-        // test knob: force the heads per work unit (must divide nheads / ngroups, at most 8)
-        if (const char *env = getenv("SSD_TC_HEADS_PER_UNIT")) {
-            const int hs = atoi(env);
-            if (hs >= 1 && hs <= 8 && (pr->nheads / pr->ngroups) % hs == 0) pl.heads_per_unit = hs;
-        }
+        const ssd::Knobs kn = ssd::knobs();
+        // test hook: forced heads per work unit (used when it divides nheads / ngroups)
+        if (kn.tc_heads_per_unit >= 1 && (pr->nheads / pr->ngroups) % kn.tc_heads_per_unit == 0)
+            pl.heads_per_unit = kn.tc_heads_per_unit;
         units = (double)pairs * (double)(pr->nheads / pl.heads_per_unit);
         pl.late_ticket = ssd::tc_late_ticket(pl.nseq * (pr->nheads / pl.heads_per_unit), std::max(1, sm_count()));
-        // test knob: force early (0) or late (1) tickets
-        if (const char *env = getenv("SSD_TC_LATE_TICKET")) {
-            if (env[0] == '0' || env[0] == '1') pl.late_ticket = env[0] == '1';
-        }
+        // test hook: forced early (0) or late (1) tickets
+        if (kn.tc_late_ticket >= 0) pl.late_ticket = kn.tc_late_ticket == 1;
     } else {
         units = (double)(varlen ? pl.nc + pl.nseq : pl.nc * pr->batch) * (double)pr->nheads;
     }
@@ -389,6 +399,19 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
     const uint32_t probe = skip_publish == -2 ? 1u : 0u;  // bounds-checked builds: plant one index past its end
     if (cudaMemcpy(&hdr->bounds_probe, &probe, sizeof(probe), cudaMemcpyHostToDevice) != cudaSuccess)
         return SSD_ERR_CUDA;
+    return SSD_OK;
+}
+
+SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
+                                     int32_t conv_tma) {
+    if (tc_heads_per_unit != -1 && (tc_heads_per_unit < 1 || tc_heads_per_unit > 8)) return SSD_ERR_INVALID_ARG;
+    if (tc_late_ticket < -1 || tc_late_ticket > 1 || simt_two_pass < -1 || simt_two_pass > 1 || conv_tma < -1 ||
+        conv_tma > 1)
+        return SSD_ERR_INVALID_ARG;
+    ssd::g_knob[0].store(tc_heads_per_unit, std::memory_order_relaxed);
+    ssd::g_knob[1].store(tc_late_ticket, std::memory_order_relaxed);
+    ssd::g_knob[2].store(simt_two_pass, std::memory_order_relaxed);
+    ssd::g_knob[3].store(conv_tma, std::memory_order_relaxed);
     return SSD_OK;
 }
 

@@ -349,9 +349,9 @@ cudaError_t launch_k(const ConvParams &c, int sms, cudaStream_t stream) {
     const int64_t items = c.nseq * ((c.L + kTileT - 1) / kTileT) * ((rowb + kTileB - 1) / kTileB);
     const int64_t grid = std::min<int64_t>(items, (int64_t)sms * 2);
     CUtensorMap map;
-    // test knob: SSD_CONV_TMA=0 runs the cp.async kernel on any rows (it serves rows that are not 16-byte multiples)
-    const char *env = getenv("SSD_CONV_TMA");
-    const bool tma_allowed = !(env && env[0] == '0');
+    // conv_tma test hook (ssd_debug_knobs) 0: the cp.async kernel on any rows (it serves rows that are not 16-byte
+    // multiples)
+    const bool tma_allowed = knobs().conv_tma != 0;
     if (tma_allowed && conv_map<IO>(&map, c, kTileT + K - 1)) {
         auto k = conv_tma_kernel<IO, K>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

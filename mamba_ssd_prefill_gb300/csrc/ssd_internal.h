@@ -19,6 +19,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// Launch-configuration overrides set by ssd_debug_knobs (test hooks; -1 = the library's own choice).
+struct Knobs {
+    int tc_heads_per_unit, tc_late_ticket, simt_two_pass, conv_tma;
+};
+Knobs knobs();
+
 // fp32 SIMT kernel (ssd_simt.cu)
 size_t simt_smem_bytes(int64_t P, int64_t N);
 cudaError_t launch_simt(const Params &p, int io_dtype, int state_dtype, int sms, cudaStream_t stream);

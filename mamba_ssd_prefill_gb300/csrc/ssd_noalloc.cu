@@ -22,6 +22,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/ssd.h"
 
 namespace {
@@ -31,7 +33,9 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-void *g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device (null until looked up)
+// device address of g_static_scratch, per device (null until looked up; host threads that race on a first call
+// look it up alike and store the same value)
+std::atomic<void *> g_scratch_addr[kMaxDevices];
 
 }  // namespace
 
@@ -45,12 +49,11 @@ extern "C" SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob
     if (need > kStaticScratchBytes) return SSD_ERR_WORKSPACE;  // problem too large for the static scratch
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
-    if (!g_scratch_addr[dev]) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return SSD_ERR_CUDA;
-        g_scratch_addr[dev] = addr;
+    void *ws = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!ws) {
+        if (cudaGetSymbolAddress(&ws, g_static_scratch) != cudaSuccess || !ws) return SSD_ERR_CUDA;
+        g_scratch_addr[dev].store(ws, std::memory_order_release);
     }
-    void *ws = g_scratch_addr[dev];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (prob->batch > 0 && prob->seqlen > 0 && cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return SSD_ERR_CUDA;
     return ssd_fwd(prob, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, ws, kStaticScratchBytes,

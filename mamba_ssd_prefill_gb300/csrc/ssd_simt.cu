@@ -312,11 +312,11 @@ cudaError_t launch_t(const Params &p, int sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     const int64_t grid = p.ctab ? (int64_t)sms * per_sm : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms * per_sm);
-    // two passes where the chains are fewer than the resident CTAs (the hops bound the launch); test knob
-    // SSD_SIMT_TWO_PASS=0/1 forces one form
+    // two passes where the chains are fewer than the resident CTAs (the hops bound the launch); the
+    // simt_two_pass test hook (ssd_debug_knobs) forces one form
     int two_pass = p.nseq * p.H < (int64_t)sms * per_sm;
-    if (const char *env = getenv("SSD_SIMT_TWO_PASS"))
-        if (env[0] == '0' || env[0] == '1') two_pass = env[0] == '1';
+    const int forced = knobs().simt_two_pass;
+    if (forced >= 0) two_pass = forced;
     k<<<(unsigned)grid, kThreads, smem, stream>>>(p, two_pass);
     return cudaGetLastError();
 }

@@ -929,7 +929,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chain, with no CTA barrier on either side of a hop:
         //  - fp32 states: the row, then its own release flag (a 64-bit tag epoch:chunk); after each publish the
         //    next head's row is prefetched when its flag is already visible;
-        //  - fp16 states: every 8-byte ring word carries two values and the tag epoch * 4096 + chunk. An aligned
+        //  - fp16 states: every 8-byte ring word carries two values and the 32-bit tag epoch * 4 + (chunk mod 4)
+        //    (a slot only has to tell chunk c from c - 2, its previous occupant, and from older launches). An aligned
         //    8-byte access is single-copy atomic, so a word with the expected tag holds this launch's values for
         //    that chunk: the data is its own flag (no release, no flag load), which shortens the serial chain of
         //    hops by a round trip. (fp32 rows would need 128 registers in flight this way.)
@@ -960,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return chk(ringv, (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1, nvec, hdr,
                        SITE_TC_RING);
         };
-        auto vtag = [&](int c) { return epoch * 4096u + (uint32_t)(c & 4095); };
+        auto vtag = [&](int c) { return (epoch << 2) | (uint32_t)(c & 3); };
         // fp16: the tagged row of chunk c as loaded, and whether any of its words is stale
         uint64_t raw[kTagged ? kP / 2 : 1];
         auto issue_tagged = [&](int64_t chain, int c) {

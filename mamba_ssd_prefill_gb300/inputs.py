@@ -143,3 +143,23 @@ def make_conv_inputs(w: Workload, width: int = 4, device="cpu", seed: int | None
     out["conv_state"] = (torch.randn(w.batch, D, width - 1, generator=g, device=device).to(DTYPES[w.io])
                          if conv_state and width > 1 else None)
     return out
+
+
+def make_chain_inputs(w: Workload, n: int, seed: int | None = None) -> dict:
+    """n independent (sequence, head) chains of workload ``w`` drawn directly on the CPU in float64, with the value
+    recipe above, for timing the oracle on a bounded sample without materialising the whole batch: x [n, L, P],
+    dt_raw [n, L], B/C [n, L, N] (the B and C columns of each chain's group), dt_bias/A/D [n] (each chain's head
+    drawn from the per-head recipe), init [n, P, N] or None. The numbers are not those of ``make_inputs`` (a
+    different generator layout); the shapes and distributions are."""
+    import numpy as np
+
+    seed = w.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    L, P, N = w.seqlen, w.headdim, w.dstate
+    dt0 = np.exp(rng.uniform(math.log(w.dt_lo), math.log(0.1), n))
+    out = dict(x=rng.standard_normal((n, L, P)), dt_raw=rng.standard_normal((n, L)),
+               dt_bias=np.log(np.expm1(dt0)), A=-np.exp(rng.uniform(0.0, math.log(16.0), n)),
+               B=rng.standard_normal((n, L, N)), C=rng.standard_normal((n, L, N)), D=rng.standard_normal(n))
+    out["init"] = rng.standard_normal((n, P, N)) * 0.1 if w.init == "normal" else (
+        np.zeros((n, P, N)) if w.init == "zeros" else None)
+    return out

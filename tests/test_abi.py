@@ -190,3 +190,24 @@ def test_bounds_checked_build_compiles_and_exports_every_symbol():
     L = ctypes.CDLL(path)
     for name in declared_functions():
         assert hasattr(L, name), name
+
+
+def test_debug_knobs_validate_and_restore(lib):
+    """The launch-configuration test hooks take -1 (the library's choice) or a valid value, and reject the rest
+    without changing anything."""
+    assert lib.ssd_debug_knobs(-1, -1, -1, -1) == 0
+    for bad in [(0, -1, -1, -1), (9, -1, -1, -1), (-1, 2, -1, -1), (-1, -1, -2, -1), (-1, -1, -1, 5)]:
+        assert lib.ssd_debug_knobs(*bad) == 1, bad
+    assert lib.ssd_debug_knobs(8, 1, 0, 0) == 0
+    m.debug_knobs()  # restore
+    with pytest.raises(m.SsdError):
+        m.debug_knobs(tc_heads_per_unit=0)
+
+
+def test_library_sources_read_no_environment():
+    """Launch choices come from the problem and the explicit test hooks only: no kernel or host file of the
+    library reads an environment variable."""
+    csrc = os.path.join(ROOT, "mamba_ssd_prefill_gb300", "csrc")
+    for fn in os.listdir(csrc):
+        src = open(os.path.join(csrc, fn)).read()
+        assert "getenv" not in src, fn

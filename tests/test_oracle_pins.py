@@ -303,3 +303,53 @@ def test_conv_oracle_width_one_and_sequences_shorter_than_the_cache():
                 seq = np.concatenate([cache[bi, ch], xs[bi, :, ch]])
                 close(out[bi, :, ch], np.convolve(seq, w[ch, ::-1], mode="valid") + bias[ch], 1e-13)
                 close(st[bi, ch], seq[-(k - 1):], 0.0)
+
+
+def test_conv_ssd_oracle_channel_split_worked_example():
+    """The x | B | C split of the convolved rows (x the first H*P channels, then B's G*N, then C's G*N): the
+    hand-worked two-token example with P = 2, N = 3 (its B and C differ, so a swap of the two slices, or x read
+    from the wrong channels, changes y) laid out as raw rows [x(2), B(3), C(3)] and passed through a width-1
+    identity convolution must give the example's hand-derived y and final state."""
+    g = json.load(open(os.path.join(GOLDEN, "two_token_p2n3.json")))
+    x, B, C = np.array(g["x"]), np.array(g["B"]), np.array(g["C"])
+    xbc = np.concatenate([x, B, C], axis=1)[None]  # [1, 2, 8]
+    ident = np.ones((8, 1))
+    y, f, st = oracle.ssd_conv_reference(xbc, ident, None, np.array(g["dt_raw"])[None, :, None],
+                                         np.array([g["dt_bias"]]), np.array([g["A"]]), nheads=1, headdim=2,
+                                         ngroups=1, dstate=3, D=np.array([g["D"]]),
+                                         init_states=np.array(g["init"])[None, None], activation="none")
+    close(y[0, :, 0], np.array(g["y"]), 1e-12)
+    close(f[0, 0], np.array(g["final"]), 1e-12)
+    assert st.shape == (1, 8, 0)
+
+
+def test_conv_ssd_oracle_channel_split_heads_and_groups():
+    """Three heads in three groups: the convolved rows sliced here channel by channel (x of head h, element p at
+    channel h*P + p; B of group g, element n at H*P + g*N + n; C at H*P + G*N + g*N + n) and run through the plain
+    oracle equal the conv oracle's own split."""
+    rng = np.random.default_rng(5)
+    b, L, H, P, G, N, k = 2, 9, 3, 2, 3, 4, 3
+    Dc = H * P + 2 * G * N
+    xbc = rng.standard_normal((b, L, Dc))
+    w = rng.standard_normal((Dc, k))
+    bias = rng.standard_normal(Dc)
+    cache = rng.standard_normal((b, Dc, k - 1))
+    dt_raw = rng.standard_normal((b, L, H))
+    dt_bias, A, Dh = rng.standard_normal(H), -np.exp(rng.uniform(0, 2, H)), rng.standard_normal(H)
+    init = rng.standard_normal((b, H, P, N)) * 0.3
+    y, f, _ = oracle.ssd_conv_reference(xbc, w, bias, dt_raw, dt_bias, A, nheads=H, headdim=P, ngroups=G, dstate=N,
+                                        D=Dh, init_states=init, conv_state=cache, activation="silu")
+    out, _ = oracle.conv1d_reference(xbc, w, bias, cache, "silu")
+    xs = np.empty((b, L, H, P))
+    Bs = np.empty((b, L, G, N))
+    Cs = np.empty((b, L, G, N))
+    for h in range(H):
+        for p in range(P):
+            xs[:, :, h, p] = out[:, :, h * P + p]
+    for gg in range(G):
+        for n in range(N):
+            Bs[:, :, gg, n] = out[:, :, H * P + gg * N + n]
+            Cs[:, :, gg, n] = out[:, :, H * P + G * N + gg * N + n]
+    yr, fr = oracle.ssd_reference(xs, dt_raw, dt_bias, A, Bs, Cs, Dh, init)
+    close(y, yr, 1e-13)
+    close(f, fr, 1e-13)

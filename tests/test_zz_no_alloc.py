@@ -9,13 +9,11 @@ problem size).
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import mamba_ssd_prefill_gb300 as m
 from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs
-from parity import gate_final, gate_y
 
 pytestmark = pytest.mark.gpu
 
@@ -46,18 +44,20 @@ def _call_static(w, inp):
 
 
 def test_static_scratch_matches_workspace_entry_point_twice():
-    cases = [WORKLOADS["m130-bf16"].with_(batch=2, seqlen=1000, nheads=8, seed=71),
-             WORKLOADS["m130-bf16"].with_(batch=4, seqlen=2048, nheads=24, state="f16", seed=72)]
-    for w in cases:  # two calls in a row, the second with a larger scratch footprint
+    """Both entry points run the same deterministic kernel on the same inputs, so y and the final states must be
+    bit for bit equal. The calls come in a row on the shared array: a small fp32-state problem, a larger fp16-state
+    one, the same fp16-state problem again (its ring words would carry the tags of the call before if the array were
+    not cleared), then the small one after the larger (stale contents past its own footprint)."""
+    small = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=1000, nheads=8, seed=71)
+    large = WORKLOADS["m130-bf16"].with_(batch=4, seqlen=2048, nheads=24, state="f16", seed=72)
+    for w in (small, large, large, small):
         inp = make_inputs(w, device="cuda")
         y_s, f_s = _call_static(w, inp)
         ws = m.Workspace("cuda")
         y_w, f_w = m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], workspace=ws)
         m.check(ws)
-        ok, s = gate_y(y_s.double().cpu().numpy(), y_w.double().cpu().numpy(), w.io)
-        assert ok, s
-        okf, sf = gate_final(f_s.double().cpu().numpy(), f_w.double().cpu().numpy(), w.io, w.state)
-        assert okf, sf
+        assert torch.equal(y_s, y_w), w
+        assert torch.equal(f_s, f_w), w
 
 
 def test_static_scratch_rejects_problems_over_the_limit():
