@@ -92,8 +92,8 @@ typedef struct {
  * workspace must be zero-filled once before its first use; after that each
  * call leaves it ready for the next one (launches on one stream may reuse it
  * back to back; concurrent launches need separate workspaces). State-passing
- * tags carry the workspace's launch count modulo 2^30 (fp16 states) or 2^32:
- * zero-fill a workspace again before its 2^30-th launch. */
+ * tags carry the workspace's launch count modulo 2^22 (fp16 states) or 2^32:
+ * zero-fill a workspace again before its 2^22-th launch. */
 SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *bytes);
 
 /* Launch the fused SSD prefill forward on `stream` (a cudaStream_t, NULL for

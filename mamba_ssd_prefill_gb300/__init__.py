@@ -111,14 +111,22 @@ def kernel_for(prob: SsdProblem) -> str:
 class Workspace:
     """A zero-initialised device workspace, grown on demand and reused across calls on one stream."""
 
+    # the state-passing tags carry the launch count modulo 2^22: the buffer is zero-filled again well before that
+    REZERO_EVERY = 1 << 21
+
     def __init__(self, device=None):
         self.device = torch.device(device or "cuda")
         self.buf = None
+        self.calls = 0
 
     def get(self, nbytes: int) -> torch.Tensor:
         if self.buf is None or self.buf.numel() < nbytes:
             # the library asks for a zero-filled workspace on first use only
             self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self.calls = 0
+        self.calls += 1
+        if self.calls % self.REZERO_EVERY == 0:
+            self.buf.zero_()  # on the current stream, ordered before the call that uses it
         return self.buf
 
 

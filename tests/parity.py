@@ -10,7 +10,16 @@ Tolerances (the bars the GPU path is held to):
   fp16 states:    the state is stored in 16 bits wherever it is passed (every chunk), so the
                   fp32 gate applies only when both the I/O and the states are fp32. fp32 I/O
                   with fp16 states takes the 16-bit rule with r = 2^-10 (the passed state's
-                  rounding); 16-bit I/O keeps r = r(I/O) whatever the state dtype.
+                  rounding).
+  tensor-core path (16-bit I/O): its contractions take fp16 operands (P, X_s, S_in rounded
+                  to 11 significant bits, the fused kernel's relaxed intermediates of the
+                  kernel-fusion page's precision section), so one dominant product of y carries
+                  up to two operand roundings, 2 * 2^-11 = 2^-10 of |y|, on top of the output's
+                  own rounding: r = r(I/O) + 2^-10 whatever the state dtype. The plain rule
+                  (r = r(I/O)) leaves only the fixed 1e-2 for that error where |y| sits just above
+                  a power of two (a bf16 y of 130 rounds by up to 0.5 = 2^-8 * 128), which a
+                  single fp16-rounded product of |y| > ~20 can exceed; the fraction of elements
+                  that also meet the plain rule is reported beside the gate ("plain_ok").
 Tensor-core operand envelope (gate_y_tc_envelope), used only for inputs far outside the pages'
 workload distributions (|y| in the hundreds, states >> 10): the tensor-core path rounds P, X_s
 and S_in to fp16 before its contractions, so on top of the bf16 output rounding its error grows
@@ -41,8 +50,12 @@ def stats(got, ref):
     }
 
 
-def gate_y(got, ref, io: str, state: str = "f32"):
-    """Return (ok, stats) for the output y (state: the dtype the states are passed in)."""
+TC_OPERAND = 2.0 ** -10  # two fp16 operand roundings of a dominant product (tensor-core path)
+
+
+def gate_y(got, ref, io: str, state: str = "f32", tc: bool = False):
+    """Return (ok, stats) for the output y (state: the dtype the states are passed in; tc: computed by the
+    tensor-core path, whose contractions take fp16 operands)."""
     s = stats(got, ref)
     if got.size == 0:
         return True, s
@@ -50,8 +63,12 @@ def gate_y(got, ref, io: str, state: str = "f32"):
         ok = s["max_abs"] <= 1e-3 * s["rms_ref"]
     else:
         r = REL[state] if io == "f32" else REL[io]
-        bound = 1e-2 + r * np.abs(ref)
-        excess = np.abs(got - ref) - bound
+        err = np.abs(got - ref)
+        plain = 1e-2 + r * np.abs(ref)
+        s["plain_ok"] = float(np.mean(err <= plain))
+        s["plain_worst_margin"] = float((err - plain).max())
+        bound = plain + (TC_OPERAND * np.abs(ref) if tc and io != "f32" else 0.0)
+        excess = err - bound
         s["worst_margin"] = float(excess.max())
         ok = bool(np.all(excess <= 0))
     return ok, s
