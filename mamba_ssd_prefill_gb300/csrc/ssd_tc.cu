@@ -12,22 +12,25 @@
 //   s_c     = B_c^T (exp(cs_last - cs_j) dt_j x_j)   (decay applied to x, the
 //                                             inner dimension of the contraction)
 //   S_c+1   = exp(cs_last) S_c + s_c          (flag-ordered chain across CTAs)
-//   y       = y_intra + exp(cs_i) C_c S_c     (tcgen05 C.S, fused epilogue)
+//   y       = y_intra + exp(cs_i) C_c S_c     (tcgen05 C.S, fused epilogue; D x enters through P's diagonal)
 //
-// Warp roles (352 threads):
-//   warp 0      unit loader (tickets, dt_raw, B/C tiles by TMA), up to two units ahead
-//   warp 10     x-tile loader (one TMA per head)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warps 2-5   "math": X_s (and the x tile to fp16), decay mask P -> TMEM, epilogue
-//               y = y_intra + exp(cs) y_inter staged in shared memory, TMA-stored
-//   warps 6-9   "chain": state passing (wait flag, S_in, S_out, publish), S_in
-//               -> shared memory as the C.S operand, final states
+// Warp roles (512 threads, four warpgroups); every per-head phase has warps of
+// its own, so the phases of consecutive heads overlap:
+//   warp 0       unit loader: tickets, B/C tiles by TMA, their bf16 -> fp16 conversion one unit behind
+//   warp 1       TMEM allocator + single-thread tcgen05.mma issuer of C.B^T and of each head's P.x and chunk state
+//   warp 2       x loader: per head one TMA of the x tile into a 3-deep ring, and the head's chunk cumsum tables
+//   warp 3       single-thread tcgen05.mma issuer of each head's C.S
+//   warps 4-7    P: the decay-masked C.B^T of each head, fp16 into TMEM
+//   warps 8-11   X_s = w o x (and x to fp16) before the head's first MMAs; the epilogue after its C.S, staged
+//                in the head's x slot (x is no longer needed then) and sent by TMA stores
+//   warps 12-15  chain: state passing, S_in -> shared memory as the C.S operand, final states
 // All MMA operands are fp16 (bf16 inputs are converted on chip; the contractions
 // with P, X_s and S need fp16's 11-bit significand to hold 1e-2).
 //
-// TMEM (512 columns): CB [0,128), P / y_inter x2 [128,256), y_intra x2
-// [256,384), chunk state s x2 [384,512).
+// TMEM (512 columns): CB [0,128), P x2 [128,256), y_intra x2 [256,384), and x2 [384,512) the chunk state s,
+// which C.S overwrites with y_inter once the chain has read it.
 #include <cuda.h>
+#include <stddef.h>
 
 #include <type_traits>
 
@@ -44,53 +47,80 @@ constexpr int kQ = 128;
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kMaxHs = 8;
-constexpr int kThreads = 352;
-constexpr int kXWarp = 10;  // x-tile loader warp
+constexpr int kThreads = 512;
 constexpr uint32_t kTile = 16384;  // [128 rows x 128 B] 128B-swizzled 16-bit tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColCB = 0, kColP = 128, kColYI = 256, kColS = 384;
-constexpr uint32_t kBarMath = 1;  // named barrier of the math warpgroup (0 is __syncthreads)
+constexpr uint32_t kBarE = 1;  // named barrier of the X_s / epilogue warpgroup (0 is __syncthreads)
 
 struct Sched {
     int32_t valid, s, c, g, h0, rows, row0, last;  // row0: the chunk's first token on the packed token axis
 };
 
+// Per head, beside its x tile: the chunk cumsum tables and what the consumers need to know about the head.
+// 16-byte aligned: the tables are written and read as float4 vectors in every slot.
+struct __align__(16) HeadTab {
+    float cs2[kQ];  // log2(e) * chunk-local inclusive cumsum of dt*A
+    float wt[kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
+    float dt[kQ];   // dt (0 past the sequence end)
+    int32_t valid;  // 0: no more work (end marker)
+    int32_t h, hh, v, c, s, row0, rows, last;
+    float dskip;  // D of the head (0 when absent)
+};
+
+template <bool CONV>
+struct __align__(128) ConvStage {  // fused convolution: per x slot the 3 raw rows before the chunk (a TMA
+                                   // destination: 128-byte aligned), the head's taps and bias
+    uint8_t halo[3][384];
+    float4 tap[3][kP];
+    float bias[3][kP];
+};
+template <>
+struct ConvStage<false> {};
+
+template <bool CONV>
 struct __align__(1024) Smem {
-    uint8_t bc[2][4][kTile];   // per unit stage: B n[0,64), B n[64,128), C n[0,64), C n[64,128)
-    uint8_t x[2][kTile];       // per head buffer: x tile (fp16 after conversion)
-    uint8_t xs[2][kTile];      // per head buffer: X_s, then S_in (fp16, C.S operand)
-    uint8_t xhalo[2][384];     // fused convolution: the 3 raw x rows before the chunk, dense [3][64] 16-bit
-    float4 xtap[2][kP];        // fused convolution: the head's taps per x channel (tap 3 on the current token)
-    float xbias[2][kP];        //                    and its bias
-    float cs2[2][kMaxHs][kQ];  // raw dt_raw from the producer, then log2(e) * cumsum(dt*A)
-    float dt[2][kMaxHs][kQ];   // dt
-    float wt[2][kMaxHs][kQ];   // exp(cs_anchor(j) - cs_j) dt_j, anchor(j) = last row of j's 32-row block
-    float dskip[2][kMaxHs];    // D of the unit's heads (0 when absent)
+    uint8_t bc[2][4][kTile];  // per unit stage: B n[0,64), B n[64,128), C n[0,64), C n[64,128)
+    uint8_t x[3][kTile];      // per head slot: x tile (fp16 after conversion), then S_in (fp16, C.S operand),
+                              // then the head's staged y
+    uint8_t xs[2][kTile];     // per head buffer: X_s
+    HeadTab tab[3];           // tables of the head in the x slot of the same index
+    ConvStage<CONV> cv;
     Sched sched[2];
     uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty, unit_go;
-    uint64_t x_full[2], x_empty[2], p_full[2], mma1[2], s_free[2], sin_full[2], mma2[2], drain;
+    uint64_t x_full[3], x_empty[3], xs_full[2], p_full[2], mma1[2], acc_free[2], sin_full[2], mma2[2], drain[2];
     uint32_t tmem_base;
     int32_t abort;
 };
 
-// Opt-in timeline trace (build with -DSSD_TRACE): CTA 0 records (%globaltimer, tag) per role.
+static_assert(sizeof(HeadTab) % 16 == 0, "every table slot starts on a 16-byte boundary");
+static_assert(offsetof(Smem<false>, x) % 1024 == 0 && offsetof(Smem<false>, xs) % 1024 == 0 &&
+                  offsetof(Smem<true>, x) % 1024 == 0 && offsetof(Smem<true>, xs) % 1024 == 0,
+              "128B-swizzled tiles start on 1024-byte boundaries");
+static_assert(offsetof(Smem<false>, tab) % 16 == 0 && offsetof(Smem<true>, tab) % 16 == 0,
+              "vector-accessed tables start on 16-byte boundaries");
+static_assert(offsetof(Smem<true>, cv) % 128 == 0 && offsetof(ConvStage<true>, halo) % 128 == 0 &&
+                  sizeof(ConvStage<true>::halo[0]) % 128 == 0 && offsetof(ConvStage<true>, tap) % 16 == 0 &&
+                  offsetof(ConvStage<true>, bias) % 16 == 0,
+              "TMA destinations start on 128-byte boundaries, vector-accessed arrays on 16-byte ones");
+static_assert(sizeof(Smem<true>) + 1024 <= 227 * 1024, "shared memory of one CTA");
+
+// Opt-in timeline trace (build with -DSSD_TRACE): in CTA 0 lane 0 of every warp records (SM clock, tag).
 #ifdef SSD_TRACE
-constexpr int kTraceN = 8192;
-__device__ unsigned long long g_trace[4][kTraceN][2];
-__device__ unsigned int g_trace_n[4];
-// one tracing thread per role keeps its own counter (no atomics: recording must not perturb the timeline)
-#define TRACE(role, tag)                                                                   \
-    do {                                                                                   \
-        if (blockIdx.x == 0 && trace_i < kTraceN) {                                        \
-            g_trace[role][trace_i][0] = globaltimer();                                     \
-            g_trace[role][trace_i][1] = (unsigned long long)(tag);                         \
-            ++trace_i;                                                                     \
-            g_trace_n[role] = trace_i;                                                     \
-        }                                                                                  \
+constexpr int kTraceRoles = 16, kTraceN = 4096;  // one record stream per warp (lane 0)
+__device__ unsigned long long g_trace[kTraceRoles][kTraceN][2];
+__device__ unsigned int g_trace_n[kTraceRoles];
+#define TRACE(role, ev, head)                                                                          \
+    do {                                                                                               \
+        if (blockIdx.x == 0 && trace_i < kTraceN) {                                                    \
+            g_trace[role][trace_i][0] = clock64();  /* SM cycles: every record comes from one SM */     \
+            g_trace[role][trace_i][1] = ((unsigned long long)(ev) << 32) | (unsigned)(head);           \
+            g_trace_n[role] = ++trace_i;                                                               \
+        }                                                                                              \
     } while (0)
 #else
-#define TRACE(role, tag) \
-    do {                 \
+#define TRACE(role, ev, head) \
+    do {                      \
     } while (0)
 #endif
 
@@ -102,6 +132,27 @@ __device__ __forceinline__ float ex2(float v) {
 
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Packed fp32 pairs (one instruction for both lanes of the pair; each lane rounded as a scalar fmul / fmaf).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
 }
 
 // Plain C++ shared-memory vector accesses, so the compiler can batch and overlap them; their
@@ -128,6 +179,9 @@ template <> __device__ __forceinline__ float2 unpack_io<__nv_bfloat16>(uint32_t 
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&v));
 }
 __device__ __forceinline__ float2 unpack_f16(uint32_t v) { return __half22float2(*reinterpret_cast<__half2 *>(&v)); }
+__device__ __forceinline__ float2 f2(uint32_t lo, uint32_t hi) {
+    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
 
 // ---------------------------------------------------------------- fused depthwise convolution (width 4)
 // SiLU with one special-function op: v sigmoid(v) = h + h tanh(h) with h = v / 2, tanh by tanh.approx.f32 (the
@@ -236,7 +290,7 @@ __device__ __noinline__ bool wait_ring(const ulonglong2 *p, uint32_t want, uint3
 // Bounded wait until *tag == want (acquire). On timeout records SSD_ERR_TIMEOUT and returns false;
 // returns false at once when another CTA aborted the launch. Out of line: it is the slow path.
 __device__ __noinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32_t epoch, WsHeader *hdr,
-                                         uint64_t limit_ns, uint32_t chunk) {
+                                      uint64_t limit_ns, uint32_t chunk) {
     const uint64_t t0 = globaltimer();
     uint32_t sleep_ns = 20;
     for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
@@ -252,8 +306,8 @@ __device__ __noinline__ bool wait_tag(const uint64_t *tag, uint64_t want, uint32
     return false;
 }
 
-__device__ __noinline__ void pipe_timeout(Smem &sm, WsHeader *hdr, uint32_t epoch) {
-    *reinterpret_cast<volatile int32_t *>(&sm.abort) = 1;
+__device__ __noinline__ void pipe_timeout(int32_t *abort_flag, WsHeader *hdr, uint32_t epoch) {
+    *reinterpret_cast<volatile int32_t *>(abort_flag) = 1;
     report_error(hdr, epoch, DEV_PIPE, 0, 0, WAIT_PIPE);
 }
 
@@ -264,21 +318,58 @@ __device__ __noinline__ void pipe_timeout(Smem &sm, WsHeader *hdr, uint32_t epoc
 // legitimately sit behind one full state-passing wait, which must time out
 // (and report itself) first. Only the first probe is inline: the polling loop
 // is one out-of-line copy, so the hot code of every role stays small.
-__device__ __noinline__ bool bwait_slow(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
+__device__ __noinline__ bool bwait_slow(uint64_t *bar, uint32_t parity, int32_t *abort_flag, WsHeader *hdr,
+                                        uint32_t epoch) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0; it < kMaxSpinIters; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 15u) {
-            if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) return false;
+            if (*reinterpret_cast<volatile int32_t *>(abort_flag)) return false;
             const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
             if (globaltimer() - t0 > limit) break;
         }
     }
-    pipe_timeout(sm, hdr, epoch);
+    pipe_timeout(abort_flag, hdr, epoch);
     return false;
 }
-__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, Smem &sm, WsHeader *hdr, uint32_t epoch) {
-    return mbar_try_wait(bar, parity) || bwait_slow(bar, parity, sm, hdr, epoch);
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, int32_t *abort_flag, WsHeader *hdr,
+                                      uint32_t epoch) {
+    return mbar_try_wait(bar, parity) || bwait_slow(bar, parity, abort_flag, hdr, epoch);
+}
+
+// 16 final-state values of one d_state row (columns p .. p + 15, kN apart from index `base`), in the state dtype.
+// Out of line: it runs at a sequence's last chunk only, so it is kept out of the chain's hot code.
+template <typename ST>
+__device__ __noinline__ void store_final16(ST *fin, int64_t base, int64_t n, WsHeader *hdr, float4 a, float4 b,
+                                           float4 c, float4 d) {
+    (void)n;
+    (void)hdr;
+    const float o[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) *chk(fin, base + (int64_t)e * kN, 1, n, hdr, SITE_TC_FINAL) = from_f32<ST>(o[e]);
+}
+
+// softplus out of line: the per-head table code stays small in the instruction cache.
+__device__ __noinline__ float softplus_ool(float v) { return softplus_f32(v); }
+
+// The diagonal 32-column block of P with exp taken per element (decay ranges too wide for the rank-1 split): CB
+// from TMEM, exp(cs_i - cs_j) dt_j, D on the diagonal, the causal mask (a NaN or inf past the diagonal included),
+// fp16 into TMEM. Out of line: it is the rare path, kept away from the hot code. Warp-collective.
+__device__ __noinline__ void p_block_exact(uint32_t cb_col, uint32_t p_col, const float *cs2, const float *dt,
+                                           float cs2i, float dskip) {
+    const int lane = threadIdx.x & 31;
+    uint32_t cb[32];
+    tmem_ld16(cb_col, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
+    tmem_ld16(cb_col + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        pk[e] = pack_f16(__uint_as_float(cb[2 * e]) * ex2(cs2i - cs2[2 * e]) * dt[2 * e] + (2 * e == lane ? dskip : 0.f),
+                         __uint_as_float(cb[2 * e + 1]) * ex2(cs2i - cs2[2 * e + 1]) * dt[2 * e + 1] +
+                             (2 * e + 1 == lane ? dskip : 0.f)) &
+                ((2 * e <= lane ? 0x0000ffffu : 0u) | (2 * e + 1 <= lane ? 0xffff0000u : 0u));
+    tmem_st16(p_col, pk);
 }
 
 template <typename IO, typename ST, bool CONV>
@@ -290,13 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned base (128B-swizzle atoms). Computed as smem_raw + pad, not through an integer
     // round trip, so the compiler keeps the shared address space and emits LDS/STS for every access.
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-    Smem &sm = *reinterpret_cast<Smem *>(smem_raw + pad);
+    Smem<CONV> &sm = *reinterpret_cast<Smem<CONV> *>(smem_raw + pad);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     WsHeader *hdr = p.hdr;
     const uint32_t epoch = ld_relaxed_gpu(&hdr->epoch) + 1u;
     constexpr bool kBf16 = sizeof(IO) == 2 && !std::is_same<IO, __half>::value;
-    unsigned int trace_i = 0;  // per-thread trace record counter (SSD_TRACE builds)
+    int32_t *abort_flag = &sm.abort;
+    unsigned int trace_i = 0;  // per-thread trace record counter (trace builds)
     (void)trace_i;
+#define BWAIT(bar, par) bwait((bar), (par), abort_flag, hdr, epoch)
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -304,18 +397,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.bc_full[i], 1);
             mbar_init(&sm.bc_conv[i], 1);
             mbar_init(&sm.bc_empty[i], 1);
-            mbar_init(&sm.x_full[i], 1);
-            mbar_init(&sm.x_empty[i], 1);
-            mbar_init(&sm.p_full[i], 1);
+            mbar_init(&sm.xs_full[i], 128);   // every X_s / epilogue thread arrives
+            mbar_init(&sm.p_full[i], 128);    // every P thread arrives
             mbar_init(&sm.mma1[i], 1);
-            mbar_init(&sm.s_free[i], 128);   // every chain thread arrives
-            mbar_init(&sm.sin_full[i], 128);
+            mbar_init(&sm.acc_free[i], 128);  // every X_s / epilogue thread arrives
+            mbar_init(&sm.sin_full[i], 128);  // every chain thread arrives
             mbar_init(&sm.mma2[i], 1);
         }
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(&sm.x_full[i], 2);   // the TMA's arrive (with its bytes) and the tables' arrive
+            mbar_init(&sm.x_empty[i], 4);  // one lane per epilogue warp, after its y store has read the slot
+        }
         mbar_init(&sm.cb_full, 1);
-        mbar_init(&sm.unit_go, 1);
-        mbar_init(&sm.cb_empty, 1);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.cb_empty, 128);
+        mbar_init(&sm.unit_go, 128);
+        mbar_init(&sm.drain[0], 1);
+        mbar_init(&sm.drain[1], 1);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -331,17 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ unit loader
-        // Per unit: ticket, dt_raw rows, B/C tiles by TMA; and, for the unit requested one iteration earlier
-        // (so its TMA latency is already behind it), the bf16 -> fp16 conversion of B/C in place (same 16-bit
-        // positions, same swizzle) and the chunk cumsum tables of its heads. Tickets are fetched one unit ahead,
-        // or, when the state chain bounds the launch (few units per chunk index), only once the unit before is
-        // three heads from its end: a ticket taken early sits on a CTA that is busy for a whole unit more, and
-        // the chain reaching that chunk waits for it; late tickets follow the order in which CTAs free up.
+        // Per unit: ticket, B/C tiles by TMA; and, for the unit requested one iteration earlier (so its TMA latency
+        // is already behind it), the bf16 -> fp16 conversion of B/C in place (same 16-bit positions, same swizzle),
+        // or with the fused convolution the B/C columns convolved in place. Tickets are fetched one unit ahead, or,
+        // when the state chain bounds the launch (few units per chunk index), only once the unit before is three
+        // heads from its end: a ticket taken early sits on a CTA that is busy for a whole unit more, and the chain
+        // reaching that chunk waits for it; late tickets follow the order in which CTAs free up.
         if (lane == 0) {
             prefetch_tensormap(&map_b);
             prefetch_tensormap(&map_c);
         }
-        const IO *dtr = static_cast<const IO *>(p.dt_raw);
         int armed_bc = 0;  // for the drain at teardown
         uint32_t bc_par[2] = {0, 0};
         uint32_t t = 0;
@@ -350,17 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         Sched prev{0, 0, 0, 0, 0, 0, 0, 0};
         const uint32_t total = total_units(p, (uint32_t)(p.G * slices));
         const bool late = p.tc_late_ticket != 0;
-        const int64_t ndt = p.batch * p.L * p.H;  // dt_raw extent (bounds-checked builds)
-#ifdef SSD_BOUNDS_CHECK
-        const int64_t probe = hdr->bounds_probe ? ndt : 0;  // test hook: plant the dt rows one extent further
-#else
-        const int64_t probe = 0;
-#endif
-        bool ok = true;
-        // conversion + tables of the unit in stage uu (whose tiles were requested earlier)
         auto finish = [&](uint32_t vv, const Sched &sc) -> bool {
             const uint32_t uu = vv & 1;
-            if (!bwait(&sm.bc_full[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
+            if (!BWAIT(&sm.bc_full[uu], (vv >> 1) & 1)) return false;
             if constexpr (CONV) {  // B, C: the raw tiles convolved in place (fp16 out), halo from the rows or the cache
                 const int64_t tok0 = sc.row0 - (int64_t)sc.c * kQ;
 #pragma unroll 1
@@ -394,49 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // chunk cumsum: dt = softplus(dt_raw + dt_bias) (0 past the sequence end), inclusive scan of
-            // dt*A over the 128 rows; this lane owns rows 4*lane .. 4*lane+3
-#pragma unroll 1
-            for (int hh = 0; hh < kMaxHs; ++hh) {
-                if (hh < hs) {
-                    const int h = sc.h0 + hh;
-                    const float bias = p.dt_bias[h], Ah = p.A[h];
-                    float dtv[4], cum[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int row = 4 * lane + jj;
-                        dtv[jj] = row < sc.rows ? softplus_f32(sm.cs2[uu][hh][row] + bias) : 0.f;
-                        cum[jj] = dtv[jj] * Ah + (jj ? cum[jj - 1] : 0.f);
-                    }
-                    float incl = cum[3];
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float w = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += w;
-                    }
-                    const float excl = incl - cum[3];
-                    float cs2v[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) cs2v[jj] = (excl + cum[jj]) * kLog2e;
-                    // anchor of these rows' 32-row block: its last row, owned by lane (lane | 7), jj = 3
-                    const float anchor = __shfl_sync(0xffffffffu, cs2v[3], lane | 7);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int row = 4 * lane + jj;
-                        sm.cs2[uu][hh][row] = cs2v[jj];
-                        sm.dt[uu][hh][row] = dtv[jj];
-                        sm.wt[uu][hh][row] = ex2(anchor - cs2v[jj]) * dtv[jj];
-                    }
-                    if (lane == 0) sm.dskip[uu][hh] = p.D ? p.D[h] : 0.f;
-                }
-            }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.bc_conv[uu]);
-            TRACE(0, (2u << 24) | vv);
+            if (lane == 0) {
+                mbar_arrive(&sm.bc_conv[uu]);
+                TRACE(warp, 2, vv);
+            }
             return true;
         };
-        for (uint32_t v = 0; ok; ++v) {
+        for (uint32_t v = 0;; ++v) {
             const uint32_t u = v & 1, nn = v >> 1;
             uint32_t t_next = 0;
             if (!late && lane == 0 && t < total) t_next = atomicAdd(&hdr->ticket, 1u);  // in flight meanwhile
@@ -444,12 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // has seen unit v-1 converted
             if (v > 0 && !finish(v - 1, prev)) break;
             if (late && v > 0) {  // the ticket only now that the unit before it is three heads from its end
-                if (!bwait(&sm.unit_go, (v - 1) & 1, sm, hdr, epoch)) break;
+                if (!BWAIT(&sm.unit_go, (v - 1) & 1)) break;
                 if (lane == 0) t = atomicAdd(&hdr->ticket, 1u);
                 t = __shfl_sync(0xffffffffu, t, 0);
             }
+            if (!BWAIT(&sm.bc_empty[u], (nn & 1) ^ 1)) break;
             if (t >= total) {
-                if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
                 if (lane == 0) {
                     sm.sched[u].valid = 0;
                     mbar_arrive(&sm.sched_full[u]);
@@ -457,8 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 break;
             }
-            if (!bwait(&sm.bc_empty[u], (nn & 1) ^ 1, sm, hdr, epoch)) break;
-            TRACE(0, (1u << 24) | v);
             const SeqChunk sq = seq_chunk(p, t / (p.G * slices));
             const int64_t r = t % (p.G * slices);
             const int64_t c = sq.c;
@@ -467,25 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t row0 = sq.tok0 + c * kQ;
             const int rows = (int)((sq.len - c * kQ) < kQ ? (sq.len - c * kQ) : kQ);
             const int last = c == (sq.len + kQ - 1) / kQ - 1;
-            // dt_raw rows 4*lane .. 4*lane+3 of the unit's heads, every load in flight at once
-            float raw[4][kMaxHs];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int i = 4 * lane + jj;
-#pragma unroll
-                for (int hh = 0; hh < kMaxHs; ++hh) {
-                    raw[jj][hh] = 0.f;
-                    if (hh < hs && i < rows)
-                        raw[jj][hh] = to_f32(*chk(dtr, (row0 + i) * p.H + h0 + hh + probe, 1, ndt, hdr, SITE_TC_DT));
-                }
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                for (int hh = 0; hh < kMaxHs; ++hh)
-                    if (hh < hs) sm.cs2[u][hh][4 * lane + jj] = raw[jj][hh];
             const Sched cur{1, (int32_t)sq.s, (int32_t)c, (int32_t)g, (int32_t)h0, rows, (int32_t)row0, last};
-            __syncwarp();
             if (lane == 0) {
                 sm.sched[u] = cur;
                 mbar_arrive(&sm.sched_full[u]);
@@ -496,7 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d(sm.bc[u][3], &map_c, &sm.bc_full[u], 64, (int)g, (int)row0, 0);
                 armed_bc |= 1 << u;
                 bc_par[u] = nn & 1;
+                TRACE(warp, 1, v);
             }
+            __syncwarp();
             prev = cur;
             if (!late) t = __shfl_sync(0xffffffffu, t_next, 0);
         }
@@ -510,61 +546,141 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
         }
         __syncwarp();
-    } else if (warp == kXWarp) {
+    } else if (warp == 2) {
         // ------------------------------------------------------------ x loader
-        // One TMA per head into the 2-deep x ring (lane 0). With the fused convolution it also brings the 3 raw rows
-        // before the chunk: by TMA inside the sequence, else written by the lanes from the conv cache (or zeros).
+        // Per head: the x tile by one TMA into the 3-deep ring (and, with the fused convolution, the 3 raw rows
+        // before the chunk and the head's taps), then the head's chunk cumsum: dt = softplus(dt_raw + dt_bias)
+        // (0 past the sequence end), inclusive scan of dt*A over the 128 rows, into the slot's tables. The end of
+        // the work goes to the consumers as a table with valid = 0.
         if (lane == 0) {
             prefetch_tensormap(&map_x);
             if (CONV) prefetch_tensormap(&map_xh);
         }
+        const IO *dtr = static_cast<const IO *>(p.dt_raw);
+        const int64_t ndt = p.batch * p.L * p.H;  // dt_raw extent (bounds-checked builds)
+#ifdef SSD_BOUNDS_CHECK
+        const int64_t probe = hdr->bounds_probe ? ndt : 0;  // test hook: plant the dt rows one extent further
+#else
+        const int64_t probe = 0;
+#endif
         uint32_t hc = 0;
         int armed_x = 0;
-        uint32_t x_par[2] = {0, 0};
-        for (uint32_t v = 0;; ++v) {
+        uint32_t x_par[3] = {0, 0, 0};
+        bool done = false;
+        for (uint32_t v = 0; !done; ++v) {
             const uint32_t u = v & 1;
-            if (!bwait(&sm.sched_full[u], (v >> 1) & 1, sm, hdr, epoch)) break;
+            if (!BWAIT(&sm.sched_full[u], (v >> 1) & 1)) break;
             const Sched sc = sm.sched[u];
-            if (!sc.valid) break;
-            bool ok = true;
-            for (int hh = 0; hh < hs; ++hh, ++hc) {
-                const uint32_t k = hc & 1, n = hc >> 1;
-                if (!bwait(&sm.x_empty[k], (n & 1) ^ 1, sm, hdr, epoch)) {
-                    ok = false;
+            const int nh = sc.valid ? hs : 1;
+            // dt_raw rows 4*lane .. 4*lane+3 of every head of the unit, all loads in flight at once (one memory
+            // latency per unit rather than per head)
+            float raw[4][kMaxHs];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int i = 4 * lane + jj;
+#pragma unroll
+                for (int hh = 0; hh < kMaxHs; ++hh)
+                    raw[jj][hh] = sc.valid && hh < hs && i < sc.rows
+                                      ? to_f32(*chk(dtr, (sc.row0 + i) * p.H + sc.h0 + hh + probe, 1, ndt, hdr, SITE_TC_DT))
+                                      : 0.f;
+            }
+            for (int hh = 0; hh < nh; ++hh, ++hc) {
+                const uint32_t k = hc % 3, n = hc / 3;
+                if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
+                    done = true;
                     break;
                 }
+                HeadTab &tb = sm.tab[k];
+                if (!sc.valid) {
+                    if (lane == 0) {
+                        tb.valid = 0;
+                        mbar_arrive(&sm.x_full[k]);
+                        mbar_arrive(&sm.x_full[k]);
+                    }
+                    done = true;
+                    break;
+                }
+                const int h = sc.h0 + hh;
                 const bool halo_tma = CONV && sc.c > 0;
-                if (CONV) {  // the head's taps and bias, read by the math warps as broadcasts
-                    const int64_t ch0 = (int64_t)(sc.h0 + hh) * kP;
-                    for (int e = lane; e < kP; e += 32) {
-                        sm.xtap[k][e] = *reinterpret_cast<const float4 *>(p.conv_w + (ch0 + e) * 4);
-                        sm.xbias[k][e] = p.conv_b ? p.conv_b[ch0 + e] : 0.f;
-                    }
-                }
-                if (CONV && sc.c == 0) {  // the sequence starts here: its conv cache (or zeros) before it
-                    const IO *st = static_cast<const IO *>(p.conv_state);
-                    IO *dst = reinterpret_cast<IO *>(sm.xhalo[k]);
-                    for (int e = lane; e < 3 * kP; e += 32) {
-                        const int r = e / kP, pc = e % kP;
-                        const int64_t ch = (int64_t)(sc.h0 + hh) * kP + pc;
-                        dst[r * kP + pc] = st ? *chk(st, ((int64_t)sc.s * p.x_ld + ch) * 3 + r, 1, p.nseq * p.x_ld * 3, hdr,
-                                                     SITE_CONV_STATE)
-                                              : from_f32<IO>(0.f);
-                    }
-                }
-                __syncwarp();
                 if (lane == 0) {
+                    TRACE(warp, 1, hc);
                     mbar_arrive_expect_tx(&sm.x_full[k], kTile + (halo_tma ? 3 * kP * 2 : 0));
-                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, sc.h0 + hh, sc.row0, 0);
-                    if (halo_tma) tma_load_4d(sm.xhalo[k], &map_xh, &sm.x_full[k], 0, sc.h0 + hh, sc.row0 - 3, 0);
+                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, h, sc.row0, 0);
+                    if constexpr (CONV) {
+                        if (halo_tma) tma_load_4d(sm.cv.halo[k], &map_xh, &sm.x_full[k], 0, h, sc.row0 - 3, 0);
+                    }
                     armed_x |= 1 << k;
                     x_par[k] = n & 1;
                 }
+                if constexpr (CONV) {  // the head's taps and bias (read as broadcasts), the cache before a sequence
+                    const int64_t ch0 = (int64_t)h * kP;
+                    for (int e = lane; e < kP; e += 32) {
+                        sm.cv.tap[k][e] = *reinterpret_cast<const float4 *>(p.conv_w + (ch0 + e) * 4);
+                        sm.cv.bias[k][e] = p.conv_b ? p.conv_b[ch0 + e] : 0.f;
+                    }
+                    if (sc.c == 0) {
+                        const IO *st = static_cast<const IO *>(p.conv_state);
+                        IO *dst = reinterpret_cast<IO *>(sm.cv.halo[k]);
+                        for (int e = lane; e < 3 * kP; e += 32) {
+                            const int r = e / kP, pc = e % kP;
+                            dst[r * kP + pc] = st ? *chk(st, ((int64_t)sc.s * p.x_ld + ch0 + pc) * 3 + r, 1,
+                                                         p.nseq * p.x_ld * 3, hdr, SITE_CONV_STATE)
+                                                  : from_f32<IO>(0.f);
+                        }
+                    }
+                }
+                float rh[4];  // this head's column of raw (a register select: hh is not a compile-time index)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    rh[jj] = raw[jj][0];
+#pragma unroll
+                    for (int e = 1; e < kMaxHs; ++e) rh[jj] = hh == e ? raw[jj][e] : rh[jj];
+                }
+                const float bias = p.dt_bias[h], Ah = p.A[h];
+                float dtv[4], cum[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    dtv[jj] = 4 * lane + jj < sc.rows ? softplus_ool(rh[jj] + bias) : 0.f;
+                    cum[jj] = dtv[jj] * Ah + (jj ? cum[jj - 1] : 0.f);
+                }
+                float incl = cum[3];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float w = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += w;
+                }
+                const float excl = incl - cum[3];
+                float cs2v[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) cs2v[jj] = (excl + cum[jj]) * kLog2e;
+                // anchor of these rows' 32-row block: its last row, owned by lane (lane | 7), jj = 3
+                const float anchor = __shfl_sync(0xffffffffu, cs2v[3], lane | 7);
+                reinterpret_cast<float4 *>(tb.cs2)[lane] = make_float4(cs2v[0], cs2v[1], cs2v[2], cs2v[3]);
+                reinterpret_cast<float4 *>(tb.dt)[lane] = make_float4(dtv[0], dtv[1], dtv[2], dtv[3]);
+                reinterpret_cast<float4 *>(tb.wt)[lane] =
+                    make_float4(ex2(anchor - cs2v[0]) * dtv[0], ex2(anchor - cs2v[1]) * dtv[1],
+                                ex2(anchor - cs2v[2]) * dtv[2], ex2(anchor - cs2v[3]) * dtv[3]);
+                if (lane == 0) {
+                    tb.valid = 1;
+                    tb.h = h;
+                    tb.hh = hh;
+                    tb.v = (int32_t)v;
+                    tb.c = sc.c;
+                    tb.s = sc.s;
+                    tb.row0 = sc.row0;
+                    tb.rows = sc.rows;
+                    tb.last = sc.last;
+                    tb.dskip = p.D ? p.D[h] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.x_full[k]);
+                    TRACE(warp, 2, hc);
+                }
             }
-            if (!ok) break;
         }
         if (lane == 0 && *reinterpret_cast<volatile int32_t *>(&sm.abort)) {
-            for (int k = 0; k < 2; ++k)
+            for (int k = 0; k < 3; ++k)
                 if (armed_x & (1 << k)) {
                     const uint64_t t0 = globaltimer();
                     while (!mbar_try_wait(&sm.x_full[k], x_par[k]) && globaltimer() - t0 < 100000000ull) {
@@ -573,367 +689,377 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Event driven: heads h are numbered across units (unit h / hs). For each head it issues
-        // MMA1 (P.x and the chunk state) once P is in TMEM, and C.S once the entering state is in
-        // shared memory, whichever is ready first, C.S preferred (the epilogue waits on it). CB of a
-        // unit goes out before the unit's first MMA1.
+        // ------------------------------------------------------------ MMA issuer: CB and MMA1
+        // Event driven: heads h are numbered across units (unit h / hs). For each head it issues MMA1 (P.x and
+        // the chunk state) once P, X_s and the head's accumulators are ready; CB of a unit goes out before the
+        // unit's first MMA1. The K loops are rolled (descriptors advance by a constant): this code runs a few
+        // times per microsecond between long idle stretches, so its footprint in the instruction cache matters.
         if (lane == 0) {
             constexpr uint32_t idCB = idesc_f16_f32(128, 128, false, false);
             constexpr uint32_t idPX = idesc_f16_f32(128, 64, false, true);
             constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true);
-            constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
             const uint32_t uhs = (uint32_t)hs;
-            uint32_t v_cb = 0;                // next unit whose CB is due
-            uint32_t h1 = 0, h2 = 0;          // next head for MMA1 / for C.S (h2 <= h1)
-            uint32_t end_heads = 0xffffffffu; // total heads, once the end-of-work unit is seen
-            uint64_t idle_since = globaltimer();
+            uint32_t v_cb = 0;  // next unit whose CB is due
+            uint32_t h1 = 0;    // next head for MMA1
+            uint64_t idle_since = 0;
+            uint32_t idle = 0;
             const uint64_t limit = 4 * (hdr->timeout_ns ? hdr->timeout_ns : kDefaultTimeoutNs) + 100000000ull;
-            for (uint32_t spin = 0;; ++spin) {
+            // Every barrier is polled without suspending (a thread suspended on one barrier does not wake for
+            // another); an idle round sleeps a few tens of ns, and the clock is read once per 256 idle rounds.
+            for (;;) {
                 bool progress = false;
-                // C.S of head h2: y_inter = C . S_in
-                if (h2 < h1 && mbar_try_wait_ns(&sm.sin_full[h2 & 1], (h2 >> 1) & 1, 64)) {
-                    const uint32_t k = h2 & 1, vu = h2 / uhs, u = vu & 1;
-                    tc_fence_after();
-                    const uint32_t ca = smem_u32(sm.bc[u][2]), sa = smem_u32(sm.xs[k]);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
-                        mma_ss(tmem + kColP + 64 * k, desc_sw128(ca + off, 16, 1024),
-                               desc_sw128(sa + 2048 * s, 8192, 1024), idCS, s > 0);
-                    }
-                    mma_commit(&sm.mma2[k]);
-                    if (h2 % uhs == uhs - 1) mma_commit(&sm.bc_empty[u]);  // last reader of the unit's B/C
-                    TRACE(1, (3u << 24) | h2);
-                    ++h2;
-                    progress = true;
-                }
-                if (end_heads != 0xffffffffu && h2 == end_heads) break;
-                // CB of unit v_cb, due when MMA1 has reached its first head
-                if (end_heads == 0xffffffffu && h1 == v_cb * uhs &&
-                    mbar_test_wait(&sm.bc_conv[v_cb & 1], (v_cb >> 1) & 1)) {
+                // CB of unit v_cb, due when MMA1 has reached its first head and the P warps are done with the last
+                if (h1 == v_cb * uhs && mbar_test_wait(&sm.bc_conv[v_cb & 1], (v_cb >> 1) & 1)) {
                     const uint32_t u = v_cb & 1;
-                    if (!*reinterpret_cast<volatile int32_t *>(&sm.sched[u].valid)) {
-                        end_heads = v_cb * uhs;
-                        progress = true;
-                    } else if (mbar_test_wait(&sm.cb_empty, (v_cb & 1) ^ 1)) {
+                    if (!*reinterpret_cast<volatile int32_t *>(&sm.sched[u].valid)) break;  // no more work
+                    if (mbar_test_wait(&sm.cb_empty, (v_cb & 1) ^ 1)) {
                         tc_fence_after();
-                        const uint32_t ba = smem_u32(sm.bc[u][0]), ca = smem_u32(sm.bc[u][2]);
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            const uint32_t off = (uint32_t)(s >> 2) * kTile + (uint32_t)(s & 3) * 32;
-                            mma_ss(tmem + kColCB, desc_sw128(ca + off, 16, 1024), desc_sw128(ba + off, 16, 1024),
-                                   idCB, s > 0);
+                        const uint64_t da = desc_sw128(smem_u32(sm.bc[u][2]), 16, 1024);
+                        const uint64_t db = desc_sw128(smem_u32(sm.bc[u][0]), 16, 1024);
+#pragma unroll 1
+                        for (uint32_t s = 0; s < 8; ++s) {  // K step s: 16-bit tile s / 4, 32-byte column s % 4
+                            const uint64_t off = (s >> 2) * (kTile >> 4) + (s & 3) * 2;
+                            mma_ss(tmem + kColCB, da + off, db + off, idCB, s > 0);
                         }
                         mma_commit(&sm.cb_full);
-                        TRACE(1, (1u << 24) | v_cb);
+                        TRACE(warp, 1, v_cb);
                         ++v_cb;
                         progress = true;
                     }
                 }
                 // MMA1 of head h1: y_intra = P . x and s = B^T . X_s
-                if (h1 < v_cb * uhs && mbar_try_wait_ns(&sm.p_full[h1 & 1], (h1 >> 1) & 1, 64) &&
-                    mbar_test_wait(&sm.s_free[h1 & 1], ((h1 >> 1) & 1) ^ 1)) {
-                    const uint32_t k = h1 & 1, u = (h1 / uhs) & 1;
-                    tc_fence_after();
-                    const uint32_t ba = smem_u32(sm.bc[u][0]);
-                    const uint32_t xa = smem_u32(sm.x[k]), xsa = smem_u32(sm.xs[k]);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma_ts(tmem + kColYI + 64 * k, tmem + kColP + 64 * k + 8 * s,
-                               desc_sw128(xa + 2048 * s, 8192, 1024), idPX, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s)
-                        mma_ss(tmem + kColS + 64 * k, desc_sw128(ba + 2048 * s, kTile, 1024),
-                               desc_sw128(xsa + 2048 * s, 8192, 1024), idST, s > 0);
-                    mma_commit(&sm.mma1[k]);
-                    mma_commit(&sm.x_empty[k]);
-                    TRACE(1, (2u << 24) | h1);
-                    ++h1;
-                    progress = true;
+                if (h1 < v_cb * uhs) {
+                    const uint32_t k = h1 & 1, n = h1 >> 1;
+                    if (mbar_test_wait(&sm.p_full[k], n & 1) && mbar_test_wait(&sm.xs_full[k], n & 1) &&
+                        mbar_test_wait(&sm.acc_free[k], (n & 1) ^ 1)) {
+                        const uint32_t u = (h1 / uhs) & 1;
+                        tc_fence_after();
+                        const uint64_t dx = desc_sw128(smem_u32(sm.x[h1 % 3]), 8192, 1024);
+                        const uint64_t dbt = desc_sw128(smem_u32(sm.bc[u][0]), kTile, 1024);
+                        const uint64_t dxs = desc_sw128(smem_u32(sm.xs[k]), 8192, 1024);
+#pragma unroll 1
+                        for (uint32_t s = 0; s < 8; ++s)  // K step s: 16 rows = 2048 bytes further
+                            mma_ts(tmem + kColYI + 64 * k, tmem + kColP + 64 * k + 8 * s, dx + 128 * s, idPX, s > 0);
+#pragma unroll 1
+                        for (uint32_t s = 0; s < 8; ++s)
+                            mma_ss(tmem + kColS + 64 * k, dbt + 128 * s, dxs + 128 * s, idST, s > 0);
+                        mma_commit(&sm.mma1[k]);
+                        TRACE(warp, 2, h1);
+                        ++h1;
+                        progress = true;
+                    }
                 }
                 if (progress) {
-                    idle_since = globaltimer();
-                } else if ((spin & 15u) == 15u) {
-                    if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) break;
-                    if (globaltimer() - idle_since > limit) {
-                        pipe_timeout(sm, hdr, epoch);
-                        break;
+                    idle = 0;
+                } else {
+                    if ((++idle & 255u) == 0) {
+                        if (*reinterpret_cast<volatile int32_t *>(&sm.abort)) break;
+                        const uint64_t now = globaltimer();
+                        if (idle == 256u) {
+                            idle_since = now;
+                        } else if (now - idle_since > limit) {
+                            pipe_timeout(abort_flag, hdr, epoch);
+                            break;
+                        }
                     }
+                    __nanosleep(32);
                 }
             }
             // drain: every MMA issued above has completed before TMEM is released
-            mma_commit(&sm.drain);
+            mma_commit(&sm.drain[0]);
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(&sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+            while (!mbar_try_wait(&sm.drain[0], 0) && globaltimer() - t0 < 1000000000ull) {
             }
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ math warpgroup
-        const int q = warp & 3;              // TMEM lane quarter of this warp
-        const int i = 32 * q + lane;         // tile row (token within the chunk) owned by this thread
-        const uint32_t lrow = (uint32_t)(32 * q) << 16;
-        const bool leader = warp == 2 && lane == 0;
-        if (lane == 0) prefetch_tensormap(&map_y);
-        uint32_t hc = 0;
-        bool pend = false;
-        uint32_t pk = 0, pn = 0;
-        float pecs = 0.f;
-        int ph = 0, prow = 0, pvr = 0;  // y of the pending head: head, first token of this warp's rows, valid rows
-        IO *yg = static_cast<IO *>(p.y);
-        bool ok = true;
-        // y = y_intra + exp(cs_i) y_inter of the pending head, staged in its C.S operand tile (free once C.S
-        // has completed) with the operand's 128B swizzle, then one TMA store per warp of its 32 rows; the
-        // store clips rows past the sequence end.
-        auto epilogue = [&]() -> bool {
-            if (!bwait(&sm.mma2[pk], pn & 1, sm, hdr, epoch)) return false;
-            if (leader) TRACE(2, (6u << 24) | (pn * 2 + pk));
-            tc_fence_after();
-            uint8_t *yrow = sm.xs[pk] + i * 128;
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ MMA issuer: C.S
+        // Per head, once the chain has put the entering state into shared memory: y_inter = C . S_in into the
+        // columns of the head's chunk state (already read by the chain). Issued apart from MMA1 so that neither
+        // waits behind the other's issue.
+        if (lane == 0) {
+            constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
+            for (uint32_t h2 = 0;; ++h2) {
+                const uint32_t k3 = h2 % 3, n3 = h2 / 3, k = h2 & 1;
+                if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+                const int32_t valid = sm.tab[k3].valid, last_of_unit = sm.tab[k3].hh == hs - 1;
+                if (!valid) break;
+                if (!BWAIT(&sm.sin_full[k], (h2 >> 1) & 1)) break;
+                const uint32_t u = (h2 / (uint32_t)hs) & 1;
+                tc_fence_after();
+                const uint64_t da = desc_sw128(smem_u32(sm.bc[u][2]), 16, 1024);
+                const uint64_t db = desc_sw128(smem_u32(sm.x[k3]), 8192, 1024);
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
+                for (uint32_t s = 0; s < 8; ++s)
+                    mma_ss(tmem + kColS + 64 * k, da + (s >> 2) * (kTile >> 4) + (s & 3) * 2, db + 128 * s, idCS, s > 0);
+                mma_commit(&sm.mma2[k]);
+                if (last_of_unit) mma_commit(&sm.bc_empty[u]);  // last reader of the unit's B/C
+                TRACE(warp, 3, h2);
+            }
+            mma_commit(&sm.drain[1]);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&sm.drain[1], 0) && globaltimer() - t0 < 1000000000ull) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P warpgroup
+        // P = CB o decay o dt, masked above the diagonal, fp16 into the head's P slot. One 32-column block of CB
+        // per step. Blocks above the diagonal block stay zero: they are written once here, and nothing else writes
+        // the P columns. Below the diagonal block exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j) with a the
+        // block's last row, both factors <= 1 (the semiseparable off-diagonal blocks are low rank). In the
+        // diagonal block the first factor is >= 1, so the split is used only while the block's whole decay range
+        // keeps it <= 2^100 (warp-uniform test), else exp is taken per element; the mask then clears every column
+        // past the row's own (an inf or NaN there included) by bit masks on the packed halves.
+        const int q = warp & 3;       // TMEM lane quarter of this warp
+        const int i = 32 * q + lane;  // tile row (token within the chunk) owned by this thread
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+            for (int k = 0; k < 2; ++k)
+                for (int J = q + 1; J < 4; ++J) tmem_st16(tmem + lrow + kColP + 64 * k + 16 * J, z);
+            tmem_st_wait();
+        }
+        // diagonal-block masks: keep columns e <= lane (low half of pair m: column 2m, high half: 2m + 1)
+        uint32_t dmask[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            dmask[m] = (2 * m <= lane ? 0x0000ffffu : 0u) | (2 * m + 1 <= lane ? 0xffff0000u : 0u);
+        for (uint32_t hc = 0;; ++hc) {
+            const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
+            if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+            const HeadTab &tb = sm.tab[k3];
+            if (!tb.valid) break;
+            if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) break;  // P slot free: MMA1 of head hc - 2 has completed
+            if (tb.hh == 0 && !BWAIT(&sm.cb_full, tb.v & 1)) break;
+            tc_fence_after();
+            if (lane == 0) TRACE(warp, 1, hc);
+            const float cs2i = tb.cs2[i];
+            const uint32_t pcol = tmem + lrow + kColP + 64 * k2;
+            const float dk = tb.dskip;
+            const float4 dadd = make_float4((lane & 3) == 0 ? dk : 0.f, (lane & 3) == 1 ? dk : 0.f,
+                                            (lane & 3) == 2 ? dk : 0.f, (lane & 3) == 3 ? dk : 0.f);
+#pragma unroll 1
+            for (int J = 0; J <= q; ++J) {
+                const float ca = tb.cs2[32 * J + 31];
+                const bool diag = J == q;
+                if (diag && tb.cs2[32 * J] - ca > 100.f) {  // rare: decay range too wide for the split
+                    p_block_exact(tmem + lrow + kColCB + 32 * J, pcol + 16 * J, tb.cs2 + 32 * J, tb.dt + 32 * J, cs2i,
+                                  tb.dskip);
+                    continue;
+                }
+                const int ed = diag ? lane >> 2 : -1;  // the 4-column group holding this row's diagonal element
+                float4 t1[8];
+                const float4 *s1 = reinterpret_cast<const float4 *>(tb.wt + 32 * J);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t1[e] = s1[e];
+                const float ui = ex2(cs2i - ca);
+                uint32_t cb[32];
+                tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
+                tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
+                tmem_ld_wait();
+                uint32_t pk[16];
+                const float2 uu = make_float2(ui, ui);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float2 a = fmul2(fmul2(f2(cb[4 * e], cb[4 * e + 1]), make_float2(t1[e].x, t1[e].y)), uu);
+                    float2 b = fmul2(fmul2(f2(cb[4 * e + 2], cb[4 * e + 3]), make_float2(t1[e].z, t1[e].w)), uu);
+                    if (e == ed) {  // D x_i enters y through P's diagonal (added before the fp16 rounding)
+                        a.x += dadd.x;
+                        a.y += dadd.y;
+                        b.x += dadd.z;
+                        b.y += dadd.w;
+                    }
+                    pk[2 * e] = pack_f16(a.x, a.y);
+                    pk[2 * e + 1] = pack_f16(b.x, b.y);
+                }
+                if (diag) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) pk[m] &= dmask[m];
+                }
+                tmem_st16(pcol + 16 * J, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[k2]);
+            if (lane == 0) TRACE(warp, 2, hc);
+            if (tb.hh == hs - 1) mbar_arrive(&sm.cb_empty);
+            if (tb.hh == (hs > 3 ? hs - 3 : 0)) mbar_arrive(&sm.unit_go);  // late tickets: the next unit
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------ X_s / epilogue warpgroup
+        // Per head: X_s = exp(cs_last - cs_j) dt_j x_j (and the x tile to fp16 in place) into the head's X_s
+        // buffer, once MMA1 two heads back has released it; then the epilogue of the head before:
+        // y = y_intra + exp(cs_i) y_inter (D x is in y_intra through P's diagonal), staged in the head's x slot in
+        // the y map's 128B swizzle and sent by one TMA store per warp (32 rows); the store clips rows past the
+        // sequence end.
+        const int q = warp & 3;
+        const int i = 32 * q + lane;
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        if (lane == 0) prefetch_tensormap(&map_y);
+        IO *yg = static_cast<IO *>(p.y);
+        auto epilogue = [&](uint32_t hp) -> bool {
+            const uint32_t k2 = hp & 1, n2 = hp >> 1, k3 = hp % 3;
+            if (!BWAIT(&sm.mma2[k2], n2 & 1)) return false;
+            tc_fence_after();
+            if (lane == 0) TRACE(warp, 3, hp);
+            const HeadTab &tb = sm.tab[k3];
+            const float ecs = ex2(tb.cs2[i]);
+            uint8_t *row = sm.x[k3] + i * 128;  // y row i, staged in the head's x slot (C.S has read S_in there)
+            const float2 e2 = make_float2(ecs, ecs);
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {  // columns 16 m .. 16 m + 15: 16-byte chunks 2 m, 2 m + 1 of the row
                 uint32_t a[16], c2[16];
-                tmem_ld16(tmem + lrow + kColYI + 64 * pk + 16 * m, a);
-                tmem_ld16(tmem + lrow + kColP + 64 * pk + 16 * m, c2);
+                tmem_ld16(tmem + lrow + kColYI + 64 * k2 + 16 * m, a);
+                tmem_ld16(tmem + lrow + kColS + 64 * k2 + 16 * m, c2);
+                const int o0 = ((2 * m) ^ (i & 7)) << 4, o1 = ((2 * m + 1) ^ (i & 7)) << 4;
                 tmem_ld_wait();
                 uint32_t o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float y0 = __uint_as_float(a[2 * e]) + pecs * __uint_as_float(c2[2 * e]);
-                    const float y1 = __uint_as_float(a[2 * e + 1]) + pecs * __uint_as_float(c2[2 * e + 1]);
-                    o[e] = pack_io<IO>(y0, y1);
+                    const float2 y = ffma2(e2, f2(c2[2 * e], c2[2 * e + 1]), f2(a[2 * e], a[2 * e + 1]));
+                    o[e] = pack_io<IO>(y.x, y.y);
                 }
-                sts128(yrow + (((2 * m) ^ (i & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
-                sts128(yrow + (((2 * m + 1) ^ (i & 7)) << 4), make_uint4(o[4], o[5], o[6], o[7]));
+                sts128(row + o0, make_uint4(o[0], o[1], o[2], o[3]));
+                sts128(row + o1, make_uint4(o[4], o[5], o[6], o[7]));
             }
-            if (pvr >= 32) {
+            tc_fence_before();
+            mbar_arrive(&sm.acc_free[k2]);  // y_intra and y_inter of this slot have been read
+            if (lane == 0) TRACE(warp, 5, hp);
+            const int vr = tb.rows - 32 * q, ph = tb.h, prow = tb.row0 + 32 * q;
+            if (vr >= 32) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_4d(&map_y, sm.xs[pk] + 32 * q * 128, 0, ph, prow, 0);
+                    tma_store_4d(&map_y, sm.x[k3] + 32 * q * 128, 0, ph, prow, 0);
                     bulk_commit();
+                    TRACE(warp, 6, hp);
+                    bulk_wait_read0();  // the store has read the slot
+                    mbar_arrive(&sm.x_empty[k3]);
                 }
-            } else if (lane < pvr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    chk(yg, ((int64_t)(prow + lane) * p.H + ph) * kP, kP, p.batch * p.L * p.H * kP, hdr, SITE_TC_Y));
+            } else {
+                if (lane < vr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        chk(yg, ((int64_t)(prow + lane) * p.H + ph) * kP, kP, p.batch * p.L * p.H * kP, hdr, SITE_TC_Y));
 #pragma unroll
-                for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(yrow + ((lc ^ (i & 7)) << 4));
+                    for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(row + ((lc ^ (i & 7)) << 4));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.x_empty[k3]);
             }
-            if (leader) TRACE(2, (7u << 24) | (pn * 2 + pk));
+            __syncwarp();
+            if (lane == 0) TRACE(warp, 4, hp);
             return true;
         };
-        for (uint32_t v = 0; ok; ++v) {
-            const uint32_t u = v & 1, nn = v >> 1;
-            if (!bwait(&sm.bc_conv[u], nn & 1, sm, hdr, epoch)) {
+        bool pend = false, ok = true;
+        uint32_t hc = 0;
+        for (;; ++hc) {
+            const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
+            if (!BWAIT(&sm.x_full[k3], n3 & 1)) {
                 ok = false;
                 break;
             }
-            const Sched sc = sm.sched[u];
-            if (!sc.valid) break;
-            if (leader) TRACE(2, (1u << 24) | v);
-
-            // (3) per head: X_s, P, then the previous head's epilogue
-            for (int hh = 0; hh < hs; ++hh, ++hc) {
-                const uint32_t k = hc & 1, n = hc >> 1;
-                const int h = sc.h0 + hh;
-                if (!bwait(&sm.x_full[k], n & 1, sm, hdr, epoch)) {
-                    ok = false;
-                    break;
-                }
-                if (leader) TRACE(2, (2u << 24) | hc);
-                if (lane == 0) bulk_wait_read0();  // this warp's y store from xs[k] (two heads back) has read it
-                __syncwarp();
-                const float cs2i = sm.cs2[u][hh][i];
-                const float xscale = ex2(sm.cs2[u][hh][kQ - 1] - cs2i) * sm.dt[u][hh][i];
-                if constexpr (CONV) {
-                    // row i of x convolved from the raw rows i-3 .. i (rows before the chunk from the halo), then,
-                    // once every row has been read, written back as fp16 together with X_s
-                    uint32_t xo[kP / 2], so[kP / 2];
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) {
-                        uint4 rr[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int r = i - 3 + j;
-                            rr[j] = r >= 0 ? lds128(sm.x[k] + r * 128 + ((lc ^ (r & 7)) << 4))
-                                           : lds128(sm.xhalo[k] + (r + 3) * 128 + lc * 16);
-                        }
-                        const float4 bb0 = reinterpret_cast<const float4 *>(sm.xbias[k])[2 * lc];
-                        const float4 bb1 = reinterpret_cast<const float4 *>(sm.xbias[k])[2 * lc + 1];
-                        const float bias8[8] = {bb0.x, bb0.y, bb0.z, bb0.w, bb1.x, bb1.y, bb1.z, bb1.w};
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {  // channel pairs of this 16-byte chunk
-                            float o[2];
-#pragma unroll
-                            for (int c2 = 0; c2 < 2; ++c2) {
-                                const int e = 2 * e2 + c2;
-                                const float4 tw = sm.xtap[k][8 * lc + e];
-                                float in[4];
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const uint32_t wv = reinterpret_cast<const uint32_t *>(&rr[j])[e2];
-                                    const float2 f = unpack_io<IO>(wv);
-                                    in[j] = c2 ? f.y : f.x;
-                                }
-                                float acc = fmaf(tw.w, in[3], fmaf(tw.z, in[2], fmaf(tw.y, in[1], fmaf(tw.x, in[0], bias8[e]))));
-                                o[c2] = p.conv_silu ? silu_fast(acc) : acc;
-                            }
-                            xo[4 * lc + e2] = pack_f16(o[0], o[1]);
-                            so[4 * lc + e2] = pack_f16(o[0] * xscale, o[1] * xscale);
-                        }
-                    }
-                    bar_sync(kBarMath, 128);  // every thread has read its raw rows: the tile may be overwritten
-                    uint8_t *xr = sm.x[k] + i * 128;
-                    uint8_t *sr = sm.xs[k] + i * 128;
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) {
-                        const int off = (lc ^ (i & 7)) << 4;
-                        sts128(xr + off, make_uint4(xo[4 * lc], xo[4 * lc + 1], xo[4 * lc + 2], xo[4 * lc + 3]));
-                        sts128(sr + off, make_uint4(so[4 * lc], so[4 * lc + 1], so[4 * lc + 2], so[4 * lc + 3]));
-                    }
-                } else {
-                    uint8_t *xr = sm.x[k] + i * 128;
-                    uint8_t *sr = sm.xs[k] + i * 128;
-                    uint4 w[8];
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) w[lc] = lds128(xr + ((lc ^ (i & 7)) << 4));
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) {
-                        const int off = (lc ^ (i & 7)) << 4;
-                        uint32_t *wv = reinterpret_cast<uint32_t *>(&w[lc]);
-                        uint4 s4;
-                        uint32_t *sv = reinterpret_cast<uint32_t *>(&s4);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_io<IO>(wv[e]);
-                            sv[e] = pack_f16(f.x * xscale, f.y * xscale);
-                            if (kBf16) wv[e] = pack_f16(f.x, f.y);
-                        }
-                        if (kBf16) sts128(xr + off, w[lc]);
-                        sts128(sr + off, s4);
-                    }
-                }
-                if (leader) TRACE(2, (8u << 24) | hc);
-                fence_proxy_async_smem();
-                if (leader) TRACE(2, (5u << 24) | hc);
-                if (hh == 0) {
-                    if (!bwait(&sm.cb_full, v & 1, sm, hdr, epoch)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                // P = CB o decay o dt (+ D on the diagonal), masked above the diagonal, fp16 into TMEM
-                const float Dh = sm.dskip[u][hh];
-                const float *cs2r = sm.cs2[u][hh];
-                const float *dtr = sm.dt[u][hh];
-                const float *wtr = sm.wt[u][hh];
-                // One 32-column block of CB per iteration (rolled: keeps the hot code small). Blocks above
-                // the diagonal block are zero. Elsewhere exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j)
-                // with a the block's last row: below the diagonal block both factors are <= 1; in the
-                // diagonal block the first is >= 1, so it is used only while the block's whole decay range
-                // keeps it <= 2^100 (warp-uniform test), else the diagonal block takes exp directly. The
-                // shared-memory tables are read before the TMEM load so their latency overlaps it.
-#pragma unroll 1
-                for (int J = 0; J < 4; ++J) {
-                    uint32_t pk16[16];
-                    if (J > q) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) pk16[e] = 0u;
-                    } else {
-                        const bool diag = J == q;
-                        const float ca = cs2r[32 * J + 31];
-                        const bool fac = !diag || cs2r[32 * J] - ca <= 100.f;
-                        float4 t1[8], t2[8];
-                        const float4 *s1 = reinterpret_cast<const float4 *>((fac ? wtr : cs2r) + 32 * J);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) t1[e] = s1[e];
-                        if (!fac) {
-                            const float4 *d4 = reinterpret_cast<const float4 *>(dtr + 32 * J);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) t2[e] = d4[e];
-                        }
-                        const float ui = ex2(cs2i - ca);
-                        uint32_t cb[32];
-                        tmem_ld16(tmem + lrow + kColCB + 32 * J, *reinterpret_cast<uint32_t(*)[16]>(&cb[0]));
-                        tmem_ld16(tmem + lrow + kColCB + 32 * J + 16, *reinterpret_cast<uint32_t(*)[16]>(&cb[16]));
-                        tmem_ld_wait();
-                        if (leader) TRACE(2, ((9u + J) << 24) | hc);
-                        if (fac) {
-                            const int lim = diag ? i : (1 << 30);  // columns j < lim are kept; j == i also takes D
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j0 = 32 * J + 4 * e;
-                                float v0 = __uint_as_float(cb[4 * e]) * ui * t1[e].x;
-                                float v1 = __uint_as_float(cb[4 * e + 1]) * ui * t1[e].y;
-                                float v2 = __uint_as_float(cb[4 * e + 2]) * ui * t1[e].z;
-                                float v3 = __uint_as_float(cb[4 * e + 3]) * ui * t1[e].w;
-                                v0 = j0 < lim ? v0 : (j0 == i ? v0 + Dh : 0.f);
-                                v1 = j0 + 1 < lim ? v1 : (j0 + 1 == i ? v1 + Dh : 0.f);
-                                v2 = j0 + 2 < lim ? v2 : (j0 + 2 == i ? v2 + Dh : 0.f);
-                                v3 = j0 + 3 < lim ? v3 : (j0 + 3 == i ? v3 + Dh : 0.f);
-                                pk16[2 * e] = pack_f16(v0, v1);
-                                pk16[2 * e + 1] = pack_f16(v2, v3);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float4 cv = t1[e], dv = t2[e];
-                                const int j0 = 32 * J + 4 * e;
-                                float v0 = __uint_as_float(cb[4 * e]) * ex2(cs2i - cv.x) * dv.x;
-                                float v1 = __uint_as_float(cb[4 * e + 1]) * ex2(cs2i - cv.y) * dv.y;
-                                float v2 = __uint_as_float(cb[4 * e + 2]) * ex2(cs2i - cv.z) * dv.z;
-                                float v3 = __uint_as_float(cb[4 * e + 3]) * ex2(cs2i - cv.w) * dv.w;
-                                v0 = j0 < i ? v0 : (j0 == i ? v0 + Dh : 0.f);
-                                v1 = j0 + 1 < i ? v1 : (j0 + 1 == i ? v1 + Dh : 0.f);
-                                v2 = j0 + 2 < i ? v2 : (j0 + 2 == i ? v2 + Dh : 0.f);
-                                v3 = j0 + 3 < i ? v3 : (j0 + 3 == i ? v3 + Dh : 0.f);
-                                pk16[2 * e] = pack_f16(v0, v1);
-                                pk16[2 * e + 1] = pack_f16(v2, v3);
-                            }
-                        }
-                    }
-                    tmem_st16(tmem + lrow + kColP + 64 * k + 16 * J, pk16);
-                }
-                tmem_st_wait();
-                if (leader) TRACE(2, (13u << 24) | hc);
-                tc_fence_before();
-                bar_sync(kBarMath, 128);
-                if (leader) TRACE(2, (14u << 24) | hc);
-                if (leader) {
-                    mbar_arrive(&sm.p_full[k]);
-                    if (hh == hs - 1) mbar_arrive(&sm.cb_empty);
-                    if (hh == (hs > 3 ? hs - 3 : 0)) mbar_arrive(&sm.unit_go);  // late tickets: the next unit
-                    TRACE(2, (3u << 24) | hc);
-                }
-                if (pend && !epilogue()) {
-                    ok = false;
-                    break;
-                }
-                pend = true;
-                pk = k;
-                pn = n;
-                pecs = ex2(cs2i);
-                ph = h;
-                prow = sc.row0 + 32 * q;
-                pvr = sc.rows - 32 * q;
+            const HeadTab &tb = sm.tab[k3];
+            if (!tb.valid) break;
+            if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) {  // X_s buffer free: MMA1 of head hc - 2 has completed
+                ok = false;
+                break;
             }
+            if (lane == 0) TRACE(warp, 1, hc);
+            const float xscale = ex2(tb.cs2[kQ - 1] - tb.cs2[i]) * tb.dt[i];
+            uint8_t *xr = sm.x[k3] + i * 128;
+            uint8_t *sr = sm.xs[k2] + i * 128;
+            if constexpr (CONV) {
+                // row i of x convolved from the raw rows i-3 .. i (rows before the chunk from the halo), then,
+                // once every row has been read, written back as fp16 together with X_s
+                uint32_t xo[kP / 2], so[kP / 2];
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc) {
+                    uint4 rr[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = i - 3 + j;
+                        rr[j] = r >= 0 ? lds128(sm.x[k3] + r * 128 + ((lc ^ (r & 7)) << 4))
+                                       : lds128(sm.cv.halo[k3] + (r + 3) * 128 + lc * 16);
+                    }
+                    const float4 bb0 = reinterpret_cast<const float4 *>(sm.cv.bias[k3])[2 * lc];
+                    const float4 bb1 = reinterpret_cast<const float4 *>(sm.cv.bias[k3])[2 * lc + 1];
+                    const float bias8[8] = {bb0.x, bb0.y, bb0.z, bb0.w, bb1.x, bb1.y, bb1.z, bb1.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {  // channel pairs of this 16-byte chunk
+                        float o[2];
+#pragma unroll
+                        for (int c2 = 0; c2 < 2; ++c2) {
+                            const int e = 2 * e2 + c2;
+                            const float4 tw = sm.cv.tap[k3][8 * lc + e];
+                            float in[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t wv = reinterpret_cast<const uint32_t *>(&rr[j])[e2];
+                                const float2 f = unpack_io<IO>(wv);
+                                in[j] = c2 ? f.y : f.x;
+                            }
+                            float acc = fmaf(tw.w, in[3], fmaf(tw.z, in[2], fmaf(tw.y, in[1], fmaf(tw.x, in[0], bias8[e]))));
+                            o[c2] = p.conv_silu ? silu_fast(acc) : acc;
+                        }
+                        xo[4 * lc + e2] = pack_f16(o[0], o[1]);
+                        so[4 * lc + e2] = pack_f16(o[0] * xscale, o[1] * xscale);
+                    }
+                }
+                bar_sync(kBarE, 128);  // every thread has read its raw rows: the tile may be overwritten
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc) {
+                    const int off = (lc ^ (i & 7)) << 4;
+                    sts128(xr + off, make_uint4(xo[4 * lc], xo[4 * lc + 1], xo[4 * lc + 2], xo[4 * lc + 3]));
+                    sts128(sr + off, make_uint4(so[4 * lc], so[4 * lc + 1], so[4 * lc + 2], so[4 * lc + 3]));
+                }
+            } else {
+                const float2 xs2 = make_float2(xscale, xscale);
+#pragma unroll 2
+                for (int lc = 0; lc < 8; ++lc) {
+                    const int off = (lc ^ (i & 7)) << 4;
+                    uint4 w = lds128(xr + off);
+                    uint32_t *wv = reinterpret_cast<uint32_t *>(&w);
+                    uint4 s4;
+                    uint32_t *sv = reinterpret_cast<uint32_t *>(&s4);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_io<IO>(wv[e]);
+                        const float2 sc = fmul2(f, xs2);
+                        sv[e] = pack_f16(sc.x, sc.y);
+                        if (kBf16) wv[e] = pack_f16(f.x, f.y);
+                    }
+                    if (kBf16) sts128(xr + off, w);
+                    sts128(sr + off, s4);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.xs_full[k2]);
+            if (lane == 0) TRACE(warp, 2, hc);
+            if (pend && !epilogue(hc - 1)) {
+                ok = false;
+                break;
+            }
+            pend = true;
         }
-        if (ok && pend) epilogue();
+        if (ok && pend) epilogue(hc - 1);
         if (lane == 0) bulk_wait0();  // every y store of this warp has completed
         __syncwarp();
-    } else {
+    } else if (warp >= 12) {
         // ------------------------------------------------------------ chain warpgroup
         // Thread n owns d_state row n of every state and passes it to the next chunk through a 2-slot ring per
         // chain, with no CTA barrier on either side of a hop:
-        //  - fp32 states: the row, then its own release flag (a 64-bit tag epoch:chunk); after each publish the
-        //    next head's row is prefetched when its flag is already visible;
-        //  - fp16 states: every 8-byte ring word carries two values and the 32-bit tag epoch * 4 + (chunk mod 4)
-        //    (a slot only has to tell chunk c from c - 2, its previous occupant, and from older launches). An aligned
-        //    8-byte access is single-copy atomic, so a word with the expected tag holds this launch's values for
-        //    that chunk: the data is its own flag (no release, no flag load), which shortens the serial chain of
-        //    hops by a round trip. (fp32 rows would need 128 registers in flight this way.)
+        //  - fp32 states: the row, then its own release flag (a 64-bit tag epoch:chunk);
+        //  - fp16 states: every 8-byte ring word carries two values and the 32-bit tag epoch * 1024 + (chunk mod
+        //    1024). A slot can still hold any earlier chunk of its chain that a unit in flight has not yet
+        //    overwritten; at most two tickets per CTA are unfinished, so those chunks lie fewer than 2 x SMs
+        //    (< 1024) indices back, and the chunk field tells them apart. An aligned 8-byte access is single-copy
+        //    atomic, so a word with the expected tag holds this launch's values for that chunk: the data is its
+        //    own flag (no release, no flag load), which shortens the serial chain of hops by a round trip.
+        // The entering row is fetched (and, if need be, awaited) first; then s_c is read from TMEM in four pieces
+        // of 16 columns, each combined, published and written to the C.S operand at once.
         const int q = warp & 3;
         const int nrow = 32 * q + lane;  // state row (d_state index) owned by this thread
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
@@ -943,17 +1069,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ST *fin = static_cast<ST *>(p.final_states);
         uint64_t *tags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]
         constexpr bool kTagged = sizeof(ST) == 2;
-        float S[kP];          // entering state of the current head (fp32)
-        bool have_S = false;  // the current head's entering state is (being) loaded into registers
-        Sched sc;
-        uint32_t v = 0;
-        int hh = 0;
-        auto enter_unit = [&](uint32_t vv) -> bool {
-            const uint32_t uu = vv & 1;
-            if (!bwait(&sm.bc_conv[uu], (vv >> 1) & 1, sm, hdr, epoch)) return false;
-            sc = sm.sched[uu];
-            return sc.valid != 0;
-        };
         ulonglong2 *ringv = static_cast<ulonglong2 *>(p.ring);  // fp16: [chain][slot][P / 4 vectors][row]
         const int64_t nvec = p.ring_bytes / 16, nstate = p.nseq * p.H * kP * kN;  // extents (bounds-checked builds)
         // row nrow of a slot: 16 vectors kN apart (checked as one span)
@@ -961,27 +1076,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             return chk(ringv, (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1, nvec, hdr,
                        SITE_TC_RING);
         };
-        auto vtag = [&](int c) { return (epoch << 2) | (uint32_t)(c & 3); };
-        // fp16: the tagged row of chunk c as loaded, and whether any of its words is stale
-        uint64_t raw[kTagged ? kP / 2 : 1];
-        auto issue_tagged = [&](int64_t chain, int c) {
-            const ulonglong2 *src = vrow_of(chain, c);
-#pragma unroll
-            for (int j = 0; j < (kTagged ? kP / 4 : 0); ++j) {
-                const ulonglong2 t = ld_ring(src + j * kN);
-                raw[2 * j] = t.x;
-                raw[2 * j + 1] = t.y;
-            }
+        auto vtag = [&](int c) { return (epoch << 10) | (uint32_t)(c & 1023); };
+        auto tag_of = [&](int64_t chain, int c) {
+            return chk(tags, (chain * 2 + (c & 1)) * kN + nrow, 1, p.flag_count, hdr, SITE_TC_FLAG);
         };
-        auto stale = [&](uint32_t want) {
-            uint32_t bad = 0;
+        auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
+        float S[kP];  // entering state of the current head (fp32)
+        for (uint32_t hc = 0;; ++hc) {
+            const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
+            if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+            const HeadTab &tb = sm.tab[k3];
+            if (!tb.valid) break;
+            const int64_t chain = (int64_t)tb.s * p.H + tb.h;
+            const int c = tb.c;
+            const bool last = tb.last != 0;
+            if (lane == 0) TRACE(warp, 1, hc);
+            // state entering the chunk
+            if (c == 0) {
 #pragma unroll
-            for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) bad |= (uint32_t)(raw[w] >> 32) ^ want;
-            return bad != 0;
-        };
-        // Row nrow of the state entering chunk c > 0 of `chain`, from the ring (the caller has seen its tag).
-        auto load_ring = [&](int64_t chain, int c) {
-            if (sizeof(ST) == 4) {
+                for (int pp = 0; pp < kP; ++pp)
+                    S[pp] = init ? to_f32(*chk(init, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_INIT)) : 0.f;
+            } else if (kTagged) {
+                const uint32_t want = vtag(c);
+                uint64_t raw[kTagged ? kP / 2 : 1];
+                auto issue = [&]() {
+                    const ulonglong2 *src = vrow_of(chain, c);
+#pragma unroll
+                    for (int j = 0; j < (kTagged ? kP / 4 : 0); ++j) {
+                        const ulonglong2 t = ld_ring(src + j * kN);
+                        raw[2 * j] = t.x;
+                        raw[2 * j + 1] = t.y;
+                    }
+                };
+                auto stale = [&]() {
+                    uint32_t bad = 0;
+#pragma unroll
+                    for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) bad |= (uint32_t)(raw[w] >> 32) ^ want;
+                    return bad != 0;
+                };
+                issue();
+                bool ok = !stale();
+                while (!ok) {  // not yet published, or only partly visible: wait on the row's last vector, reload
+                    if (aborted(hdr, epoch) ||
+                        !wait_ring(vrow_of(chain, c) + (kP / 4 - 1) * kN, want, epoch, hdr, limit, (uint32_t)c))
+                        break;
+                    issue();
+                    ok = !stale();
+                }
+#pragma unroll
+                for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) {  // zeros after a recorded error: the CTA drains
+                    const float2 f = ok ? unpack_f16((uint32_t)raw[w]) : make_float2(0.f, 0.f);
+                    S[2 * w] = f.x;
+                    S[2 * w + 1] = f.y;
+                }
+            } else if (ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
+                       (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c))) {
                 const float4 *src = chk(reinterpret_cast<const float4 *>(p.ring),
                                         (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
                                         nvec, hdr, SITE_TC_RING);
@@ -993,146 +1142,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                     S[4 * m + 2] = f.z;
                     S[4 * m + 3] = f.w;
                 }
+            } else {  // the error is recorded; carry on with zeros so the CTA drains
+#pragma unroll
+                for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
             }
-        };
-        auto tag_of = [&](int64_t chain, int c) {
-            return chk(tags, (chain * 2 + (c & 1)) * kN + nrow, 1, p.flag_count, hdr, SITE_TC_FLAG);
-        };
-        auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
-        // Prefetch (fp32 states): load the entering state now when its producer's tag is already visible.
-        auto prefetch = [&](int64_t chain, int c) -> bool {
-            if (kTagged || c == 0 || ld_acquire_u64(tag_of(chain, c)) != want_of(c)) return false;
-            load_ring(chain, c);
-            return true;
-        };
-        bool more = enter_unit(0);
-        int64_t chain = 0;
-        int c = 0;
-        if (more) {
-            chain = (int64_t)sc.s * p.H + sc.h0;
-            c = sc.c;
-        }
-        uint32_t hc = 0;
-        while (more) {
-            const uint32_t k = hc & 1, n = hc >> 1;
-            // state entering the chunk
-            auto fetch_S = [&]() {
-                if (!have_S) {
-                    if (c == 0) {
+            // chunk state s_c from TMEM, in pieces of 16 columns: S_out = a S_in + s_c, published; S_in to the
+            // C.S operand (K-row nrow of a [128 x 64] MN-major 128B-swizzled tile)
+            if (lane == 0) TRACE(warp, 2, hc);
+            if (!BWAIT(&sm.mma1[k2], n2 & 1)) break;
+            tc_fence_after();
+            if (lane == 0) TRACE(warp, 3, hc);
+            const float a = ex2(tb.cs2[kQ - 1]);  // decay across the chunk
+            const bool publish = !last && c != skip;
+            uint8_t *srow = sm.x[k3] + nrow * 128;  // the x tile is dead once MMA1 has read it
+            float4 *dst32 = nullptr;
+            ulonglong2 *dst16 = nullptr;
+            if (publish) {
+                if (kTagged)
+                    dst16 = vrow_of(chain, c + 1);
+                else
+                    dst32 = chk(reinterpret_cast<float4 *>(p.ring),
+                                (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
+                                nvec, hdr, SITE_TC_RING);
+            }
+            const uint64_t tg = (uint64_t)vtag(c + 1) << 32;
 #pragma unroll
-                        for (int pp = 0; pp < kP; ++pp)
-                            S[pp] = init ? to_f32(*chk(init, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_INIT)) : 0.f;
-                    } else if (kTagged) {
-                        const uint32_t want = vtag(c);
-                        issue_tagged(chain, c);
-                        bool ok = !stale(want);
-                        while (!ok) {  // not yet published, or only partly visible: wait on the row's last vector, reload
-                            if (aborted(hdr, epoch) ||
-                                !wait_ring(vrow_of(chain, c) + (kP / 4 - 1) * kN, want, epoch, hdr, limit, (uint32_t)c))
-                                break;
-                            issue_tagged(chain, c);
-                            ok = !stale(want);
-                        }
-                        if (ok) {
+            for (int m = 0; m < 4; ++m) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lrow + kColS + 64 * k2 + 16 * m, r);
+                tmem_ld_wait();
+                if (m == 1 && lane == 0) TRACE(warp, 5, hc);
+                float o[16];
 #pragma unroll
-                            for (int w = 0; w < (kTagged ? kP / 2 : 0); ++w) {
-                                const float2 f = unpack_f16((uint32_t)raw[w]);
-                                S[2 * w] = f.x;
-                                S[2 * w + 1] = f.y;
-                            }
-                        } else {  // the error is recorded; carry on with zeros so the CTA drains
+                for (int e = 0; e < 16; ++e) o[e] = fmaf(a, S[16 * m + e], __uint_as_float(r[e]));
+                if (last) {
+                    if (fin)
+                        store_final16<ST>(fin, (chain * kP + 16 * m) * kN + nrow, nstate, hdr,
+                                          make_float4(o[0], o[1], o[2], o[3]), make_float4(o[4], o[5], o[6], o[7]),
+                                          make_float4(o[8], o[9], o[10], o[11]), make_float4(o[12], o[13], o[14], o[15]));
+                } else if (publish) {
+                    if (kTagged) {  // tagged words, the row's last vector last
 #pragma unroll
-                            for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
-                        }
-                    } else if ((ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
-                                (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c)))) {
-                        load_ring(chain, c);
-                    } else {  // the error is recorded; carry on with zeros so the CTA drains
+                        for (int j = 0; j < 4; ++j)
+                            st_ring(dst16 + (4 * m + j) * kN, tg | pack_f16(o[4 * j], o[4 * j + 1]),
+                                    tg | pack_f16(o[4 * j + 2], o[4 * j + 3]));
+                    } else {
 #pragma unroll
-                        for (int pp = 0; pp < kP; ++pp) S[pp] = 0.f;
+                        for (int j = 0; j < 4; ++j)
+                            __stcg(dst32 + (4 * m + j) * kN, make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]));
                     }
                 }
-            };
-            // fp16 states fetch (and, if need be, wait for) the entering row before s_c is read, so no wait is a
-            // call with s_c's 64 registers live; fp32 states free s_c's TMEM columns first
-            if (kTagged) fetch_S();
-            // chunk state s_c from TMEM
-            if (!bwait(&sm.mma1[k], n & 1, sm, hdr, epoch)) break;
-            tc_fence_after();
-            float s[kP];
-            {
-                uint32_t r[4][16];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) tmem_ld16(tmem + lrow + kColS + 64 * k + 16 * m, r[m]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) s[16 * m + e] = __uint_as_float(r[m][e]);
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.s_free[k]);
-            if (warp == 6 && lane == 0) TRACE(3, (1u << 24) | hc);
-            const float a = ex2(sm.cs2[v & 1][hh][kQ - 1]);  // decay across the chunk
-            if (!kTagged) fetch_S();
-            // state leaving the chunk: S_out = a S_in + s (kept in s[])
-#pragma unroll
-            for (int pp = 0; pp < kP; ++pp) s[pp] = fmaf(a, S[pp], s[pp]);
-            const bool publish = !sc.last && c != skip;
-            if (sc.last) {
-                if (fin) {
-#pragma unroll
-                    for (int pp = 0; pp < kP; ++pp)
-                        *chk(fin, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_FINAL) = from_f32<ST>(s[pp]);
-                }
-            } else if (publish) {
-                if (sizeof(ST) == 4) {
-                    float4 *dst = chk(reinterpret_cast<float4 *>(p.ring),
-                                      (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
-                                      nvec, hdr, SITE_TC_RING);
-#pragma unroll
-                    for (int m = 0; m < kP / 4; ++m)
-                        __stcg(dst + m * kN, make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
-                } else {  // tagged words, the last vector last
-                    ulonglong2 *dst = vrow_of(chain, c + 1);
-                    const uint64_t tg = (uint64_t)vtag(c + 1) << 32;
-#pragma unroll
-                    for (int j = 0; j < kP / 4; ++j)
-                        st_ring(dst + j * kN, tg | pack_f16(s[4 * j], s[4 * j + 1]), tg | pack_f16(s[4 * j + 2], s[4 * j + 3]));
-                }
-            }
-            // S_in (fp16) -> the C.S operand: K-row nrow of a [128 x 64] MN-major 128B-swizzled tile
-            {
-                uint8_t *row = sm.xs[k] + nrow * 128;
-#pragma unroll
-                for (int lc = 0; lc < 8; ++lc)
-                    sts128(row + ((lc ^ (nrow & 7)) << 4),
+                for (int lc = 2 * m; lc < 2 * m + 2; ++lc)
+                    sts128(srow + ((lc ^ (nrow & 7)) << 4),
                            make_uint4(pack_f16(S[8 * lc], S[8 * lc + 1]), pack_f16(S[8 * lc + 2], S[8 * lc + 3]),
                                       pack_f16(S[8 * lc + 4], S[8 * lc + 5]), pack_f16(S[8 * lc + 6], S[8 * lc + 7])));
             }
+            tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(&sm.sin_full[k]);
-            if (warp == 6 && lane == 0) TRACE(3, (3u << 24) | hc);
-            // publish this head's row (the release orders the row's stores before the tag), then move to
-            // the next head and prefetch its entering state
+            mbar_arrive(&sm.sin_full[k2]);
+            if (lane == 0) TRACE(warp, 4, hc);
+            // publish this head's row (the release orders the row's stores before the tag)
             if (publish && !kTagged)
-                st_release_u64(tags + (chain * 2 + ((c + 1) & 1)) * kN + nrow,
-                               ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
-            ++hc;
-            if (hh + 1 < hs) {
-                ++hh;
-                ++chain;
-            } else {
-                ++v;
-                hh = 0;
-                more = enter_unit(v);
-                if (!more) break;
-                chain = (int64_t)sc.s * p.H + sc.h0;
-                c = sc.c;
-            }
-            have_S = prefetch(chain, c);
+                st_release_u64(tags + (chain * 2 + ((c + 1) & 1)) * kN + nrow, ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
         }
     }
+#undef BWAIT
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
@@ -1183,7 +1258,7 @@ cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     if (CONV ? !make_map(&mxh, p.x, bf, kP, p.H, T, p.x_ld, 3, false) : false) return cudaErrorInvalidValue;
     if (!CONV) mxh = mx;
-    const size_t smem = sizeof(Smem) + 1024;
+    const size_t smem = sizeof(Smem<CONV>) + 1024;
     auto k = tc_kernel<IO, ST, CONV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1211,10 +1286,8 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
     return (size_t)chains * 2 * (size_t)(P * N) * 4;
 }
 
-// Late tickets pay where few units share a chunk index, so that the state chain bounds the launch (measured on
-// GB300: -13 % at L = 256K and -6 % at L = 16K with 10-16 units per chunk index, -7 % on the 130M-shaped batch
-// with 32; +17-24 % at batch 8-32 with 80 and more, where the loads then exposed at every unit boundary cost more
-// than the chain).
+// Late tickets pay where few units share a chunk index, so that the state chain bounds the launch; where many
+// units share one, the loads then exposed at every unit boundary cost more than the chain.
 bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 4 <= sms; }
 
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {
@@ -1224,9 +1297,7 @@ uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs)
 
 // Heads per work unit: the largest divisor of heads-per-group (<= 8) that still leaves at least six units per
 // SM; small problems fall back to 1. More heads per unit share one C.B^T and one B/C load; more units spread the
-// chunk-serial state chain over more SMs (measured on GB300: the 130M-shaped batch runs 3 heads per unit 7-9 %
-// faster than 4 with late tickets; 4 beat 8 by 8-9 % where 8 left 2.5-4 units per SM; 8 beat 4 by 8 % at 33 units
-// per SM).
+// chunk-serial state chain over more SMs.
 int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms) {
     const int64_t hpg = H / G;
     for (int d = kMaxHs; d >= 1; --d)
@@ -1244,6 +1315,7 @@ cudaError_t launch_any(const Params &p, int io_dtype, int state_dtype, int hs, i
 }
 
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
+    if (hs < 1 || hs > kMaxHs || p.heads_per_group % hs) return cudaErrorInvalidValue;
     return p.conv_w ? launch_any<true>(p, io_dtype, state_dtype, hs, sms, stream)
                     : launch_any<false>(p, io_dtype, state_dtype, hs, sms, stream);
 }
@@ -1254,7 +1326,7 @@ cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, 
 extern "C" __attribute__((visibility("default"))) int ssd_trace_read(unsigned long long *dst, unsigned int *counts) {
     if (cudaMemcpyFromSymbol(counts, ssd::g_trace_n, sizeof(ssd::g_trace_n)) != cudaSuccess) return -1;
     if (cudaMemcpyFromSymbol(dst, ssd::g_trace, sizeof(ssd::g_trace)) != cudaSuccess) return -1;
-    static const unsigned int zero[4] = {0, 0, 0, 0};
+    static const unsigned int zero[ssd::kTraceRoles] = {};
     return cudaMemcpyToSymbol(ssd::g_trace_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -1;
 }
 #endif
