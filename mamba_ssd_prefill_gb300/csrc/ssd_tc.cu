@@ -389,7 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t *abort_flag = &sm.abort;
     unsigned int trace_i = 0;  // per-thread trace record counter (trace builds)
     (void)trace_i;
-#define BWAIT(bar, par) bwait((bar), (par), abort_flag, hdr, epoch)
+// Waits of whole warps are made warp-uniform (a timeout or abort seen by some lanes only must not leave the others
+// in a warp-collective instruction); BWAIT1 is the wait of a single issuing lane.
+#define BWAIT(bar, par) __all_sync(0xffffffffu, bwait((bar), (par), abort_flag, hdr, epoch))
+#define BWAIT1(bar, par) bwait((bar), (par), abort_flag, hdr, epoch)
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -584,6 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ? to_f32(*chk(dtr, (sc.row0 + i) * p.H + sc.h0 + hh + probe, 1, ndt, hdr, SITE_TC_DT))
                                       : 0.f;
             }
+            // the unit's per-head parameters, lane hh holding head h0 + hh's (broadcast per head by shuffles)
+            const bool own = sc.valid && lane < hs;
+            const float u_bias = own ? p.dt_bias[sc.h0 + lane] : 0.f, u_A = own ? p.A[sc.h0 + lane] : 0.f;
+            const float u_D = own && p.D ? p.D[sc.h0 + lane] : 0.f;
             for (int hh = 0; hh < nh; ++hh, ++hc) {
                 const uint32_t k = hc % 3, n = hc / 3;
                 if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
@@ -636,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 1; e < kMaxHs; ++e) rh[jj] = hh == e ? raw[jj][e] : rh[jj];
                 }
-                const float bias = p.dt_bias[h], Ah = p.A[h];
+                const float bias = __shfl_sync(0xffffffffu, u_bias, hh), Ah = __shfl_sync(0xffffffffu, u_A, hh);
+                const float dskip = __shfl_sync(0xffffffffu, u_D, hh);
                 float dtv[4], cum[4];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
@@ -670,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tb.row0 = sc.row0;
                     tb.rows = sc.rows;
                     tb.last = sc.last;
-                    tb.dskip = p.D ? p.D[h] : 0.f;
+                    tb.dskip = dskip;
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -781,10 +789,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
             for (uint32_t h2 = 0;; ++h2) {
                 const uint32_t k3 = h2 % 3, n3 = h2 / 3, k = h2 & 1;
-                if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+                if (!BWAIT1(&sm.x_full[k3], n3 & 1)) break;
                 const int32_t valid = sm.tab[k3].valid, last_of_unit = sm.tab[k3].hh == hs - 1;
                 if (!valid) break;
-                if (!BWAIT(&sm.sin_full[k], (h2 >> 1) & 1)) break;
+                if (!BWAIT1(&sm.sin_full[k], (h2 >> 1) & 1)) break;
                 const uint32_t u = (h2 / (uint32_t)hs) & 1;
                 tc_fence_after();
                 const uint64_t da = desc_sw128(smem_u32(sm.bc[u][2]), 16, 1024);
@@ -1208,6 +1216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 #undef BWAIT
+#undef BWAIT1
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
