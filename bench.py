@@ -68,7 +68,7 @@ def algorithmic(w):
 
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("ssd_tc.cu", "sm100_ptx.cuh", "ssd_common.cuh"):
+    for f in ("ssd_tc.cu", "ssd_segstate.cu", "sm100_ptx.cuh", "ssd_common.cuh"):
         h.update(open(os.path.join(ROOT, "mamba_ssd_prefill_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -273,6 +273,7 @@ def run_gpu(args, w):
     inp = make_inputs(w, device=dev, seed=w.seed + rank)
     prob = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io], st)
     kernel = m.kernel_for(prob)
+    plan = m.plan_info(prob)
     ws = m.Workspace(dev)
     y = torch.empty_like(inp["x"])
     fin = torch.empty(w.batch, w.nheads, w.headdim, w.dstate, dtype=st, device=dev)
@@ -363,7 +364,9 @@ def run_gpu(args, w):
         dtv = torch.nn.functional.softplus(inp["dt_raw"].float() + inp["dt_bias"].float())
         cfg["dt_realised"] = [float(dtv.min()), float(dtv.max())]
         del dtv
-    cfg.update({"kernel": kernel, "l2": f"{FLUSH_BYTES >> 20} MiB buffer written before every step, outside the events",
+    cfg.update({"kernel": kernel, "segments": plan["segments"], "segment_chunks": plan["segment_chunks"],
+                "launches_per_step": plan["launches"],
+                "l2": f"{FLUSH_BYTES >> 20} MiB buffer written before every step, outside the events",
                 "wall_s_timed_region": round(wall, 3)})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -371,7 +374,7 @@ def run_gpu(args, w):
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "path": "ssd_fwd_host: pinned host buffers streamed in 8 token pieces (copies overlap compute)"},
-            "gpu_launches": args.steps, "clocks": clk.summary(wall0, wall1, load_end)}
+            "gpu_launches": args.steps * plan["launches"], "clocks": clk.summary(wall0, wall1, load_end)}
     if world == 1 and not args.no_cpu_baseline:
         import oracle
 

@@ -104,6 +104,10 @@ SSD_API ssd_status_t ssd_fwd_workspace_size(const ssd_problem_t *prob, size_t *b
  *  init_states          optional (NULL: zero initial state)
  *  final_states         optional (NULL: not written)
  *  workspace            required, 256-byte aligned, >= ssd_fwd_workspace_size
+ *                       (for long sequences that size includes two-level
+ *                       state passing; a workspace too small for it but large
+ *                       enough for one state chain per sequence runs without
+ *                       it, with the same results up to rounding)
  * Returns SSD_OK once the launch is queued. */
 SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw,
                              const float *dt_bias, const float *A, const void *B, const void *C,
@@ -199,10 +203,16 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
  *  conv_tma           depthwise convolution: 0 = the 16-byte-copy pipeline
  *                     (the form for rows that are not 16-byte multiples),
  *                     1 = the TMA-fed one where the rows allow it
+ *  tc_segment_chunks  tensor-core kernel, regular batches: 0 = one state
+ *                     chain per sequence, n >= 1 = two-level state passing
+ *                     with segments of n chunks (of 128 tokens); used only
+ *                     when it cuts a sequence into two or more segments.
+ *                     It changes the workspace size: set it before
+ *                     ssd_fwd_workspace_size.
  * The values are read by later calls on any host thread (not by calls already
  * queued). The library reads no environment variable. */
 SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
-                                     int32_t conv_tma);
+                                     int32_t conv_tma, int32_t tc_segment_chunks);
 
 /* ssd_fwd without a workspace argument, for callers that cannot allocate
  * device memory (no counterpart on the pages; it is a library convenience).
@@ -268,6 +278,24 @@ SSD_API ssd_status_t ssd_fwd_host(const ssd_problem_t *prob, int32_t pieces, con
 /* Which kernel ssd_fwd would run for `prob` (SSD_KERNEL_SIMT or _TC), or a
  * negative ssd_status_t if the problem is rejected. */
 SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob);
+
+/* What ssd_fwd plans for `prob` (a regular batch; host only, no CUDA call but
+ * the SM count): the kernel, the kernel launches one call makes, and the
+ * state passing. With two-level state passing (long sequences on the
+ * tensor-core path) every sequence is cut into `segments` segments of
+ * `segment_chunks` chunks of 128 tokens ("Accelerating Mamba2 with Kernel
+ * Fusion", state passing step, regrouped): a block kernel and a combine kernel
+ * compute the states entering the segments before the fused kernel, whose
+ * chunk-to-chunk state chain then restarts at every segment. segments == 1:
+ * one chain per sequence. */
+typedef struct {
+    int32_t kernel;          /* ssd_kernel_t (SSD_KERNEL_SIMT, _TC or _STEP)  */
+    int32_t launches;        /* kernel launches per ssd_fwd call              */
+    int64_t segments;        /* per sequence (1: no two-level state passing)  */
+    int64_t segment_chunks;  /* chunks per segment                             */
+    size_t workspace_bytes;  /* = ssd_fwd_workspace_size                       */
+} ssd_plan_t;
+SSD_API ssd_status_t ssd_fwd_plan(const ssd_problem_t *prob, ssd_plan_t *plan);
 
 /* Static text for a status code. */
 SSD_API const char *ssd_status_string(ssd_status_t status);

@@ -15,7 +15,7 @@ import threading
 
 import torch
 
-__all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "debug_knobs", "kernel_for", "SsdError",
+__all__ = ["ssd_fwd", "ssd_fwd_host", "ssd_fwd_varlen", "ssd_fwd_conv", "workspace_size", "make_problem", "check", "debug_set", "debug_knobs", "kernel_for", "plan_info", "SsdError",
            "Workspace", "lib", "LIB_PATH", "STATUS"]
 
 # MAMBA_SSD_LIB selects another build of the library (the bounds-checked debug build, libmamba_ssd_checked.so)
@@ -32,6 +32,11 @@ class SsdProblem(ctypes.Structure):
                 ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
                 ("chunk_size", ctypes.c_int64), ("io_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
                 ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class SsdPlan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("launches", ctypes.c_int32), ("segments", ctypes.c_int64),
+                ("segment_chunks", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class SsdError(RuntimeError):
@@ -75,10 +80,12 @@ def lib():
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
             L.ssd_debug_set.restype = ctypes.c_int
-            L.ssd_debug_knobs.argtypes = [ctypes.c_int32] * 4
+            L.ssd_debug_knobs.argtypes = [ctypes.c_int32] * 5
             L.ssd_debug_knobs.restype = ctypes.c_int
             L.ssd_fwd_kernel_for.argtypes = [pp]
             L.ssd_fwd_kernel_for.restype = ctypes.c_int
+            L.ssd_fwd_plan.argtypes = [pp, ctypes.POINTER(SsdPlan)]
+            L.ssd_fwd_plan.restype = ctypes.c_int
             L.ssd_status_string.argtypes = [ctypes.c_int]
             L.ssd_status_string.restype = ctypes.c_char_p
             L.ssd_version.argtypes = []
@@ -99,6 +106,16 @@ def workspace_size(prob: SsdProblem) -> int:
     if st:
         raise SsdError(st, "ssd_fwd_workspace_size")
     return int(n.value)
+
+
+def plan_info(prob: SsdProblem) -> dict:
+    """What ssd_fwd plans for a regular batch: kernel, launches per call, segments, chunks per segment, workspace."""
+    pl = SsdPlan()
+    st = lib().ssd_fwd_plan(ctypes.byref(prob), ctypes.byref(pl))
+    if st:
+        raise SsdError(st, "ssd_fwd_plan")
+    return {"kernel": {1: "simt", 2: "tc", 3: "step"}[pl.kernel], "launches": pl.launches, "segments": pl.segments,
+            "segment_chunks": pl.segment_chunks, "workspace_bytes": pl.workspace_bytes}
 
 
 def kernel_for(prob: SsdProblem) -> str:
@@ -375,8 +392,10 @@ def debug_set(workspace, timeout_ns=0, skip_publish=-1, stream=None):
         raise SsdError(st, "ssd_debug_set")
 
 
-def debug_knobs(tc_heads_per_unit=-1, tc_late_ticket=-1, simt_two_pass=-1, conv_tma=-1):
-    """Test hook: force launch-configuration choices of later calls (-1 everywhere restores the library's own)."""
-    st = lib().ssd_debug_knobs(int(tc_heads_per_unit), int(tc_late_ticket), int(simt_two_pass), int(conv_tma))
+def debug_knobs(tc_heads_per_unit=-1, tc_late_ticket=-1, simt_two_pass=-1, conv_tma=-1, tc_segment_chunks=-1):
+    """Test hook: force launch-configuration choices of later calls (-1 everywhere restores the library's own).
+    tc_segment_chunks changes the workspace size: allocate the workspace after setting it."""
+    st = lib().ssd_debug_knobs(int(tc_heads_per_unit), int(tc_late_ticket), int(simt_two_pass), int(conv_tma),
+                               int(tc_segment_chunks))
     if st:
         raise SsdError(st, "ssd_debug_knobs")

@@ -11,7 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libmamba_ssd.so")
 LIB_CHECKED = os.path.join(PKG, "libmamba_ssd_checked.so")  # debug build: every kernel's global indices range-checked
-SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_step.cu", "ssd_varlen.cu", "ssd_conv.cu", "ssd_noalloc.cu", "ssd_host.cu"]
+SOURCES = ["ssd_api.cu", "ssd_simt.cu", "ssd_tc.cu", "ssd_step.cu", "ssd_varlen.cu", "ssd_conv.cu", "ssd_noalloc.cu", "ssd_host.cu",
+           "ssd_segstate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

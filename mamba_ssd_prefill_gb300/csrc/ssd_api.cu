@@ -27,12 +27,14 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 namespace {
-std::atomic<int> g_knob[4] = {{-1}, {-1}, {-1}, {-1}};  // heads per unit, late ticket, SIMT two pass, conv TMA
+// heads per unit, late ticket, SIMT two pass, conv TMA, chunks per segment
+std::atomic<int> g_knob[5] = {{-1}, {-1}, {-1}, {-1}, {-1}};
 }  // namespace
 
 Knobs knobs() {
     return Knobs{g_knob[0].load(std::memory_order_relaxed), g_knob[1].load(std::memory_order_relaxed),
-                 g_knob[2].load(std::memory_order_relaxed), g_knob[3].load(std::memory_order_relaxed)};
+                 g_knob[2].load(std::memory_order_relaxed), g_knob[3].load(std::memory_order_relaxed),
+                 g_knob[4].load(std::memory_order_relaxed)};
 }
 
 }  // namespace ssd
@@ -73,7 +75,8 @@ struct Plan {
     int heads_per_unit = 1;  // TC only
     bool late_ticket = false;  // TC only: next ticket taken when the unit before it nears its end
     uint32_t total_units = 0;
-    size_t flags_off = 0, ring_off = 0, tab_off = 0, bytes = 0;
+    ssd::SegChoice seg{1, 0, 0, 0, 1};  // TC only, regular batches: two-level state passing when seg.nseg > 1
+    size_t flags_off = 0, ring_off = 0, tab_off = 0, seg_off = 0, blk_s_off = 0, blk_L_off = 0, bytes = 0;
 };
 
 // Variable-length tables after the ring: chunk pairs (int2), then four uint32 arrays of nc + 2 (histogram of
@@ -84,7 +87,7 @@ size_t varlen_table_bytes(int64_t nc, int64_t nseq) {
 
 // Validate the problem and lay out the workspace. No CUDA calls except the
 // SM count used to size the tensor-core work units. nseq < 0: a regular batch.
-ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
+ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out, bool segments = true) {
     if (!pr || !out) return SSD_ERR_INVALID_ARG;
     if (pr->reserved != 0) return SSD_ERR_INVALID_ARG;
     if (pr->batch < 0 || pr->seqlen < 0 || pr->nheads < 1 || pr->headdim < 1 || pr->dstate < 1 ||
@@ -134,9 +137,15 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
     }
     // regular: chunks per sequence; variable-length: no sequence has more than ceil(T / chunk)
     pl.nc = (pr->seqlen + pl.exec_chunk - 1) / pl.exec_chunk;
-    const int64_t chains = pl.nseq * pr->nheads;
+    int64_t chains = pl.nseq * pr->nheads;
     double units;
     if (pl.kernel == SSD_KERNEL_TC) {
+        if (!varlen && segments) {
+            // test hook: forced chunks per segment (0: off)
+            const int forced = ssd::knobs().tc_segment_chunks;
+            pl.seg = ssd::choose_segments(pl.nseq, pl.nc, pr->nheads, pr->ngroups, std::max(1, sm_count()), forced);
+            chains *= pl.seg.nseg;  // one state chain per (sequence, segment, head)
+        }
         // for a variable-length batch the chunk count is only bounded here (pairs <= nc + nseq); it sizes the units
         const int64_t pairs = varlen ? pl.nc + pl.nseq : pl.nc * pr->batch;
         pl.heads_per_unit = ssd::tc_heads_per_unit(1, pr->nheads, pr->ngroups, pairs, std::max(1, sm_count()));
@@ -145,7 +154,8 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
         if (kn.tc_heads_per_unit >= 1 && (pr->nheads / pr->ngroups) % kn.tc_heads_per_unit == 0)
             pl.heads_per_unit = kn.tc_heads_per_unit;
         units = (double)pairs * (double)(pr->nheads / pl.heads_per_unit);
-        pl.late_ticket = ssd::tc_late_ticket(pl.nseq * (pr->nheads / pl.heads_per_unit), std::max(1, sm_count()));
+        pl.late_ticket = ssd::tc_late_ticket(pl.nseq * pl.seg.nseg * (pr->nheads / pl.heads_per_unit),
+                                             std::max(1, sm_count()));
         // test hook: forced early (0) or late (1) tickets
         if (kn.tc_late_ticket >= 0) pl.late_ticket = kn.tc_late_ticket == 1;
     } else {
@@ -162,7 +172,14 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out) {
     else
         ring = (size_t)chains * 2 * (size_t)(pr->headdim * pr->dstate) * elem_size(pr->state_dtype);
     pl.tab_off = align_up(pl.ring_off + ring, 256);
-    pl.bytes = align_up(pl.tab_off + (varlen ? varlen_table_bytes(pl.nc, pl.nseq) : 0), 256);
+    pl.seg_off = align_up(pl.tab_off + (varlen ? varlen_table_bytes(pl.nc, pl.nseq) : 0), 256);
+    pl.blk_s_off = pl.blk_L_off = pl.bytes = pl.seg_off;
+    if (pl.seg.nseg > 1) {  // segment entering states, block aggregates and block decays (fp32)
+        const size_t st = (size_t)(pr->headdim * pr->dstate) * 4;
+        pl.blk_s_off = align_up(pl.seg_off + (size_t)(pl.nseq * (pl.seg.nseg - 1) * pr->nheads) * st, 256);
+        pl.blk_L_off = align_up(pl.blk_s_off + (size_t)(pl.nseq * pl.seg.nblk * pr->nheads) * st, 256);
+        pl.bytes = align_up(pl.blk_L_off + (size_t)(pl.nseq * pl.seg.nblk * pr->nheads) * 4, 256);
+    }
     *out = pl;
     return SSD_OK;
 }
@@ -198,6 +215,10 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
         const cudaError_t e = init_states ? cudaMemcpyAsync(final_states, init_states, n, cudaMemcpyDeviceToDevice, s)
                                           : cudaMemsetAsync(final_states, 0, n, s);
         return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    if (workspace_bytes < pl.bytes) {  // too small for two-level state passing: one state chain per sequence
+        Plan one;
+        if (plan(prob, nseq, &one, false) == SSD_OK && workspace_bytes >= one.bytes) pl = one;
     }
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.bytes) return SSD_ERR_WORKSPACE;
     const int sms = sm_count();
@@ -235,6 +256,13 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.tc_late_ticket = pl.late_ticket ? 1 : 0;
     p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
     p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
+    ssd::SegPlan sp{pl.seg.blk, pl.seg.nblk, pl.seg.hs, reinterpret_cast<float *>(ws + pl.blk_s_off),
+                    reinterpret_cast<float *>(ws + pl.blk_L_off)};
+    // two-level state passing (not with the fused convolution: the block kernel reads x as stored)
+    const bool seg = pl.seg.nseg > 1 && !conv;
+    p.nseg = seg ? pl.seg.nseg : 1;
+    p.seg_chunks = seg ? pl.seg.seg_chunks : pl.nc;
+    p.seg_states = seg ? reinterpret_cast<const float *>(ws + pl.seg_off) : nullptr;
     if (conv) {  // convolution fused into the tensor-core kernel: x, B, C are slices of the raw rows
         p.conv_w = conv->conv_w;
         p.conv_b = conv->conv_b;
@@ -257,14 +285,25 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     }
     if (pl.kernel == SSD_KERNEL_STEP)
         e = ssd::launch_step(p, pr.io_dtype, pr.state_dtype, sms, s);
-    else if (pl.kernel == SSD_KERNEL_TC)
-        e = ssd::launch_tc(p, pr.io_dtype, pr.state_dtype, pl.heads_per_unit, sms, s);
+    else if (pl.kernel == SSD_KERNEL_TC) {
+        if (seg) e = ssd::launch_segstate(p, sp, pr.io_dtype, pr.state_dtype, sms, s);
+        if (e == cudaSuccess) e = ssd::launch_tc(p, pr.io_dtype, pr.state_dtype, pl.heads_per_unit, sms, s);
+    }
     else
         e = ssd::launch_simt(p, pr.io_dtype, pr.state_dtype, sms, s);
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace ssd {
+ssd_status_t workspace_bytes(const ssd_problem_t *prob, bool segments, size_t *bytes) {
+    Plan pl;
+    const ssd_status_t st = plan(prob, -1, &pl, segments);
+    if (st == SSD_OK) *bytes = pl.bytes;
+    return st;
+}
+}  // namespace ssd
 
 extern "C" {
 
@@ -281,6 +320,20 @@ SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob) {
     Plan pl;
     const ssd_status_t st = plan(prob, -1, &pl);
     return st == SSD_OK ? pl.kernel : -(int)st;
+}
+
+SSD_API ssd_status_t ssd_fwd_plan(const ssd_problem_t *prob, ssd_plan_t *out) {
+    if (!out) return SSD_ERR_INVALID_ARG;
+    Plan pl;
+    const ssd_status_t st = plan(prob, -1, &pl);
+    if (st != SSD_OK) return st;
+    const bool tokens = prob->batch > 0 && prob->seqlen > 0;
+    out->kernel = pl.kernel;
+    out->segments = pl.seg.nseg;
+    out->segment_chunks = pl.seg.nseg > 1 ? pl.seg.seg_chunks : pl.nc;
+    out->launches = !tokens ? 0 : (pl.seg.nseg > 1 ? 3 : 1);
+    out->workspace_bytes = pl.bytes;
+    return SSD_OK;
 }
 
 SSD_API ssd_status_t ssd_fwd(const ssd_problem_t *prob, const void *x, const void *dt_raw, const float *dt_bias,
@@ -403,11 +456,12 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
 }
 
 SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
-                                     int32_t conv_tma) {
+                                     int32_t conv_tma, int32_t tc_segment_chunks) {
     if (tc_heads_per_unit != -1 && (tc_heads_per_unit < 1 || tc_heads_per_unit > 8)) return SSD_ERR_INVALID_ARG;
     if (tc_late_ticket < -1 || tc_late_ticket > 1 || simt_two_pass < -1 || simt_two_pass > 1 || conv_tma < -1 ||
-        conv_tma > 1)
+        conv_tma > 1 || tc_segment_chunks < -1)
         return SSD_ERR_INVALID_ARG;
+    ssd::g_knob[4].store(tc_segment_chunks, std::memory_order_relaxed);
     ssd::g_knob[0].store(tc_heads_per_unit, std::memory_order_relaxed);
     ssd::g_knob[1].store(tc_late_ticket, std::memory_order_relaxed);
     ssd::g_knob[2].store(simt_two_pass, std::memory_order_relaxed);

@@ -52,6 +52,8 @@ enum BoundsSite : uint32_t {
     SITE_SIMT_FLAG = 116,
     SITE_STEP_IN = 121, SITE_STEP_Y = 122, SITE_STEP_STATE = 123,
     SITE_CONV_IN = 131, SITE_CONV_OUT = 132, SITE_CONV_STATE = 133,
+    SITE_SEG_DT = 141, SITE_SEG_BLK = 142, SITE_SEG_DECAY = 143, SITE_SEG_STATE = 144, SITE_SEG_INIT = 145,
+    SITE_SEG_TMA = 146,
 };
 
 // Parameters common to the kernels. Element strides are implied by the packed
@@ -91,6 +93,12 @@ struct Params {
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
     int tc_late_ticket;    // tensor-core kernel: take each next ticket only when the unit before it nears its end
     int64_t ring_bytes, flag_count;  // extents of the ring and the flags (bounds-checked builds compare with them)
+    // Two-level state passing (tensor-core kernel, regular batches): with nseg > 1 every sequence is cut into nseg
+    // segments of seg_chunks chunks (the last one shorter or equal), the chunk-to-chunk state chain restarts at
+    // every segment, and the state entering segment k >= 1 is read from seg_states [nseq][nseg - 1][H][P][N]
+    // (fp32), computed beforehand from block aggregates. nseg <= 1: one chain per sequence.
+    int64_t nseg, seg_chunks;
+    const float *seg_states;
 };
 
 // Causal depthwise convolution over the packed token axis (nseq sequences of L tokens, D channels).
@@ -118,6 +126,24 @@ __device__ __forceinline__ SeqChunk seq_chunk(const Params &p, int64_t cp) {
         r.c = e.y;
         r.tok0 = p.cu[r.s];
         r.len = p.cu[r.s + 1] - r.tok0;
+    } else if (p.nseg > 1) {
+        // position-major over the (sequence, segment) chains, so that the segments of one sequence run side by
+        // side; only each sequence's last segment can be shorter (last_len chunks)
+        const int64_t nvs = p.nseq * p.nseg, last_len = p.nc - (p.nseg - 1) * p.seg_chunks;
+        int64_t pos, k;
+        if (cp < last_len * nvs) {
+            pos = cp / nvs;
+            r.s = (cp % nvs) / p.nseg;
+            k = (cp % nvs) % p.nseg;
+        } else {
+            const int64_t m = p.nseq * (p.nseg - 1), q = cp - last_len * nvs;
+            pos = last_len + q / m;
+            r.s = (q % m) / (p.nseg - 1);
+            k = (q % m) % (p.nseg - 1);
+        }
+        r.c = k * p.seg_chunks + pos;
+        r.tok0 = r.s * p.L;
+        r.len = p.L;
     } else {
         r.s = cp % p.nseq;
         r.c = cp / p.nseq;
@@ -125,6 +151,11 @@ __device__ __forceinline__ SeqChunk seq_chunk(const Params &p, int64_t cp) {
         r.len = p.L;
     }
     return r;
+}
+// Index of the state chain of chunk c of sequence s, head h: one per (sequence, head), or with two-level state
+// passing one per (sequence, segment, head).
+__device__ __forceinline__ int64_t chain_of(const Params &p, int64_t s, int64_t c, int64_t h) {
+    return p.nseg > 1 ? (s * p.nseg + c / p.seg_chunks) * p.H + h : s * p.H + h;
 }
 // Chunk pairs of this launch (regular batches know it on the host; variable-length ones read the device count).
 __device__ __forceinline__ uint32_t total_units(const Params &p, uint32_t units_per_pair) {

@@ -8,9 +8,13 @@
 
 #include <algorithm>
 
+#include "../../include/ssd.h"
 #include "ssd_common.cuh"
 
 namespace ssd {
+
+// Workspace bytes of a regular batch with or without two-level state passing (ssd_api.cu).
+ssd_status_t workspace_bytes(const ssd_problem_t *prob, bool segments, size_t *bytes);
 
 // cuTensorMapEncodeTiled, looked up once through the runtime's driver entry points (ssd_api.cu); null when the
 // driver has none
@@ -22,6 +26,7 @@ EncodeTiledFn encode_tiled_fn();
 // Launch-configuration overrides set by ssd_debug_knobs (test hooks; -1 = the library's own choice).
 struct Knobs {
     int tc_heads_per_unit, tc_late_ticket, simt_two_pass, conv_tma;
+    int tc_segment_chunks;  // -1: the library's choice, 0: one state chain per sequence, >= 1: chunks per segment
 };
 Knobs knobs();
 
@@ -47,5 +52,21 @@ uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hea
 int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms);
 bool tc_late_ticket(int64_t units_per_chunk, int sms);  // ticket order = finishing order (chain-bound problems)
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int heads_per_unit, int sms, cudaStream_t stream);
+
+// two-level state passing (ssd_segstate.cu): segment entering states from block aggregates, before launch_tc
+struct SegChoice {
+    int64_t nseg, seg_chunks;  // segments per sequence (1: off) and chunks per segment
+    int64_t blk, nblk;         // chunks per aggregate block, blocks per sequence with an aggregate
+    int hs;                    // heads per block-kernel work unit
+};
+SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced);
+struct SegPlan {
+    int64_t blk, nblk;
+    int hs;
+    float *blk_s;  // [nseq][nblk][H][P][N] block aggregates
+    float *blk_L;  // [nseq][nblk][H] log2 of the block decays
+};
+cudaError_t launch_segstate(const Params &p, const SegPlan &sp, int io_dtype, int state_dtype, int sms,
+                            cudaStream_t stream);
 
 }  // namespace ssd

@@ -18,13 +18,16 @@
 // between them) race on it and must not be issued. Each call zero-fills the
 // part of the array it uses (the part the kernel expects to start at zero) on
 // its stream before the launch, so the contents left by the previous call do
-// not matter. No call allocates or frees device memory.
+// not matter. No call allocates or frees device memory. Where two-level state
+// passing (long sequences) would need more than the array, the call runs with
+// one state chain per sequence instead.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <atomic>
 
 #include "../../include/ssd.h"
+#include "ssd_internal.h"
 
 namespace {
 
@@ -44,9 +47,13 @@ extern "C" SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob
                                                        const void *C, const float *D, const void *init_states,
                                                        void *y, void *final_states, void *stream) {
     size_t need = 0;
-    const ssd_status_t st = ssd_fwd_workspace_size(prob, &need);
+    ssd_status_t st = ssd_fwd_workspace_size(prob, &need);
     if (st != SSD_OK) return st;
-    if (need > kStaticScratchBytes) return SSD_ERR_WORKSPACE;  // problem too large for the static scratch
+    if (need > kStaticScratchBytes) {  // without two-level state passing, if that fits
+        st = ssd::workspace_bytes(prob, false, &need);
+        if (st != SSD_OK) return st;
+        if (need > kStaticScratchBytes) return SSD_ERR_WORKSPACE;  // problem too large for the static scratch
+    }
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
     void *ws = g_scratch_addr[dev].load(std::memory_order_acquire);
@@ -56,6 +63,6 @@ extern "C" SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (prob->batch > 0 && prob->seqlen > 0 && cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return SSD_ERR_CUDA;
-    return ssd_fwd(prob, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, ws, kStaticScratchBytes,
-                   stream);
+    // the workspace size passed is `need`: ssd_fwd then plans exactly what was sized (and zero-filled) here
+    return ssd_fwd(prob, x, dt_raw, dt_bias, A, B, C, D, init_states, y, final_states, ws, need, stream);
 }

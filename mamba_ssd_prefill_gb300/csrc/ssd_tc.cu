@@ -1095,20 +1095,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
             const HeadTab &tb = sm.tab[k3];
             if (!tb.valid) break;
-            const int64_t chain = (int64_t)tb.s * p.H + tb.h;
+            const int64_t chain = (int64_t)tb.s * p.H + tb.h;  // (sequence, head): initial and final states
             const int c = tb.c;
+            const int64_t rchain = chain_of(p, tb.s, c, tb.h);  // the state chain through the ring
             const bool last = tb.last != 0;
+            const bool seg_start = p.nseg > 1 && c > 0 && c % p.seg_chunks == 0;
             if (lane == 0) TRACE(warp, 1, hc);
             // state entering the chunk
             if (c == 0) {
 #pragma unroll
                 for (int pp = 0; pp < kP; ++pp)
                     S[pp] = init ? to_f32(*chk(init, (chain * kP + pp) * kN + nrow, 1, nstate, hdr, SITE_TC_INIT)) : 0.f;
+            } else if (seg_start) {  // the segment's entering state, computed before this launch
+                const int64_t base = ((tb.s * (p.nseg - 1) + c / p.seg_chunks - 1) * p.H + tb.h) * kP * kN + nrow;
+#pragma unroll
+                for (int pp = 0; pp < kP; ++pp)
+                    S[pp] = __ldcg(chk(p.seg_states, base + pp * kN, 1, p.nseq * (p.nseg - 1) * p.H * kP * kN, hdr,
+                                       SITE_TC_INIT));
             } else if (kTagged) {
                 const uint32_t want = vtag(c);
                 uint64_t raw[kTagged ? kP / 2 : 1];
                 auto issue = [&]() {
-                    const ulonglong2 *src = vrow_of(chain, c);
+                    const ulonglong2 *src = vrow_of(rchain, c);
 #pragma unroll
                     for (int j = 0; j < (kTagged ? kP / 4 : 0); ++j) {
                         const ulonglong2 t = ld_ring(src + j * kN);
@@ -1126,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = !stale();
                 while (!ok) {  // not yet published, or only partly visible: wait on the row's last vector, reload
                     if (aborted(hdr, epoch) ||
-                        !wait_ring(vrow_of(chain, c) + (kP / 4 - 1) * kN, want, epoch, hdr, limit, (uint32_t)c))
+                        !wait_ring(vrow_of(rchain, c) + (kP / 4 - 1) * kN, want, epoch, hdr, limit, (uint32_t)c))
                         break;
                     issue();
                     ok = !stale();
@@ -1137,10 +1145,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     S[2 * w] = f.x;
                     S[2 * w + 1] = f.y;
                 }
-            } else if (ld_acquire_u64(tag_of(chain, c)) == want_of(c) ||
-                       (!aborted(hdr, epoch) && wait_tag(tag_of(chain, c), want_of(c), epoch, hdr, limit, (uint32_t)c))) {
+            } else if (ld_acquire_u64(tag_of(rchain, c)) == want_of(c) ||
+                       (!aborted(hdr, epoch) && wait_tag(tag_of(rchain, c), want_of(c), epoch, hdr, limit, (uint32_t)c))) {
                 const float4 *src = chk(reinterpret_cast<const float4 *>(p.ring),
-                                        (chain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
+                                        (rchain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
                                         nvec, hdr, SITE_TC_RING);
 #pragma unroll
                 for (int m = 0; m < kP / 4; ++m) {
@@ -1161,16 +1169,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (lane == 0) TRACE(warp, 3, hc);
             const float a = ex2(tb.cs2[kQ - 1]);  // decay across the chunk
-            const bool publish = !last && c != skip;
+            // no publish after the last chunk of a sequence or of a segment (the next segment starts from its own
+            // entering state)
+            const bool publish = !last && c != skip && !(p.nseg > 1 && (c + 1) % p.seg_chunks == 0);
             uint8_t *srow = sm.x[k3] + nrow * 128;  // the x tile is dead once MMA1 has read it
             float4 *dst32 = nullptr;
             ulonglong2 *dst16 = nullptr;
             if (publish) {
                 if (kTagged)
-                    dst16 = vrow_of(chain, c + 1);
+                    dst16 = vrow_of(rchain, c + 1);
                 else
                     dst32 = chk(reinterpret_cast<float4 *>(p.ring),
-                                (chain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
+                                (rchain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
                                 nvec, hdr, SITE_TC_RING);
             }
             const uint64_t tg = (uint64_t)vtag(c + 1) << 32;
@@ -1212,7 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) TRACE(warp, 4, hc);
             // publish this head's row (the release orders the row's stores before the tag)
             if (publish && !kTagged)
-                st_release_u64(tags + (chain * 2 + ((c + 1) & 1)) * kN + nrow, ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
+                st_release_u64(tags + (rchain * 2 + ((c + 1) & 1)) * kN + nrow, ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
         }
     }
 #undef BWAIT

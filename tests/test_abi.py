@@ -195,10 +195,11 @@ def test_bounds_checked_build_compiles_and_exports_every_symbol():
 def test_debug_knobs_validate_and_restore(lib):
     """The launch-configuration test hooks take -1 (the library's choice) or a valid value, and reject the rest
     without changing anything."""
-    assert lib.ssd_debug_knobs(-1, -1, -1, -1) == 0
-    for bad in [(0, -1, -1, -1), (9, -1, -1, -1), (-1, 2, -1, -1), (-1, -1, -2, -1), (-1, -1, -1, 5)]:
+    assert lib.ssd_debug_knobs(-1, -1, -1, -1, -1) == 0
+    for bad in [(0, -1, -1, -1, -1), (9, -1, -1, -1, -1), (-1, 2, -1, -1, -1), (-1, -1, -2, -1, -1),
+                (-1, -1, -1, 5, -1), (-1, -1, -1, -1, -2)]:
         assert lib.ssd_debug_knobs(*bad) == 1, bad
-    assert lib.ssd_debug_knobs(8, 1, 0, 0) == 0
+    assert lib.ssd_debug_knobs(8, 1, 0, 0, 4) == 0
     m.debug_knobs()  # restore
     with pytest.raises(m.SsdError):
         m.debug_knobs(tc_heads_per_unit=0)
@@ -211,3 +212,40 @@ def test_library_sources_read_no_environment():
     for fn in os.listdir(csrc):
         src = open(os.path.join(csrc, fn)).read()
         assert "getenv" not in src, fn
+
+
+def test_segment_knob_sizes_the_workspace(lib):
+    """Two-level state passing (forced through the test hook) adds the segment entering states, the block
+    aggregates and one state ring per segment to the workspace; a segment as long as the sequence changes nothing."""
+    p = prob(batch=2, seqlen=4096, nheads=8, ngroups=2)  # 32 chunks per sequence
+    base = m.workspace_size(p)
+    try:
+        m.debug_knobs(tc_segment_chunks=32)
+        assert m.workspace_size(p) == base
+        m.debug_knobs(tc_segment_chunks=8)  # 4 segments
+        seg = m.workspace_size(p)
+    finally:
+        m.debug_knobs()
+    state = 64 * 128 * 4
+    entering = 2 * 3 * 8 * state           # sequences x (segments - 1) x heads
+    assert seg >= base + entering + 2 * 3 * 8 * state  # at least one aggregate block per segment boundary
+    assert m.workspace_size(p) == base
+
+
+def test_plan_query_reports_kernel_launches_and_segments(lib):
+    """ssd_fwd_plan: the kernel, the launches of one call (three with two-level state passing: block aggregates,
+    their combination, the fused kernel) and the segments, consistent with ssd_fwd_workspace_size."""
+    p = prob(batch=2, seqlen=4096, nheads=8, ngroups=2)  # 32 chunks
+    info = m.plan_info(p)
+    assert info["kernel"] == "tc" and info["segments"] == 1 and info["launches"] == 1
+    assert info["segment_chunks"] == 32 and info["workspace_bytes"] == m.workspace_size(p)
+    try:
+        m.debug_knobs(tc_segment_chunks=5)  # 32 chunks: 7 segments, the last of 2 chunks
+        info = m.plan_info(p)
+        assert info["segments"] == 7 and info["segment_chunks"] == 5 and info["launches"] == 3
+        assert info["workspace_bytes"] == m.workspace_size(p)
+    finally:
+        m.debug_knobs()
+    assert m.plan_info(prob(seqlen=1))["kernel"] == "step"
+    assert m.plan_info(prob(seqlen=0, kernel="tc"))["launches"] == 0
+    assert m.plan_info(prob(io_dtype=torch.float32, dstate=64))["kernel"] == "simt"

@@ -8,7 +8,7 @@ import torch
 
 import mamba_ssd_prefill_gb300 as m
 import oracle
-from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_inputs
+from mamba_ssd_prefill_gb300.inputs import DTYPES, WORKLOADS, make_conv_inputs, make_inputs
 from parity import gate_final, gate_y, gate_y_tc_envelope
 
 pytestmark = pytest.mark.gpu
@@ -240,6 +240,71 @@ def test_tc_ticket_order(late, hs, knobs):
     knobs(tc_late_ticket=1 if late == "0" else 0)
     y2, f2 = run_gpu(w, inp, kernel="tc")
     assert torch.equal(y, y2) and torch.equal(fin, f2)
+
+
+SEGMENTS = [
+    # (workload, overrides, chunks per segment): two-level state passing forced through the test hook
+    ("m130-bf16", dict(batch=2, seqlen=2000, nheads=8, ngroups=2), 3),                 # 16 chunks: 6 segments, ragged
+    ("m130-bf16", dict(batch=1, seqlen=4096, nheads=16, ngroups=2, io="f16", state="f16"), 8),
+    ("m130-bf16", dict(batch=3, seqlen=1500, nheads=10, ngroups=2), 2),                # 5 heads per unit (odd)
+    ("m130-bf16", dict(batch=2, seqlen=1024, nheads=4, state="f16"), 1),               # every chunk a segment
+    ("long-L256k-g8", dict(seqlen=16384, nheads=16), 32),                              # 8 groups, fp32, no init
+    ("m130-bf16", dict(batch=1, seqlen=3000, nheads=24, init="none", dt_lo=1e-4), 5),  # slow decay, no init
+]
+
+
+@pytest.mark.parametrize("name,over,seg", SEGMENTS, ids=[f"seg{i}" for i in range(len(SEGMENTS))])
+def test_tc_segmented_state_passing(name, over, seg, knobs):
+    """Two-level state passing: block aggregates and segment entering states computed before the fused kernel,
+    whose state chain then restarts at every segment start. Against the oracle, and against the one-chain run."""
+    w = WORKLOADS[name].with_(**over)
+    inp = make_inputs(w, device="cuda")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    knobs(tc_segment_chunks=seg)
+    y, fin = run_gpu(w, inp, kernel="tc")
+    assert_parity(w, y, fin, yr, fr, f"tc segments of {seg} {name} {over}", kernel="tc")
+    knobs(tc_segment_chunks=0)
+    y1, f1 = run_gpu(w, inp, kernel="tc")
+    d = (y.double() - y1.double()).abs().max().item()
+    assert d <= 1e-2 + 2e-2 * y1.double().abs().max().item(), d
+
+
+@pytest.mark.parametrize("late", [0, 1], ids=["early-tickets", "late-tickets"])
+@pytest.mark.parametrize("hs", [1, 4])
+def test_tc_segments_with_tickets_and_heads(late, hs, knobs):
+    """Segments together with every ticket order and head count: bit for bit the same across ticket orders."""
+    knobs(tc_segment_chunks=4, tc_late_ticket=late, tc_heads_per_unit=hs)
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=2600, nheads=8, seed=90 + hs)
+    inp = make_inputs(w, device="cuda")
+    y, fin = run_gpu(w, inp, kernel="tc")
+    yr, fr = oracle.ssd_reference(**cpu(inp))
+    assert_parity(w, y, fin, yr, fr, f"tc segments late={late} hs={hs}", kernel="tc")
+    knobs(tc_late_ticket=1 - late)
+    y2, f2 = run_gpu(w, inp, kernel="tc")
+    assert torch.equal(y, y2) and torch.equal(fin, f2)
+
+
+@pytest.mark.parametrize("fuse", [True, False], ids=["fused-conv", "conv-then-ssd"])
+def test_tc_segments_repeat_and_conv_paths(fuse, knobs):
+    """Repeated segmented launches on one workspace are bit-identical. With the convolution in front, the unfused
+    path (convolved rows written first) runs segmented and the fused path (raw rows convolved as they load) keeps
+    one chain per sequence under the same setting; both match the oracle."""
+    knobs(tc_segment_chunks=2)
+    w = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=1300, nheads=8, ngroups=2)
+    inp = make_inputs(w, device="cuda")
+    ws = m.Workspace("cuda")
+    y0, f0 = run_gpu(w, inp, kernel="tc", ws=ws)
+    for _ in range(2):
+        y1, f1 = run_gpu(w, inp, kernel="tc", ws=ws)
+        assert torch.equal(y0, y1) and torch.equal(f0, f1)
+    ci = make_conv_inputs(w, 4, device="cuda", seed=62)
+    y, fin, cs, xo = m.ssd_fwd_conv(**ci, nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate,
+                                    activation="silu", chunk_size=w.chunk, state_dtype=DTYPES[w.state], kernel="tc",
+                                    workspace=ws, fuse=fuse)
+    m.check(ws)
+    assert (xo is None) == fuse
+    yr, fr, _ = conv_reference(w, ci, 4, "silu")
+    assert_parity(w, y, fin, yr, fr, f"conv fuse={fuse} with segments set", kernel="tc")
 
 
 def test_tc_no_D_alias_and_determinism():

@@ -50,14 +50,40 @@ def test_static_scratch_matches_workspace_entry_point_twice():
     not cleared), then the small one after the larger (stale contents past its own footprint)."""
     small = WORKLOADS["m130-bf16"].with_(batch=2, seqlen=1000, nheads=8, seed=71)
     large = WORKLOADS["m130-bf16"].with_(batch=4, seqlen=2048, nheads=24, state="f16", seed=72)
-    for w in (small, large, large, small):
-        inp = make_inputs(w, device="cuda")
+    try:
+        # one state chain per sequence in both entry points (two-level state passing would not fit the array
+        # for the larger problem; the static entry point then runs without it, tested below)
+        m.debug_knobs(tc_segment_chunks=0)
+        for w in (small, large, large, small):
+            inp = make_inputs(w, device="cuda")
+            y_s, f_s = _call_static(w, inp)
+            ws = m.Workspace("cuda")
+            y_w, f_w = m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], workspace=ws)
+            m.check(ws)
+            assert torch.equal(y_s, y_w), w
+            assert torch.equal(f_s, f_w), w
+    finally:
+        m.debug_knobs()
+
+
+def test_static_scratch_without_room_for_segments():
+    """Where the plan would cut the sequences into segments whose buffers do not fit the static array, the static
+    entry point runs with one chain per sequence: the same result as the workspace entry point with segments off."""
+    w = WORKLOADS["m130-bf16"].with_(batch=4, seqlen=2048, nheads=24, state="f16", seed=73)
+    inp = make_inputs(w, device="cuda")
+    try:
+        m.debug_knobs(tc_segment_chunks=2)  # 8 segments per sequence: 8 x the state ring
+        prob = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io],
+                              DTYPES[w.state])
+        assert m.workspace_size(prob) > 16 << 20
         y_s, f_s = _call_static(w, inp)
+        m.debug_knobs(tc_segment_chunks=0)
         ws = m.Workspace("cuda")
         y_w, f_w = m.ssd_fwd(**inp, chunk_size=w.chunk, state_dtype=DTYPES[w.state], workspace=ws)
         m.check(ws)
-        assert torch.equal(y_s, y_w), w
-        assert torch.equal(f_s, f_w), w
+    finally:
+        m.debug_knobs()
+    assert torch.equal(y_s, y_w) and torch.equal(f_s, f_w)
 
 
 def test_static_scratch_rejects_problems_over_the_limit():
