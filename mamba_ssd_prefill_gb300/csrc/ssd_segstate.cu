@@ -18,12 +18,12 @@
 //   warp 0       TMA: per chunk the B tile (two 64-column halves), per head the x tile into an 8-deep ring
 //   warp 1       TMEM allocator + single-thread tcgen05.mma issuer (M = 128 d_state rows, N = 64, K = 128 tokens)
 //   warps 2, 3   B tile halves bf16 -> fp16 in place (fp16 inputs pass straight through)
-//   warps 4-7    weight tables: warp 4 + (head mod 4) walks its heads' chunks in order, with dt, the chunk cumsum
-//                (4 tokens a lane) and the running later-chunk decay, into its own double-buffered table; at the
-//                unit end the block decays
-//   warps 8-11   X' = w o x to fp16 in place in the x slot (the MMA's B operand there) for the items of even
-//                index, 12-15 for the odd ones; at the unit end the accumulators of the even (8-11) and odd
-//                (12-15) heads to global memory
+//   warps 4-7    weight tables, item j by warp 4 + (j mod 4): dt, the chunk cumsum (4 tokens a lane), the
+//                within-chunk weights exp(cs_end - cs_t) dt_t and the chunk's summed dt A, into a ring of its own
+//   warps 8-11   X' = exp(after) w o x to fp16 in place in the x slot (the MMA's B operand there) for the heads of
+//                even index, 12-15 for the odd ones (hs is even, so a warpgroup sees every chunk of its heads, in
+//                order, and keeps their running `after`); at the unit end these heads' accumulators and block
+//                decays to global memory
 // Combine kernel (SIMT): per sequence, head and state element, S <- exp(L_k) S + s_blk_k from the initial state
 // over the blocks, storing S at each segment start.
 #include <cuda.h>
@@ -50,7 +50,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct __align__(1024) SmemB {
     uint8_t b[2][2][kTile];   // per chunk stage: B n[0,64), B n[64,128)
     uint8_t x[kXR][kTile];    // per (chunk, head) item: the x tile, then X' in its place
-    float wt[4][kTB][kQ];     // per weight-table warp, a ring of kTB: an item's weights w_t
+    float wt[4][kTB][kQ];     // per weight-table warp, a ring of kTB: an item's within-chunk weights
+    float tot[4][kTB];        // beside each table: the chunk's summed dt A (log2 units)
     uint64_t b_full[2], b_conv[2], b_empty[2], x_full[kXR], x_conv[kXR], x_empty[kXR];
     uint64_t t_full[4][kTB], t_empty[4][kTB];
     uint64_t acc_full, acc_empty, drain;
@@ -58,7 +59,8 @@ struct __align__(1024) SmemB {
     int32_t abort;
 };
 static_assert(offsetof(SmemB, x) % 1024 == 0 && offsetof(SmemB, wt) % 16 == 0, "swizzled tiles are 1024-aligned");
-static_assert(kXR % 2 == 0, "X' warpgroup w fills the slots of parity w");
+static_assert(kXR == 8, "a chunk's items fill consecutive slots for every hs in {2, 4, 8}; X' warpgroup w fills "
+                         "the slots of parity w");
 static_assert(sizeof(SmemB) + 1024 <= 227 * 1024, "shared memory of one CTA");
 
 __device__ __forceinline__ float ex2f(float v) {
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true);
+            constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true) & ~(0x3Fu << 17);  // N set per MMA
             uint32_t bc = 0, uc = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x, ++uc) {
@@ -279,24 +281,32 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                         break;
                     }
                     STRACE(1, 4, bc);
-                    tc_fence_after();
-                    const uint64_t dbt = desc_sw128(smem_u32(sm.b[st][0]), kTile, 1024);
-                    for (int hh = 0; hh < hs; ++hh) {
-                        const uint32_t j = bc * (uint32_t)hs + (uint32_t)hh;  // item index in this CTA
-                        const uint32_t k = j % kXR;
-                        if (!WAIT1(&sm.x_conv[k], (j / kXR) & 1)) {
-                            ok = false;
-                            break;
-                        }
-                        STRACE(1, 5, j);
-                        tc_fence_after();
-                        const uint64_t dxs = desc_sw128(smem_u32(sm.x[k]), 8192, 1024);
-#pragma unroll 1
-                        for (uint32_t s = 0; s < 8; ++s)  // K step s: 16 tokens = 2048 bytes further
-                            mma_ss(tmem + 64 * hh, dbt + 128 * s, dxs + 128 * s, idST, ci > 0 || s > 0);
-                        mma_commit(&sm.x_empty[k]);
-                        STRACE(1, 2, j);
+                    // every item of the chunk first, then all their MMAs in one burst: one thread issues every MMA,
+                    // and any wait or bookkeeping between two MMAs leaves the tensor pipe idle (it takes about 50
+                    // cycles for one)
+                    const uint32_t j0 = bc * (uint32_t)hs;  // first item of the chunk in this CTA
+                    for (int hh = 0; hh < hs && ok; ++hh)
+                        if (!WAIT1(&sm.x_conv[(j0 + hh) % kXR], ((j0 + hh) / kXR) & 1)) ok = false;
+                    if (!ok) break;
+                    STRACE(1, 5, j0);
+                    uint64_t da[8];
+#pragma unroll
+                    for (uint32_t s = 0; s < 8; ++s) da[s] = desc_sw128(smem_u32(sm.b[st][0]), kTile, 1024) + 128 * s;
+                    // up to four heads per MMA: their X' tiles sit in consecutive slots (a chunk's items start on a
+                    // multiple of hs, and hs divides the ring), the slot stride is the B operand's stride between
+                    // 64-column atoms, and their accumulators are adjacent in TMEM (N = 64 per head)
+                    for (int g = 0; g < hs; g += 4) {
+                        const int nh = hs - g < 4 ? hs - g : 4;
+                        const uint32_t id = idST | ((uint32_t)(64 * nh) >> 3 << 17);
+                        const uint64_t dxs = desc_sw128(smem_u32(sm.x[(j0 + g) % kXR]), kTile, 1024);
+                        const uint32_t d = tmem + 64 * g;
+                        // K step s: 16 tokens = 2048 bytes further
+                        mma_ss(d, da[0], dxs, id, ci > 0);
+#pragma unroll
+                        for (uint32_t s = 1; s < 8; ++s) mma_ss(d, da[s], dxs + 128 * s, id, 1);
                     }
+                    for (int hh = 0; hh < hs; ++hh) mma_commit(&sm.x_empty[(j0 + hh) % kXR]);
+                    STRACE(1, 2, j0);
                     mma_commit(&sm.b_empty[st]);
                 }
                 mma_commit(&sm.acc_full);
@@ -353,81 +363,65 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         __syncwarp();
     } else if (warp < 8) {
-        // ------------------------------------------------------------ weight tables (warp 4 + head mod 4)
+        // ------------------------------------------------------------ weight tables (item j: warp 4 + j mod 4)
         // Per item (chunk ci of the block, walked from the last, head hh): dt = softplus(dt_raw + dt_bias), lane l
         // holding tokens 4 l .. 4 l + 3; cs = chunk-local inclusive cumsum of dt A (log2 units); the weights
-        // w_t = exp2(after + cs_end - cs_t) dt_t into the item's slot table; then after += cs_end.
+        // exp2(cs_end - cs_t) dt_t and the total cs_end into the warp's ring slot r mod kTB, r = j / 4.
         const int tw = warp - 4;
         const IO *dtr = static_cast<const IO *>(p.dt_raw);
-        uint32_t r = 0;  // this warp's items so far
+        uint32_t xc = 0;  // items before this unit (the unit's items are xc .. xc + blk hs - 1)
         bool ok = true;
+        const int64_t nitems = blk * hs;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
             const Unit un = unit_of(p, sp, u);
-            float bias[2], Al[2], after[2];  // this warp's heads tw and tw + 4
+            // lane hh < hs holds head hh's dt_bias and A log2(e) (broadcast per item by shuffles)
+            const float lb = lane < hs ? p.dt_bias[un.h0 + lane] : 0.f;
+            const float la = lane < hs ? p.A[un.h0 + lane] * kLog2e : 0.f;
+            auto load_raw = [&](int64_t jj, float (&r)[4]) {  // dt_raw of this lane's 4 tokens for local item jj
+                const int64_t c = un.k * blk + blk - 1 - jj / hs, hh = jj % hs;
+                const int64_t row = un.s * p.L + c * kQ + 4 * lane;
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int hh = tw + 4 * m;
-                bias[m] = hh < hs ? p.dt_bias[un.h0 + hh] : 0.f;
-                Al[m] = hh < hs ? p.A[un.h0 + hh] * kLog2e : 0.f;
-                after[m] = 0.f;
-            }
-            // dt_raw of this lane's 4 tokens for the warp's heads, one chunk ahead
-            auto load_raw = [&](int64_t ci, float (&r)[2][4]) {
-                const int64_t row = un.s * p.L + (un.k * blk + blk - 1 - ci) * kQ + 4 * lane;
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        r[m][jj] = tw + 4 * m < hs ? to_f32(*chk(dtr, (row + jj) * p.H + un.h0 + tw + 4 * m, 1,
-                                                                 p.batch * p.L * p.H, hdr, SITE_SEG_DT))
-                                                   : 0.f;
+                for (int e = 0; e < 4; ++e)
+                    r[e] = jj < nitems ? to_f32(*chk(dtr, (row + e) * p.H + un.h0 + hh, 1, p.batch * p.L * p.H, hdr,
+                                                     SITE_SEG_DT))
+                                       : 0.f;
             };
-            float rawc[2][4], rawn[2][4] = {};
-            load_raw(0, rawc);
-            for (int64_t ci = 0; ci < blk; ++ci) {
-                if (ci + 1 < blk) load_raw(ci + 1, rawn);
+            int64_t jj = (int64_t)((tw - (int)(xc & 3u)) & 3);  // this warp's first local item in the unit
+            float raw[4], nxt[4];
+            load_raw(jj, raw);
+            for (; jj < nitems; jj += 4) {
+                load_raw(jj + 4, nxt);  // one item ahead
+                const uint32_t j = xc + (uint32_t)jj, r = j >> 2;
+                const int hh = (int)(jj % hs);
+                const float bias = __shfl_sync(0xffffffffu, lb, hh), Al = __shfl_sync(0xffffffffu, la, hh);
+                float dt[4], cum[4];
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int hh = tw + 4 * m;
-                    if (hh >= hs) break;
-                    const float *raw = rawc[m];
-                    float dt[4], cum[4];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        dt[jj] = softplus_f32(raw[jj] + bias[m]);
-                        cum[jj] = fmaf(dt[jj], Al[m], jj ? cum[jj - 1] : 0.f);
-                    }
-                    float incl = cum[3];
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float t = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += t;
-                    }
-                    const float excl = incl - cum[3];
-                    const float end = __shfl_sync(0xffffffffu, incl, 31);
-                    const float base = after[m] + end - excl;
-                    const float4 wv = make_float4(ex2f(base - cum[0]) * dt[0], ex2f(base - cum[1]) * dt[1],
-                                                  ex2f(base - cum[2]) * dt[2], ex2f(base - cum[3]) * dt[3]);
-                    if (lane == 0) STRACE(warp, 1, r);
-                    if (ok && !WAITW(&sm.t_empty[tw][r % kTB], ((r / kTB) & 1) ^ 1)) ok = false;  // buffer read
-                    if (lane == 0) STRACE(warp, 2, r);
-                    *reinterpret_cast<float4 *>(&sm.wt[tw][r % kTB][4 * lane]) = wv;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.t_full[tw][r % kTB]);
-                    after[m] += end;
-                    ++r;
+                for (int e = 0; e < 4; ++e) {
+                    dt[e] = softplus_f32(raw[e] + bias);
+                    cum[e] = fmaf(dt[e], Al, e ? cum[e - 1] : 0.f);
                 }
+                float incl = cum[3];
 #pragma unroll
-                for (int m = 0; m < 2; ++m)
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                const float excl = incl - cum[3];
+                const float end = __shfl_sync(0xffffffffu, incl, 31);
+                const float base = end - excl;
+                const float4 wv = make_float4(ex2f(base - cum[0]) * dt[0], ex2f(base - cum[1]) * dt[1],
+                                              ex2f(base - cum[2]) * dt[2], ex2f(base - cum[3]) * dt[3]);
+                if (lane == 0) STRACE(warp, 1, r);
+                if (ok && !WAITW(&sm.t_empty[tw][r % kTB], ((r / kTB) & 1) ^ 1)) ok = false;  // slot read
+                if (lane == 0) STRACE(warp, 2, r);
+                *reinterpret_cast<float4 *>(&sm.wt[tw][r % kTB][4 * lane]) = wv;
+                if (lane == 0) sm.tot[tw][r % kTB] = end;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.t_full[tw][r % kTB]);
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) rawc[m][jj] = rawn[m][jj];
+                for (int e = 0; e < 4; ++e) raw[e] = nxt[e];
             }
-            if (lane == 0) {  // the block decays of this warp's heads
-                const int64_t base = (un.s * sp.nblk + un.k) * p.H + un.h0;
-                for (int m = 0; m < 2; ++m)
-                    if (tw + 4 * m < hs)
-                        *chk(sp.blk_L, base + tw + 4 * m, 1, p.nseq * sp.nblk * p.H, hdr, SITE_SEG_DECAY) = after[m];
-            }
+            xc += (uint32_t)nitems;
         }
     } else {
         // ------------------------------------------------------------ X' warpgroups (w = 0: even items, 1: odd)
@@ -436,21 +430,26 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         const int w = (warp - 8) >> 2;
         const int i = tid - 256 - 128 * w;  // token row of the chunk, and TMEM lane (d_state row) in the epilogue
         const uint32_t lrow = (uint32_t)(32 * (warp & 3)) << 16;
-        const int nmine = (hs - w + 1) / 2;  // heads of this warpgroup in the epilogue (0 when hs == 1 and w == 1)
+        const int nmine = hs / 2;  // heads w, w + 2, ... of every unit (hs is even)
         uint32_t xc = 0, uc = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
             const Unit un = unit_of(p, sp, u);
-            for (uint32_t xj = xc + ((xc & 1u) ^ (uint32_t)w); xj < xc + (uint32_t)(blk * hs); xj += 2) {
+            float after[4] = {0.f, 0.f, 0.f, 0.f};  // per own head: summed dt A (log2) of the chunks already done
+            for (uint32_t xj = xc + (uint32_t)w; xj < xc + (uint32_t)(blk * hs); xj += 2) {
                 const uint32_t xk = xj % kXR;
-                // the item's table: warp t = head mod 4, its r-th item (heads t, t + 4 of every earlier chunk)
-                const uint32_t hh = xj % (uint32_t)hs, t = hh & 3;
-                const uint32_t r = (xj / (uint32_t)hs) * (uint32_t)((hs - (int)t + 3) / 4) + (hh >> 2);
+                const uint32_t t = xj & 3, r = xj >> 2;  // the item's table: warp t, its r-th item
+                const int m = (int)((xj - xc) % (uint32_t)hs) >> 1;  // this warpgroup's head index
                 if (lane == 0) STRACE(warp, 2, xj);
                 if (ok && !WAITW(&sm.x_full[xk], (xj / kXR) & 1)) ok = false;
                 if (ok && !WAITW(&sm.t_full[t][r % kTB], (r / kTB) & 1)) ok = false;
                 if (lane == 0) STRACE(warp, 3, xj);
-                const float wt = sm.wt[t][r % kTB][i];
+                float am = after[0];
+#pragma unroll
+                for (int e = 1; e < 4; ++e) am = m == e ? after[e] : am;
+                const float wt = sm.wt[t][r % kTB][i] * ex2f(am), end = sm.tot[t][r % kTB];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) after[e] += m == e ? end : 0.f;
                 uint8_t *xr = sm.x[xk] + i * 128;
                 // X' in place (same 16-byte positions: the swizzle carries over); the 8 chunks of the row are read
                 // first, in an order rotated by the row so that the 8 threads of a quarter-warp hit 8 bank groups
@@ -483,6 +482,12 @@ __global__ void __launch_bounds__(kThreadsB, 1)
                 const int hh = w + 2 * m;
                 float *dst = chk(sp.blk_s, (base + un.h0 + hh) * (int64_t)(kP * kN) + i, (kP - 1) * kN + 1,
                                  p.nseq * sp.nblk * p.H * kP * kN, hdr, SITE_SEG_BLK);
+                if (i == 0) {  // the block decay of this head
+                    float am = after[0];
+#pragma unroll
+                    for (int e = 1; e < 4; ++e) am = m == e ? after[e] : am;
+                    *chk(sp.blk_L, base + un.h0 + hh, 1, p.nseq * sp.nblk * p.H, hdr, SITE_SEG_DECAY) = am;
+                }
 #pragma unroll 1
                 for (int pc = 0; pc < 4; ++pc) {
                     uint32_t r[16];
@@ -593,9 +598,10 @@ cudaError_t launch_blocks(const Params &p, const SegPlan &sp, int sms, cudaStrea
 // 2.7B-shaped 256K-token sequence: 8 segments beat 4 and 16). A block holds at least min(segment, 8) chunks, so
 // that its
 // aggregate (32 KB a head) costs at most a quarter of the x it reads; among such blocks and the head counts per
-// unit (divisors of the heads per group, at most 8, and not 1 where the groups have more heads: the block kernel
-// gives alternate heads to its two warpgroups), the first pair, by more heads then longer blocks, that gives every
-// SM two block units, else the pair with the most units.
+// unit (2, 4 or 8 dividing the heads per group: a chunk's heads then fill consecutive ring slots and share MMAs
+// of up to N = 256, and each X' warpgroup owns half of them; groups of an odd number of heads keep one chain per
+// sequence), the first pair, by more heads then longer blocks, that gives every SM two block units, else the pair
+// with the most units.
 SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced) {
     SegChoice r{1, nc, 0, 0, 1};
     if (nseq < 1 || nc < 2 || sms < 1) return r;
@@ -617,8 +623,9 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
     const int64_t hpg = H / G, min_blk = std::min<int64_t>(seg, 8);
     int64_t best_units = -1;
     bool found = false;
-    for (int hs = 8; hs >= 1 && !found; --hs) {
-        if (hpg % hs || (hs == 1 && hpg > 1)) continue;
+    if (hpg % 2) return SegChoice{1, nc, 0, 0, 1};  // the block kernel takes an even number of heads
+    for (int hs = 8; hs >= 2 && !found; hs /= 2) {
+        if (hpg % hs) continue;
         for (int64_t blk = std::min<int64_t>(32, seg); blk >= min_blk; --blk) {
             if (seg % blk) continue;
             const int64_t units = nseq * (r.nseg - 1) * (seg / blk) * (H / hs);
@@ -645,8 +652,8 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
 
 cudaError_t launch_segstate(const Params &p, const SegPlan &sp, int io_dtype, int state_dtype, int sms,
                             cudaStream_t stream) {
-    if (p.nseg < 2 || sp.nblk < 1 || sp.hs < 1 || sp.hs > 8 || p.H % sp.hs || p.heads_per_group % sp.hs ||
-        p.seg_chunks % sp.blk)
+    if (p.nseg < 2 || sp.nblk < 1 || (sp.hs != 2 && sp.hs != 4 && sp.hs != 8) || p.H % sp.hs ||
+        p.heads_per_group % sp.hs || p.seg_chunks % sp.blk)
         return cudaErrorInvalidValue;
     cudaError_t e = io_dtype == 1 ? launch_blocks<__nv_bfloat16>(p, sp, sms, stream)
                                   : launch_blocks<__half>(p, sp, sms, stream);
