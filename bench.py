@@ -268,6 +268,8 @@ def run_gpu(args, w):
 
     world, rank, local = dist_setup()
     torch.cuda.set_device(local)
+    if args.segment_chunks != -1:
+        m.debug_knobs(tc_segment_chunks=args.segment_chunks)
     dev = torch.device("cuda", local)
     st = DTYPES[w.state]
     inp = make_inputs(w, device=dev, seed=w.seed + rank)
@@ -393,6 +395,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--segment-chunks", type=int, default=-1,
+                    help="two-level state passing: chunks per segment (0: one chain per sequence; default: the "
+                         "library's choice); for profiling the segment kernels on reduced workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

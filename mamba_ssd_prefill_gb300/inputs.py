@@ -59,6 +59,9 @@ WORKLOADS = {
     "m2p7-L8k-b32": Workload("m2p7-L8k-b32", 32, 8192, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal", seed=1004),
     "long-L256k-g8": Workload("long-L256k-g8", 1, 262144, 80, 64, 128, 8, 128, io="bf16", state="f32", init="none",
                               dt_lo=1e-4, seed=1005),
+    # the long-context layer at 1/8 of its length (profiling captures: 0.8 GB of inputs and outputs)
+    "long-L32k-g8": Workload("long-L32k-g8", 1, 32768, 80, 64, 128, 8, 128, io="bf16", state="f32", init="none",
+                             dt_lo=1e-4, seed=1005),
     # the fp16-state variants of the fp32-state workloads above (states passed and returned in fp16)
     "long-L256k-g8-f16": Workload("long-L256k-g8-f16", 1, 262144, 80, 64, 128, 8, 128, io="bf16", state="f16",
                                   init="none", dt_lo=1e-4, seed=1005),
