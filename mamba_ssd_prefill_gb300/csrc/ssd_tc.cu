@@ -84,7 +84,8 @@ struct __align__(1024) Smem {
     uint8_t x[3][kTile];      // per head slot: x tile (fp16 after conversion), then S_in (fp16, C.S operand),
                               // then the head's staged y
     uint8_t xs[2][kTile];     // per head buffer: X_s
-    HeadTab tab[3];           // tables of the head in the x slot of the same index
+    HeadTab tab[4];           // head h's tables in slot h mod 4 (one more than the x slots: the x loader fills
+                              // a head's table while it still waits for the head's x slot)
     ConvStage<CONV> cv;
     Sched sched[2];
     uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty, unit_go;
@@ -593,12 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u_D = own && p.D ? p.D[sc.h0 + lane] : 0.f;
             for (int hh = 0; hh < nh; ++hh, ++hc) {
                 const uint32_t k = hc % 3, n = hc / 3;
-                if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
-                    done = true;
-                    break;
-                }
-                HeadTab &tb = sm.tab[k];
+                HeadTab &tb = sm.tab[hc % 4];  // last read by head hc - 4, whose slot's wait passed a head ago
                 if (!sc.valid) {
+                    if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
+                        done = true;
+                        break;
+                    }
                     if (lane == 0) {
                         tb.valid = 0;
                         mbar_arrive(&sm.x_full[k]);
@@ -608,34 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int h = sc.h0 + hh;
-                const bool halo_tma = CONV && sc.c > 0;
-                if (lane == 0) {
-                    TRACE(warp, 1, hc);
-                    mbar_arrive_expect_tx(&sm.x_full[k], kTile + (halo_tma ? 3 * kP * 2 : 0));
-                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, h, sc.row0, 0);
-                    if constexpr (CONV) {
-                        if (halo_tma) tma_load_4d(sm.cv.halo[k], &map_xh, &sm.x_full[k], 0, h, sc.row0 - 3, 0);
-                    }
-                    armed_x |= 1 << k;
-                    x_par[k] = n & 1;
-                }
-                if constexpr (CONV) {  // the head's taps and bias (read as broadcasts), the cache before a sequence
-                    const int64_t ch0 = (int64_t)h * kP;
-                    for (int e = lane; e < kP; e += 32) {
-                        sm.cv.tap[k][e] = *reinterpret_cast<const float4 *>(p.conv_w + (ch0 + e) * 4);
-                        sm.cv.bias[k][e] = p.conv_b ? p.conv_b[ch0 + e] : 0.f;
-                    }
-                    if (sc.c == 0) {
-                        const IO *st = static_cast<const IO *>(p.conv_state);
-                        IO *dst = reinterpret_cast<IO *>(sm.cv.halo[k]);
-                        for (int e = lane; e < 3 * kP; e += 32) {
-                            const int r = e / kP, pc = e % kP;
-                            dst[r * kP + pc] = st ? *chk(st, ((int64_t)sc.s * p.x_ld + ch0 + pc) * 3 + r, 1,
-                                                         p.nseq * p.x_ld * 3, hdr, SITE_CONV_STATE)
-                                                  : from_f32<IO>(0.f);
-                        }
-                    }
-                }
+                // the head's table first, while the x slot may still be in use (its barrier is already in this
+                // head's phase: the phase before completed when head hc - 3's tile landed)
                 float rh[4];  // this head's column of raw (a register select: hh is not a compile-time index)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
@@ -681,9 +656,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tb.dskip = dskip;
                 }
                 __syncwarp();
-                if (lane == 0) {
+                if (!CONV && lane == 0) {
                     mbar_arrive(&sm.x_full[k]);
                     TRACE(warp, 2, hc);
+                }
+                if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
+                    done = true;
+                    break;
+                }
+                const bool halo_tma = CONV && sc.c > 0;
+                if (lane == 0) {
+                    TRACE(warp, 1, hc);
+                    mbar_arrive_expect_tx(&sm.x_full[k], kTile + (halo_tma ? 3 * kP * 2 : 0));
+                    tma_load_4d(sm.x[k], &map_x, &sm.x_full[k], 0, h, sc.row0, 0);
+                    if constexpr (CONV) {
+                        if (halo_tma) tma_load_4d(sm.cv.halo[k], &map_xh, &sm.x_full[k], 0, h, sc.row0 - 3, 0);
+                    }
+                    armed_x |= 1 << k;
+                    x_par[k] = n & 1;
+                }
+                if constexpr (CONV) {  // the head's taps and bias (read as broadcasts), the cache before a sequence
+                    const int64_t ch0 = (int64_t)h * kP;
+                    for (int e = lane; e < kP; e += 32) {
+                        sm.cv.tap[k][e] = *reinterpret_cast<const float4 *>(p.conv_w + (ch0 + e) * 4);
+                        sm.cv.bias[k][e] = p.conv_b ? p.conv_b[ch0 + e] : 0.f;
+                    }
+                    if (sc.c == 0) {
+                        const IO *st = static_cast<const IO *>(p.conv_state);
+                        IO *dst = reinterpret_cast<IO *>(sm.cv.halo[k]);
+                        for (int e = lane; e < 3 * kP; e += 32) {
+                            const int r = e / kP, pc = e % kP;
+                            dst[r * kP + pc] = st ? *chk(st, ((int64_t)sc.s * p.x_ld + ch0 + pc) * 3 + r, 1,
+                                                         p.nseq * p.x_ld * 3, hdr, SITE_CONV_STATE)
+                                                  : from_f32<IO>(0.f);
+                        }
+                    }
+                }
+                if constexpr (CONV) {  // with the convolution the slot's taps and halo are part of what is announced
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&sm.x_full[k]);
+                        TRACE(warp, 2, hc);
+                    }
                 }
             }
         }
@@ -790,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t h2 = 0;; ++h2) {
                 const uint32_t k3 = h2 % 3, n3 = h2 / 3, k = h2 & 1;
                 if (!BWAIT1(&sm.x_full[k3], n3 & 1)) break;
-                const int32_t valid = sm.tab[k3].valid, last_of_unit = sm.tab[k3].hh == hs - 1;
+                const int32_t valid = sm.tab[h2 % 4].valid, last_of_unit = sm.tab[h2 % 4].hh == hs - 1;
                 if (!valid) break;
                 if (!BWAIT1(&sm.sin_full[k], (h2 >> 1) & 1)) break;
                 const uint32_t u = (h2 / (uint32_t)hs) & 1;
@@ -838,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t hc = 0;; ++hc) {
             const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
             if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
-            const HeadTab &tb = sm.tab[k3];
+            const HeadTab &tb = sm.tab[hc % 4];
             if (!tb.valid) break;
             if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) break;  // P slot free: MMA1 of head hc - 2 has completed
             if (tb.hh == 0 && !BWAIT(&sm.cb_full, tb.v & 1)) break;
@@ -913,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!BWAIT(&sm.mma2[k2], n2 & 1)) return false;
             tc_fence_after();
             if (lane == 0) TRACE(warp, 3, hp);
-            const HeadTab &tb = sm.tab[k3];
+            const HeadTab &tb = sm.tab[hp % 4];
             const float ecs = ex2(tb.cs2[i]);
             uint8_t *row = sm.x[k3] + i * 128;  // y row i, staged in the head's x slot (C.S has read S_in there)
             const float2 e2 = make_float2(ecs, ecs);
@@ -969,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const HeadTab &tb = sm.tab[k3];
+            const HeadTab &tb = sm.tab[hc % 4];
             if (!tb.valid) break;
             if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) {  // X_s buffer free: MMA1 of head hc - 2 has completed
                 ok = false;
@@ -1093,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t hc = 0;; ++hc) {
             const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
             if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
-            const HeadTab &tb = sm.tab[k3];
+            const HeadTab &tb = sm.tab[hc % 4];
             if (!tb.valid) break;
             const int64_t chain = (int64_t)tb.s * p.H + tb.h;  // (sequence, head): initial and final states
             const int c = tb.c;
