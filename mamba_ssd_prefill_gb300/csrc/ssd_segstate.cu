@@ -594,8 +594,9 @@ cudaError_t launch_blocks(const Params &p, const SegPlan &sp, int sms, cudaStrea
 // serial state chain of a sequence (about 2.4 us per chunk to chunk hop). Two-level passing costs a block pass
 // over most of x (about 0.9 us per head and chunk on an SM) and two more launches, so it is taken only where the
 // launch is long (at least 256 heads x chunks per SM) and the chain is at least 1.5 times the cadence time;
-// segments are then cut so that a segment's chain takes at most a quarter of the cadence time (measured on the
-// 2.7B-shaped 256K-token sequence: 8 segments beat 4 and 16). A block holds at least min(segment, 8) chunks, so
+// segments are then cut so that a segment's chain takes at most a third of the cadence time (measured on the
+// 2.7B-shaped 256K-token sequence with fp32 states: 6 segments of 342 chunks 4.03 ms, 8 of 256 4.11, 4 of 512
+// 4.25, 16 of 128 4.73). A block holds at least min(segment, 8) chunks, so
 // that its
 // aggregate (32 KB a head) costs at most a quarter of the x it reads; among such blocks and the head counts per
 // unit (2, 4 or 8 dividing the heads per group: a chunk's heads then fill consecutive ring slots and share MMAs
@@ -612,7 +613,7 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
     } else {
         const double per_sm = (double)nseq * (double)nc * (double)H / sms, cadence_us = per_sm * 2.3;
         if (per_sm < 256.0 || (double)nc * 2.4 < 1.5 * cadence_us) return r;
-        const int64_t seg_max = (int64_t)(cadence_us / (4.0 * 2.4));
+        const int64_t seg_max = (int64_t)(cadence_us / (3.0 * 2.4));
         if (seg_max >= nc || seg_max < 4) return r;
         const int64_t nseg0 = (nc + seg_max - 1) / seg_max;
         seg = (nc + nseg0 - 1) / nseg0;
