@@ -144,6 +144,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Warp-collective (all 32 lanes converged): true in exactly one lane, the lowest. An MMA issuer warp runs its
+// loop on every lane, with the operands in warp-uniform values, and issues each MMA and commit from that lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p = 0;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t.reg .b32 l;\n\t"
+        "elect.sync l|P1, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
 // Arrive once on `bar` when every tcgen05 op this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))

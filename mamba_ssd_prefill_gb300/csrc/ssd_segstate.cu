@@ -266,55 +266,64 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform waits) and one elected lane issues the MMAs and commits: a
+        // burst issued this way completes sooner than one lane's.
+        {
             constexpr uint32_t idST = idesc_f16_f32(128, 64, true, true) & ~(0x3Fu << 17);  // N set per MMA
+            const bool leader = elect_one();
             uint32_t bc = 0, uc = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x, ++uc) {
-                if (!WAIT1(&sm.acc_empty, (uc & 1) ^ 1)) break;  // the last unit's accumulators have been read
+                if (!WAITW(&sm.acc_empty, (uc & 1) ^ 1)) break;  // the last unit's accumulators have been read
                 tc_fence_after();
-                STRACE(1, 1, uc);
+                if (lane == 0) STRACE(1, 1, uc);
                 for (int64_t ci = 0; ok && ci < blk; ++ci, ++bc) {
                     const uint32_t st = bc & 1;
-                    if (!WAIT1(&sm.b_conv[st], (bc >> 1) & 1)) {
+                    if (!WAITW(&sm.b_conv[st], (bc >> 1) & 1)) {
                         ok = false;
                         break;
                     }
-                    STRACE(1, 4, bc);
-                    // every item of the chunk first, then all their MMAs in one burst: one thread issues every MMA,
-                    // and any wait or bookkeeping between two MMAs leaves the tensor pipe idle (it takes about 50
-                    // cycles for one)
+                    if (lane == 0) STRACE(1, 4, bc);
+                    // every item of the chunk first, then all their MMAs in one burst: any wait or bookkeeping
+                    // between two MMAs leaves the tensor pipe idle (it takes about 50 cycles for one)
                     const uint32_t j0 = bc * (uint32_t)hs;  // first item of the chunk in this CTA
                     for (int hh = 0; hh < hs && ok; ++hh)
-                        if (!WAIT1(&sm.x_conv[(j0 + hh) % kXR], ((j0 + hh) / kXR) & 1)) ok = false;
+                        if (!WAITW(&sm.x_conv[(j0 + hh) % kXR], ((j0 + hh) / kXR) & 1)) ok = false;
                     if (!ok) break;
-                    STRACE(1, 5, j0);
+                    if (lane == 0) STRACE(1, 5, j0);
+                    tc_fence_after();
                     uint64_t da[8];
 #pragma unroll
                     for (uint32_t s = 0; s < 8; ++s) da[s] = desc_sw128(smem_u32(sm.b[st][0]), kTile, 1024) + 128 * s;
-                    // up to four heads per MMA: their X' tiles sit in consecutive slots (a chunk's items start on a
-                    // multiple of hs, and hs divides the ring), the slot stride is the B operand's stride between
-                    // 64-column atoms, and their accumulators are adjacent in TMEM (N = 64 per head)
-                    for (int g = 0; g < hs; g += 4) {
-                        const int nh = hs - g < 4 ? hs - g : 4;
-                        const uint32_t id = idST | ((uint32_t)(64 * nh) >> 3 << 17);
-                        const uint64_t dxs = desc_sw128(smem_u32(sm.x[(j0 + g) % kXR]), kTile, 1024);
-                        const uint32_t d = tmem + 64 * g;
-                        // K step s: 16 tokens = 2048 bytes further
-                        mma_ss(d, da[0], dxs, id, ci > 0);
+                    if (leader) {
+                        // up to four heads per MMA: their X' tiles sit in consecutive slots (a chunk's items start on
+                        // a multiple of hs, and hs divides the ring), the slot stride is the B operand's stride
+                        // between 64-column atoms, and their accumulators are adjacent in TMEM (N = 64 per head)
+                        for (int g = 0; g < hs; g += 4) {
+                            const int nh = hs - g < 4 ? hs - g : 4;
+                            const uint32_t id = idST | ((uint32_t)(64 * nh) >> 3 << 17);
+                            const uint64_t dxs = desc_sw128(smem_u32(sm.x[(j0 + g) % kXR]), kTile, 1024);
+                            const uint32_t d = tmem + 64 * g;
+                            // K step s: 16 tokens = 2048 bytes further
+                            mma_ss(d, da[0], dxs, id, ci > 0);
 #pragma unroll
-                        for (uint32_t s = 1; s < 8; ++s) mma_ss(d, da[s], dxs + 128 * s, id, 1);
+                            for (uint32_t s = 1; s < 8; ++s) mma_ss(d, da[s], dxs + 128 * s, id, 1);
+                        }
+                        for (int hh = 0; hh < hs; ++hh) mma_commit(&sm.x_empty[(j0 + hh) % kXR]);
+                        mma_commit(&sm.b_empty[st]);
                     }
-                    for (int hh = 0; hh < hs; ++hh) mma_commit(&sm.x_empty[(j0 + hh) % kXR]);
-                    STRACE(1, 2, j0);
-                    mma_commit(&sm.b_empty[st]);
+                    __syncwarp();
+                    if (lane == 0) STRACE(1, 2, j0);
                 }
-                mma_commit(&sm.acc_full);
+                if (leader) mma_commit(&sm.acc_full);
+                __syncwarp();
             }
             // every MMA issued above completes before TMEM is released
-            mma_commit(&sm.drain);
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(&sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+            if (leader) {
+                mma_commit(&sm.drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&sm.drain, 0) && globaltimer() - t0 < 1000000000ull) {
+                }
             }
         }
         __syncwarp();
