@@ -20,9 +20,10 @@
 //   warp 1       TMEM allocator + tcgen05.mma issuer (one elected lane) of C.B^T and of each head's P.x and chunk state
 //   warp 2       x loader: per head one TMA of the x tile into a 3-deep ring, and the head's chunk cumsum tables
 //   warp 3       tcgen05.mma issuer (one elected lane) of each head's C.S
-//   warps 4-7    P: the decay-masked C.B^T of each head, fp16 into TMEM
-//   warps 8-11   X_s = w o x (and x to fp16) before the head's first MMAs; the epilogue after its C.S, staged
-//                in the head's x slot (x is no longer needed then) and sent by TMA stores
+//   warps 4-7    P: the decay-masked C.B^T of each head, fp16 into TMEM; then the head's X_s = w o x (and x to
+//                fp16), both before the head's first MMAs
+//   warps 8-11   epilogue after the head's C.S, staged in the head's x slot (x is no longer needed then) and
+//                sent by TMA stores
 //   warps 12-15  chain: state passing, S_in -> shared memory as the C.S operand, final states
 // All MMA operands are fp16 (bf16 inputs are converted on chip; the contractions
 // with P, X_s and S need fp16's 11-bit significand to hold 1e-2).
@@ -51,7 +52,7 @@ constexpr int kThreads = 512;
 constexpr uint32_t kTile = 16384;  // [128 rows x 128 B] 128B-swizzled 16-bit tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColCB = 0, kColP = 128, kColYI = 256, kColS = 384;
-constexpr uint32_t kBarE = 1;  // named barrier of the X_s / epilogue warpgroup (0 is __syncthreads)
+constexpr uint32_t kBarE = 1;  // named barrier of the P / X_s warpgroup (0 is __syncthreads)
 
 struct Sched {
     int32_t valid, s, c, g, h0, rows, row0, last;  // row0: the chunk's first token on the packed token axis
@@ -89,6 +90,7 @@ struct __align__(1024) Smem {
     ConvStage<CONV> cv;
     Sched sched[2];
     uint64_t sched_full[2], bc_full[2], bc_conv[2], bc_empty[2], cb_full, cb_empty, unit_go;
+    uint64_t tab_full[4];  // head h's table written (slot h mod 4)
     uint64_t x_full[3], x_empty[3], xs_full[2], p_full[2], mma1[2], acc_free[2], sin_full[2], mma2[2], drain[2];
     uint32_t tmem_base;
     int32_t abort;
@@ -408,9 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.mma2[i], 1);
         }
         for (int i = 0; i < 3; ++i) {
-            mbar_init(&sm.x_full[i], 2);   // the TMA's arrive (with its bytes) and the tables' arrive
+            mbar_init(&sm.x_full[i], CONV ? 2 : 1);  // the TMA's arrive (with its bytes); with the convolution
+                                                     // also the arrive after the taps and the halo
             mbar_init(&sm.x_empty[i], 4);  // one lane per epilogue warp, after its y store has read the slot
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.tab_full[i], 1);
         mbar_init(&sm.cb_full, 1);
         mbar_init(&sm.cb_empty, 128);
         mbar_init(&sm.unit_go, 128);
@@ -601,8 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (lane == 0) {
                         tb.valid = 0;
+                        mbar_arrive(&sm.tab_full[hc % 4]);
                         mbar_arrive(&sm.x_full[k]);
-                        mbar_arrive(&sm.x_full[k]);
+                        if (CONV) mbar_arrive(&sm.x_full[k]);
                     }
                     done = true;
                     break;
@@ -655,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tb.dskip = dskip;
                 }
                 __syncwarp();
-                if (!CONV && lane == 0) {
-                    mbar_arrive(&sm.x_full[k]);
+                if (lane == 0) {  // the table's readers that need no x (P, C.S, chain) start from here
+                    mbar_arrive(&sm.tab_full[hc % 4]);
                     TRACE(warp, 2, hc);
                 }
                 if (!BWAIT(&sm.x_empty[k], (n & 1) ^ 1)) {
@@ -693,10 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if constexpr (CONV) {  // with the convolution the slot's taps and halo are part of what is announced
                     __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&sm.x_full[k]);
-                        TRACE(warp, 2, hc);
-                    }
+                    if (lane == 0) mbar_arrive(&sm.x_full[k]);
                 }
             }
         }
@@ -815,8 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
             const bool leader = elect_one();
             for (uint32_t h2 = 0;; ++h2) {
-                const uint32_t k3 = h2 % 3, n3 = h2 / 3, k = h2 & 1;
-                if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+                const uint32_t k3 = h2 % 3, k = h2 & 1;
+                if (!BWAIT(&sm.tab_full[h2 % 4], (h2 / 4) & 1)) break;
                 const int32_t valid = sm.tab[h2 % 4].valid, last_of_unit = sm.tab[h2 % 4].hh == hs - 1;
                 if (!valid) break;
                 if (!BWAIT(&sm.sin_full[k], (h2 >> 1) & 1)) break;
@@ -844,14 +846,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ P warpgroup
-        // P = CB o decay o dt, masked above the diagonal, fp16 into the head's P slot. One 32-column block of CB
+        // ------------------------------------------------------------ P / X_s warpgroup
+        // Per head P, then X_s. P = CB o decay o dt, masked above the diagonal, fp16 into the head's P slot. One 32-column block of CB
         // per step. Blocks above the diagonal block stay zero: they are written once here, and nothing else writes
         // the P columns. Below the diagonal block exp(cs_i - cs_j) = exp(cs_i - cs_a) exp(cs_a - cs_j) with a the
         // block's last row, both factors <= 1 (the semiseparable off-diagonal blocks are low rank). In the
         // diagonal block the first factor is >= 1, so the split is used only while the block's whole decay range
         // keeps it <= 2^100 (warp-uniform test), else exp is taken per element; the mask then clears every column
         // past the row's own (an inf or NaN there included) by bit masks on the packed halves.
+        // X_s = exp(cs_last - cs_j) dt_j x_j (and the x tile to fp16 in place) into the head's X_s buffer, once
+        // the x tile has landed.
         const int q = warp & 3;       // TMEM lane quarter of this warp
         const int i = 32 * q + lane;  // tile row (token within the chunk) owned by this thread
         const uint32_t lrow = (uint32_t)(32 * q) << 16;
@@ -870,10 +874,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dmask[m] = (2 * m <= lane ? 0x0000ffffu : 0u) | (2 * m + 1 <= lane ? 0xffff0000u : 0u);
         for (uint32_t hc = 0;; ++hc) {
             const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
-            if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+            if (!BWAIT(&sm.tab_full[hc % 4], (hc / 4) & 1)) break;  // the head's table (its x tile is not needed)
             const HeadTab &tb = sm.tab[hc % 4];
             if (!tb.valid) break;
-            if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) break;  // P slot free: MMA1 of head hc - 2 has completed
+            if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) break;  // P slot and X_s buffer free: MMA1 of head hc - 2 done
             if (tb.hh == 0 && !BWAIT(&sm.cb_full, tb.v & 1)) break;
             tc_fence_after();
             if (lane == 0) TRACE(warp, 1, hc);
@@ -928,87 +932,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) TRACE(warp, 2, hc);
             if (tb.hh == hs - 1) mbar_arrive(&sm.cb_empty);
             if (tb.hh == (hs > 3 ? hs - 3 : 0)) mbar_arrive(&sm.unit_go);  // late tickets: the next unit
-        }
-    } else if (warp >= 8 && warp < 12) {
-        // ------------------------------------------------------------ X_s / epilogue warpgroup
-        // Per head: X_s = exp(cs_last - cs_j) dt_j x_j (and the x tile to fp16 in place) into the head's X_s
-        // buffer, once MMA1 two heads back has released it; then the epilogue of the head before:
-        // y = y_intra + exp(cs_i) y_inter (D x is in y_intra through P's diagonal), staged in the head's x slot in
-        // the y map's 128B swizzle and sent by one TMA store per warp (32 rows); the store clips rows past the
-        // sequence end.
-        const int q = warp & 3;
-        const int i = 32 * q + lane;
-        const uint32_t lrow = (uint32_t)(32 * q) << 16;
-        if (lane == 0) prefetch_tensormap(&map_y);
-        IO *yg = static_cast<IO *>(p.y);
-        auto epilogue = [&](uint32_t hp) -> bool {
-            const uint32_t k2 = hp & 1, n2 = hp >> 1, k3 = hp % 3;
-            if (!BWAIT(&sm.mma2[k2], n2 & 1)) return false;
-            tc_fence_after();
-            if (lane == 0) TRACE(warp, 3, hp);
-            const HeadTab &tb = sm.tab[hp % 4];
-            const float ecs = ex2(tb.cs2[i]);
-            uint8_t *row = sm.x[k3] + i * 128;  // y row i, staged in the head's x slot (C.S has read S_in there)
-            const float2 e2 = make_float2(ecs, ecs);
-#pragma unroll 1
-            for (int m = 0; m < 4; ++m) {  // columns 16 m .. 16 m + 15: 16-byte chunks 2 m, 2 m + 1 of the row
-                uint32_t a[16], c2[16];
-                tmem_ld16(tmem + lrow + kColYI + 64 * k2 + 16 * m, a);
-                tmem_ld16(tmem + lrow + kColS + 64 * k2 + 16 * m, c2);
-                const int o0 = ((2 * m) ^ (i & 7)) << 4, o1 = ((2 * m + 1) ^ (i & 7)) << 4;
-                tmem_ld_wait();
-                uint32_t o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 y = ffma2(e2, f2(c2[2 * e], c2[2 * e + 1]), f2(a[2 * e], a[2 * e + 1]));
-                    o[e] = pack_io<IO>(y.x, y.y);
-                }
-                sts128(row + o0, make_uint4(o[0], o[1], o[2], o[3]));
-                sts128(row + o1, make_uint4(o[4], o[5], o[6], o[7]));
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.acc_free[k2]);  // y_intra and y_inter of this slot have been read
-            if (lane == 0) TRACE(warp, 5, hp);
-            const int vr = tb.rows - 32 * q, ph = tb.h, prow = tb.row0 + 32 * q;
-            if (vr >= 32) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_4d(&map_y, sm.x[k3] + 32 * q * 128, 0, ph, prow, 0);
-                    bulk_commit();
-                    TRACE(warp, 6, hp);
-                    bulk_wait_read0();  // the store has read the slot
-                    mbar_arrive(&sm.x_empty[k3]);
-                }
-            } else {
-                if (lane < vr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
-                    uint4 *dst = reinterpret_cast<uint4 *>(
-                        chk(yg, ((int64_t)(prow + lane) * p.H + ph) * kP, kP, p.batch * p.L * p.H * kP, hdr, SITE_TC_Y));
-#pragma unroll
-                    for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(row + ((lc ^ (i & 7)) << 4));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.x_empty[k3]);
-            }
-            __syncwarp();
-            if (lane == 0) TRACE(warp, 4, hp);
-            return true;
-        };
-        bool pend = false, ok = true;
-        uint32_t hc = 0;
-        for (;; ++hc) {
-            const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
-            if (!BWAIT(&sm.x_full[k3], n3 & 1)) {
-                ok = false;
-                break;
-            }
-            const HeadTab &tb = sm.tab[hc % 4];
-            if (!tb.valid) break;
-            if (!BWAIT(&sm.mma1[k2], (n2 & 1) ^ 1)) {  // X_s buffer free: MMA1 of head hc - 2 has completed
-                ok = false;
-                break;
-            }
-            if (lane == 0) TRACE(warp, 1, hc);
+            // X_s of the same head (x tile landed; its buffer was released with the P slot, by MMA1 two heads back)
+            if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+            if (lane == 0) TRACE(warp, 6, hc);
             const float xscale = ex2(tb.cs2[kQ - 1] - tb.cs2[i]) * tb.dt[i];
             uint8_t *xr = sm.x[k3] + i * 128;
             uint8_t *sr = sm.xs[k2] + i * 128;
@@ -1078,14 +1004,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&sm.xs_full[k2]);
-            if (lane == 0) TRACE(warp, 2, hc);
-            if (pend && !epilogue(hc - 1)) {
+            if (lane == 0) TRACE(warp, 7, hc);
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ------------------------------------------------------------ epilogue warpgroup
+        // Per head, after its C.S: y = y_intra + exp(cs_i) y_inter (D x is in y_intra through P's diagonal),
+        // staged in the head's x slot in the y map's 128B swizzle and sent by one TMA store per warp (32 rows);
+        // the store clips rows past the sequence end. These warps do nothing else, so that no other phase of a
+        // later head waits behind an epilogue (X_s of head h + 2 once did, and the chain of waits MMA1 -> chain ->
+        // C.S -> epilogue -> X_s paced every head).
+        const int q = warp & 3;
+        const int i = 32 * q + lane;
+        const uint32_t lrow = (uint32_t)(32 * q) << 16;
+        if (lane == 0) prefetch_tensormap(&map_y);
+        IO *yg = static_cast<IO *>(p.y);
+        auto epilogue = [&](uint32_t hp) -> bool {
+            const uint32_t k2 = hp & 1, n2 = hp >> 1, k3 = hp % 3;
+            if (!BWAIT(&sm.mma2[k2], n2 & 1)) return false;
+            tc_fence_after();
+            if (lane == 0) TRACE(warp, 3, hp);
+            const HeadTab &tb = sm.tab[hp % 4];
+            const float ecs = ex2(tb.cs2[i]);
+            uint8_t *row = sm.x[k3] + i * 128;  // y row i, staged in the head's x slot (C.S has read S_in there)
+            const float2 e2 = make_float2(ecs, ecs);
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {  // columns 16 m .. 16 m + 15: 16-byte chunks 2 m, 2 m + 1 of the row
+                uint32_t a[16], c2[16];
+                tmem_ld16(tmem + lrow + kColYI + 64 * k2 + 16 * m, a);
+                tmem_ld16(tmem + lrow + kColS + 64 * k2 + 16 * m, c2);
+                const int o0 = ((2 * m) ^ (i & 7)) << 4, o1 = ((2 * m + 1) ^ (i & 7)) << 4;
+                tmem_ld_wait();
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 y = ffma2(e2, f2(c2[2 * e], c2[2 * e + 1]), f2(a[2 * e], a[2 * e + 1]));
+                    o[e] = pack_io<IO>(y.x, y.y);
+                }
+                sts128(row + o0, make_uint4(o[0], o[1], o[2], o[3]));
+                sts128(row + o1, make_uint4(o[4], o[5], o[6], o[7]));
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.acc_free[k2]);  // y_intra and y_inter of this slot have been read
+            if (lane == 0) TRACE(warp, 5, hp);
+            const int vr = tb.rows - 32 * q, ph = tb.h, prow = tb.row0 + 32 * q;
+            if (vr >= 32) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&map_y, sm.x[k3] + 32 * q * 128, 0, ph, prow, 0);
+                    bulk_commit();
+                    TRACE(warp, 6, hp);
+                    bulk_wait_read0();  // the store has read the slot
+                    mbar_arrive(&sm.x_empty[k3]);
+                }
+            } else {
+                if (lane < vr) {  // ragged last chunk: the valid rows one by one (the next sequence follows)
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        chk(yg, ((int64_t)(prow + lane) * p.H + ph) * kP, kP, p.batch * p.L * p.H * kP, hdr, SITE_TC_Y));
+#pragma unroll
+                    for (int lc = 0; lc < 8; ++lc) dst[lc] = lds128(row + ((lc ^ (i & 7)) << 4));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.x_empty[k3]);
+            }
+            __syncwarp();
+            if (lane == 0) TRACE(warp, 4, hp);
+            return true;
+        };
+        bool ok = true;
+        for (uint32_t hc = 0;; ++hc) {
+            if (!BWAIT(&sm.tab_full[hc % 4], (hc / 4) & 1)) {
                 ok = false;
                 break;
             }
-            pend = true;
+            if (!sm.tab[hc % 4].valid) break;
+            if (!epilogue(hc)) {
+                ok = false;
+                break;
+            }
         }
-        if (ok && pend) epilogue(hc - 1);
+        (void)ok;
         if (lane == 0) bulk_wait0();  // every y store of this warp has completed
         __syncwarp();
     } else if (warp >= 12) {
@@ -1124,8 +1122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
         float S[kP];  // entering state of the current head (fp32)
         for (uint32_t hc = 0;; ++hc) {
-            const uint32_t k3 = hc % 3, n3 = hc / 3, k2 = hc & 1, n2 = hc >> 1;
-            if (!BWAIT(&sm.x_full[k3], n3 & 1)) break;
+            const uint32_t k2 = hc & 1, n2 = hc >> 1;
+            if (!BWAIT(&sm.tab_full[hc % 4], (hc / 4) & 1)) break;  // the head's table (its x tile is not needed)
             const HeadTab &tb = sm.tab[hc % 4];
             if (!tb.valid) break;
             const int64_t chain = (int64_t)tb.s * p.H + tb.h;  // (sequence, head): initial and final states
@@ -1205,7 +1203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // no publish after the last chunk of a sequence or of a segment (the next segment starts from its own
             // entering state)
             const bool publish = !last && c != skip && !(p.nseg > 1 && (c + 1) % p.seg_chunks == 0);
-            uint8_t *srow = sm.x[k3] + nrow * 128;  // the x tile is dead once MMA1 has read it
+            uint8_t *srow = sm.x[hc % 3] + nrow * 128;  // the x tile is dead once MMA1 has read it
             float4 *dst32 = nullptr;
             ulonglong2 *dst16 = nullptr;
             if (publish) {
