@@ -603,10 +603,12 @@ cudaError_t launch_blocks(const Params &p, const SegPlan &sp, int sms, cudaStrea
 // serial state chain of a sequence (about 2.4 us per chunk to chunk hop). Two-level passing costs a block pass
 // over most of x (about 0.9 us per head and chunk on an SM) and two more launches, so it is taken only where the
 // launch is long (at least 256 heads x chunks per SM) and the chain is at least 1.5 times the cadence time;
-// segments are then cut so that a segment's chain takes at most a third of the cadence time (measured on the
-// 2.7B-shaped 256K-token sequence with fp32 states: 6 segments of 342 chunks 4.03 ms, 8 of 256 4.11, 4 of 512
-// 4.25, 16 of 128 4.73). A block holds at least min(segment, 8) chunks, so
-// that its
+// segments are then cut so that a segment's chain takes at most half the cadence time, rounded up to a multiple
+// of 8 chunks (measured on the 2.7B-shaped 256K-token sequence with fp32 states: 4
+// segments of 512 chunks 3.55 ms, 5 of 410 3.70, 6 of 342 3.64, 8 of 256 3.74, 2 of 1024 3.74; the 8K-token
+// batch-1 layer gains 16 % with 8 segments of 8 chunks but the 16K one loses 7 %, so short sequences keep one
+// chain). A segment with no block length in [min(segment, 8), 32] keeps one chain. A block holds at least
+// min(segment, 8) chunks, so that its
 // aggregate (32 KB a head) costs at most a quarter of the x it reads; among such blocks and the head counts per
 // unit (2, 4 or 8 dividing the heads per group: a chunk's heads then fill consecutive ring slots and share MMAs
 // of up to N = 256, and each X' warpgroup owns half of them; groups of an odd number of heads keep one chain per
@@ -622,10 +624,11 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
     } else {
         const double per_sm = (double)nseq * (double)nc * (double)H / sms, cadence_us = per_sm * 2.3;
         if (per_sm < 256.0 || (double)nc * 2.4 < 1.5 * cadence_us) return r;
-        const int64_t seg_max = (int64_t)(cadence_us / (3.0 * 2.4));
-        if (seg_max >= nc || seg_max < 4) return r;
+        const int64_t seg_max = (int64_t)(cadence_us / (2.0 * 2.4));
+        if (seg_max >= nc || seg_max < 8) return r;
         const int64_t nseg0 = (nc + seg_max - 1) / seg_max;
         seg = (nc + nseg0 - 1) / nseg0;
+        seg = (seg + 7) / 8 * 8;  // a multiple of 8: blocks of 8 chunks always divide it
     }
     r.nseg = (nc + seg - 1) / seg;
     if (r.nseg < 2) return SegChoice{1, nc, 0, 0, 1};
@@ -652,10 +655,7 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
             }
         }
     }
-    if (r.blk < 1) {  // no divisor of the segment in [min_blk, 32]: blocks of one chunk
-        r.blk = 1;
-        r.hs = 1;
-    }
+    if (r.blk < 1) return SegChoice{1, nc, 0, 0, 1};  // no divisor of the segment in [min_blk, 32]: one chain
     r.nblk = (r.nseg - 1) * (seg / r.blk);
     return r;
 }

@@ -232,6 +232,21 @@ def test_segment_knob_sizes_the_workspace(lib):
     assert m.workspace_size(p) == base
 
 
+def test_segment_length_without_a_block_length_keeps_one_chain(lib):
+    """A segment length with no block length in [8, 32] dividing it (683, a prime) cannot be cut into block units
+    of whole chunks: the plan keeps one chain per sequence instead of a configuration the block kernel rejects."""
+    p = prob(batch=1, seqlen=262144, nheads=80, ngroups=8)  # 2048 chunks
+    try:
+        m.debug_knobs(tc_segment_chunks=683)
+        info = m.plan_info(p)
+        assert info["segments"] == 1 and info["launches"] == 1 and info["segment_chunks"] == 2048
+        m.debug_knobs(tc_segment_chunks=688)  # a multiple of 8: 3 segments
+        info = m.plan_info(p)
+        assert info["segments"] == 3 and info["segment_chunks"] == 688 and info["launches"] == 3
+    finally:
+        m.debug_knobs()
+
+
 def test_plan_query_reports_kernel_launches_and_segments(lib):
     """ssd_fwd_plan: the kernel, the launches of one call (three with two-level state passing: block aggregates,
     their combination, the fused kernel) and the segments, consistent with ssd_fwd_workspace_size."""
