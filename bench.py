@@ -68,7 +68,7 @@ def algorithmic(w):
 
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("ssd_tc.cu", "ssd_segstate.cu", "sm100_ptx.cuh", "ssd_common.cuh"):
+    for f in ("ssd_tc.cu", "sm100_ptx.cuh", "ssd_common.cuh"):  # the fused kernel's sources
         h.update(open(os.path.join(ROOT, "mamba_ssd_prefill_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
