@@ -209,10 +209,14 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
  *                     when it cuts a sequence into two or more segments.
  *                     It changes the workspace size: set it before
  *                     ssd_fwd_workspace_size.
+ *  tc_head_flags      tensor-core kernel, fp32 states: 0 = every state row
+ *                     published behind its own release flag by its chain
+ *                     thread, 1 = one release flag per head, stored by the C.S
+ *                     warp once all rows are written
  * The values are read by later calls on any host thread (not by calls already
  * queued). The library reads no environment variable. */
 SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
-                                     int32_t conv_tma, int32_t tc_segment_chunks);
+                                     int32_t conv_tma, int32_t tc_segment_chunks, int32_t tc_head_flags);
 
 /* ssd_fwd without a workspace argument, for callers that cannot allocate
  * device memory (no counterpart on the pages; it is a library convenience).

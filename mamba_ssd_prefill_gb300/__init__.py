@@ -80,7 +80,7 @@ def lib():
             L.ssd_fwd_check.restype = ctypes.c_int
             L.ssd_debug_set.argtypes = [vp, ctypes.c_uint64, i64, vp]
             L.ssd_debug_set.restype = ctypes.c_int
-            L.ssd_debug_knobs.argtypes = [ctypes.c_int32] * 5
+            L.ssd_debug_knobs.argtypes = [ctypes.c_int32] * 6
             L.ssd_debug_knobs.restype = ctypes.c_int
             L.ssd_fwd_kernel_for.argtypes = [pp]
             L.ssd_fwd_kernel_for.restype = ctypes.c_int
@@ -392,10 +392,11 @@ def debug_set(workspace, timeout_ns=0, skip_publish=-1, stream=None):
         raise SsdError(st, "ssd_debug_set")
 
 
-def debug_knobs(tc_heads_per_unit=-1, tc_late_ticket=-1, simt_two_pass=-1, conv_tma=-1, tc_segment_chunks=-1):
+def debug_knobs(tc_heads_per_unit=-1, tc_late_ticket=-1, simt_two_pass=-1, conv_tma=-1, tc_segment_chunks=-1,
+                tc_head_flags=-1):
     """Test hook: force launch-configuration choices of later calls (-1 everywhere restores the library's own).
     tc_segment_chunks changes the workspace size: allocate the workspace after setting it."""
     st = lib().ssd_debug_knobs(int(tc_heads_per_unit), int(tc_late_ticket), int(simt_two_pass), int(conv_tma),
-                               int(tc_segment_chunks))
+                               int(tc_segment_chunks), int(tc_head_flags))
     if st:
         raise SsdError(st, "ssd_debug_knobs")

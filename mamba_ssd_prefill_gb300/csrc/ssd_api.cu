@@ -28,13 +28,13 @@ EncodeTiledFn encode_tiled_fn() {
 
 namespace {
 // heads per unit, late ticket, SIMT two pass, conv TMA, chunks per segment
-std::atomic<int> g_knob[5] = {{-1}, {-1}, {-1}, {-1}, {-1}};
+std::atomic<int> g_knob[6] = {{-1}, {-1}, {-1}, {-1}, {-1}, {-1}};
 }  // namespace
 
 Knobs knobs() {
     return Knobs{g_knob[0].load(std::memory_order_relaxed), g_knob[1].load(std::memory_order_relaxed),
                  g_knob[2].load(std::memory_order_relaxed), g_knob[3].load(std::memory_order_relaxed),
-                 g_knob[4].load(std::memory_order_relaxed)};
+                 g_knob[4].load(std::memory_order_relaxed), g_knob[5].load(std::memory_order_relaxed)};
 }
 
 }  // namespace ssd
@@ -74,6 +74,7 @@ struct Plan {
     bool varlen = false;
     int heads_per_unit = 1;  // TC only
     bool late_ticket = false;  // TC only: next ticket taken when the unit before it nears its end
+    bool head_flags = false;   // TC only, fp32 states: one release flag per head
     uint32_t total_units = 0;
     ssd::SegChoice seg{1, 0, 0, 0, 1};  // TC only, regular batches: two-level state passing when seg.nseg > 1
     size_t flags_off = 0, ring_off = 0, tab_off = 0, seg_off = 0, blk_s_off = 0, blk_L_off = 0, bytes = 0;
@@ -158,6 +159,8 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out, bool segment
                                              std::max(1, sm_count()));
         // test hook: forced early (0) or late (1) tickets
         if (kn.tc_late_ticket >= 0) pl.late_ticket = kn.tc_late_ticket == 1;
+        pl.head_flags = ssd::tc_head_flags(pl.nseq * pl.seg.nseg * pr->nheads, pl.late_ticket, std::max(1, sm_count()));
+        if (kn.tc_head_flags >= 0) pl.head_flags = kn.tc_head_flags == 1;  // test hook
     } else {
         units = (double)(varlen ? pl.nc + pl.nseq : pl.nc * pr->batch) * (double)pr->nheads;
     }
@@ -254,6 +257,7 @@ ssd_status_t run(const ssd_problem_t *prob, int64_t nseq, const int32_t *cu_seql
     p.ring_bytes = (int64_t)(pl.tab_off - pl.ring_off);
     p.flag_count = (int64_t)((pl.ring_off - pl.flags_off) / sizeof(uint64_t));
     p.tc_late_ticket = pl.late_ticket ? 1 : 0;
+    p.tc_head_flags = pl.head_flags ? 1 : 0;
     p.x_ld = x_ld ? x_ld : pr.nheads * pr.headdim;
     p.bc_ld = bc_ld ? bc_ld : pr.ngroups * pr.dstate;
     ssd::SegPlan sp{pl.seg.blk, pl.seg.nblk, pl.seg.hs, reinterpret_cast<float *>(ws + pl.blk_s_off),
@@ -456,11 +460,12 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
 }
 
 SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,
-                                     int32_t conv_tma, int32_t tc_segment_chunks) {
+                                     int32_t conv_tma, int32_t tc_segment_chunks, int32_t tc_head_flags) {
     if (tc_heads_per_unit != -1 && (tc_heads_per_unit < 1 || tc_heads_per_unit > 8)) return SSD_ERR_INVALID_ARG;
     if (tc_late_ticket < -1 || tc_late_ticket > 1 || simt_two_pass < -1 || simt_two_pass > 1 || conv_tma < -1 ||
-        conv_tma > 1 || tc_segment_chunks < -1)
+        conv_tma > 1 || tc_segment_chunks < -1 || tc_head_flags < -1 || tc_head_flags > 1)
         return SSD_ERR_INVALID_ARG;
+    ssd::g_knob[5].store(tc_head_flags, std::memory_order_relaxed);
     ssd::g_knob[4].store(tc_segment_chunks, std::memory_order_relaxed);
     ssd::g_knob[0].store(tc_heads_per_unit, std::memory_order_relaxed);
     ssd::g_knob[1].store(tc_late_ticket, std::memory_order_relaxed);

@@ -92,6 +92,7 @@ struct Params {
     const int2 *ctab;      // variable-length: (sequence, chunk) of each chunk pair, chunk-major
     const uint32_t *vtot;  // variable-length: number of chunk pairs (written by the planning kernel)
     int tc_late_ticket;    // tensor-core kernel: take each next ticket only when the unit before it nears its end
+    int tc_head_flags;     // tensor-core kernel, fp32 states: one release flag per head (by the C.S warp), not per row
     int64_t ring_bytes, flag_count;  // extents of the ring and the flags (bounds-checked builds compare with them)
     // Two-level state passing (tensor-core kernel, regular batches): with nseg > 1 every sequence is cut into nseg
     // segments of seg_chunks chunks (the last one shorter or equal), the chunk-to-chunk state chain restarts at

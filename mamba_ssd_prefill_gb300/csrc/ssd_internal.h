@@ -27,6 +27,7 @@ EncodeTiledFn encode_tiled_fn();
 struct Knobs {
     int tc_heads_per_unit, tc_late_ticket, simt_two_pass, conv_tma;
     int tc_segment_chunks;  // -1: the library's choice, 0: one state chain per sequence, >= 1: chunks per segment
+    int tc_head_flags;      // -1: the library's choice, 0: a release flag per state row, 1: one per head
 };
 Knobs knobs();
 
@@ -51,6 +52,7 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype);
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int heads_per_unit);
 int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms);
 bool tc_late_ticket(int64_t units_per_chunk, int sms);  // ticket order = finishing order (chain-bound problems)
+bool tc_head_flags(int64_t chains_per_position, bool late_ticket, int sms);  // fp32 states: one release per head
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int heads_per_unit, int sms, cudaStream_t stream);
 
 // two-level state passing (ssd_segstate.cu): segment entering states from block aggregates, before launch_tc

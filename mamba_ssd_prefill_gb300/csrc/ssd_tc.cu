@@ -375,7 +375,9 @@ __device__ __noinline__ void p_block_exact(uint32_t cb_col, uint32_t p_col, cons
     tmem_st16(p_col, pk);
 }
 
-template <typename IO, typename ST, bool CONV>
+// HF: fp32 states published behind one release flag per head, stored by the C.S warp (a separate instantiation,
+// so that the kernel without it keeps its own code).
+template <typename IO, typename ST, bool CONV, bool HF>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const Params p, const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
               const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_y,
@@ -813,9 +815,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Per head, once the chain has put the entering state into shared memory: y_inter = C . S_in into the
         // columns of the head's chunk state (already read by the chain). Issued apart from MMA1 so that neither
         // waits behind the other's issue; like MMA1, by one elected lane of the whole warp, K steps unrolled.
+        // With fp32 states and per-head flags (HF) this warp also publishes the head's leaving state:
+        // every chain thread stored its row before arriving on sin_full (release, CTA scope), this warp's wait
+        // acquires them, and one release store of the head's flag at GPU scope (cumulative: it orders the rows
+        // this warp has observed) publishes the whole state, right after C.S is issued. The chain threads then
+        // never wait on a release fence (about half a microsecond a head), at the price of a later publish.
         {
             constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
+            static_assert(!HF || sizeof(ST) == 4, "per-head flags publish fp32 states");
             const bool leader = elect_one();
+            const int64_t skip = hdr->skip_publish - 1;
+            uint64_t *flags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]: row 0's place per head
+            (void)skip;
+            (void)flags;
             for (uint32_t h2 = 0;; ++h2) {
                 const uint32_t k3 = h2 % 3, k = h2 & 1;
                 if (!BWAIT(&sm.tab_full[h2 % 4], (h2 / 4) & 1)) break;
@@ -835,6 +847,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (last_of_unit) mma_commit(&sm.bc_empty[u]);  // last reader of the unit's B/C
                 }
                 __syncwarp();
+                if constexpr (HF) {
+                    const HeadTab &tb = sm.tab[h2 % 4];
+                    const int c = tb.c;
+                    // no publish after the last chunk of a sequence or of a segment
+                    if (lane == 0 && !tb.last && c != skip && !(p.nseg > 1 && (c + 1) % p.seg_chunks == 0))
+                        st_release_u64(chk(flags, (chain_of(p, tb.s, c, tb.h) * 2 + ((c + 1) & 1)) * kN, 1,
+                                           p.flag_count, hdr, SITE_TC_FLAG),
+                                       ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
+                    __syncwarp();
+                }
                 if (lane == 0) TRACE(warp, 3, h2);
             }
             if (leader) {
@@ -1090,7 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ chain warpgroup
         // Thread n owns d_state row n of every state and passes it to the next chunk through a 2-slot ring per
         // chain, with no CTA barrier on either side of a hop:
-        //  - fp32 states: the row, then its own release flag (a 64-bit tag epoch:chunk);
+        //  - fp32 states: the row, then its release flag (a 64-bit tag epoch:chunk): per row, by its thread, or
+        //    (HF) one per head, by the C.S warp once all 128 rows are stored;
         //  - fp16 states: every 8-byte ring word carries two values and the 32-bit tag epoch * 1024 + (chunk mod
         //    1024). A slot can still hold any earlier chunk of its chain that a unit in flight has not yet
         //    overwritten; at most two tickets per CTA are unfinished, so those chunks lie fewer than 2 x SMs
@@ -1116,8 +1139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        SITE_TC_RING);
         };
         auto vtag = [&](int c) { return (epoch << 10) | (uint32_t)(c & 1023); };
-        auto tag_of = [&](int64_t chain, int c) {
-            return chk(tags, (chain * 2 + (c & 1)) * kN + nrow, 1, p.flag_count, hdr, SITE_TC_FLAG);
+        auto tag_of = [&](int64_t chain, int c) {  // fp32: the row's flag, or with HF the head's (row 0's place)
+            return chk(tags, (chain * 2 + (c & 1)) * kN + (HF ? 0 : nrow), 1, p.flag_count, hdr, SITE_TC_FLAG);
         };
         auto want_of = [&](int c) { return ((uint64_t)epoch << 32) | (uint32_t)c; };
         float S[kP];  // entering state of the current head (fp32)
@@ -1251,9 +1274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             mbar_arrive(&sm.sin_full[k2]);
             if (lane == 0) TRACE(warp, 4, hc);
-            // publish this head's row (the release orders the row's stores before the tag)
-            if (publish && !kTagged)
-                st_release_u64(tags + (rchain * 2 + ((c + 1) & 1)) * kN + nrow, ((uint64_t)epoch << 32) | (uint32_t)(c + 1));
+            // per-row flags: publish this head's row (the release orders the row's stores before the tag)
+            if (publish && !kTagged && !HF) st_release_u64(tag_of(rchain, c + 1), want_of(c + 1));
         }
     }
 #undef BWAIT
@@ -1297,7 +1319,7 @@ bool make_map(CUtensorMap *m, const void *base, bool bf16, int64_t inner, int64_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename IO, typename ST, bool CONV>
+template <typename IO, typename ST, bool CONV, bool HF>
 cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
     CUtensorMap mx, mb, mc, my, mxh;
     const bool bf = !std::is_same<IO, __half>::value;
@@ -1308,7 +1330,7 @@ cudaError_t launch_t(const Params &p, int hs, int sms, cudaStream_t stream) {
     if (CONV ? !make_map(&mxh, p.x, bf, kP, p.H, T, p.x_ld, 3, false) : false) return cudaErrorInvalidValue;
     if (!CONV) mxh = mx;
     const size_t smem = sizeof(Smem<CONV>) + 1024;
-    auto k = tc_kernel<IO, ST, CONV>;
+    auto k = tc_kernel<IO, ST, CONV, HF>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = p.ctab ? (int64_t)sms : std::min<int64_t>((int64_t)p.total_units, (int64_t)sms);
@@ -1339,6 +1361,15 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
 // units share one, the loads then exposed at every unit boundary cost more than the chain.
 bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 4 <= sms; }
 
+// fp32 states: one release flag per head, stored by the C.S warp after all rows, frees the chain threads of a
+// release fence every head but publishes a head's state later (once its C.S is issued). That pays only where a
+// chunk's successor starts well after it: early tickets and many head chains per chunk position (the 2.7B layer
+// at batch 8 and 32: -8 % and -4 %); the 256K-token layer in 4 segments (320 chains) lost 14 %, late-ticket
+// launches 10-15 % (same-box A/B).
+bool tc_head_flags(int64_t chains_per_position, bool late_ticket, int sms) {
+    return !late_ticket && chains_per_position >= 3 * (int64_t)sms;
+}
+
 uint32_t tc_total_units(int64_t batch, int64_t H, int64_t G, int64_t nc, int hs) {
     (void)G;
     return (uint32_t)(nc * batch * (H / hs));
@@ -1354,13 +1385,22 @@ int tc_heads_per_unit(int64_t batch, int64_t H, int64_t G, int64_t nc, int sms) 
     return 1;
 }
 
+// fp32 states: per-head flags where the plan chose them (not with the fused convolution)
+template <typename IO, bool CONV>
+cudaError_t launch_f32(const Params &p, int hs, int sms, cudaStream_t stream) {
+    if constexpr (!CONV) {
+        if (p.tc_head_flags) return launch_t<IO, float, CONV, true>(p, hs, sms, stream);
+    }
+    return launch_t<IO, float, CONV, false>(p, hs, sms, stream);
+}
+
 template <bool CONV>
 cudaError_t launch_any(const Params &p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
     if (io_dtype == 1)
-        return state_dtype == 0 ? launch_t<__nv_bfloat16, float, CONV>(p, hs, sms, stream)
-                                : launch_t<__nv_bfloat16, __half, CONV>(p, hs, sms, stream);
-    return state_dtype == 0 ? launch_t<__half, float, CONV>(p, hs, sms, stream)
-                            : launch_t<__half, __half, CONV>(p, hs, sms, stream);
+        return state_dtype == 0 ? launch_f32<__nv_bfloat16, CONV>(p, hs, sms, stream)
+                                : launch_t<__nv_bfloat16, __half, CONV, false>(p, hs, sms, stream);
+    return state_dtype == 0 ? launch_f32<__half, CONV>(p, hs, sms, stream)
+                            : launch_t<__half, __half, CONV, false>(p, hs, sms, stream);
 }
 
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {

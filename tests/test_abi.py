@@ -195,11 +195,11 @@ def test_bounds_checked_build_compiles_and_exports_every_symbol():
 def test_debug_knobs_validate_and_restore(lib):
     """The launch-configuration test hooks take -1 (the library's choice) or a valid value, and reject the rest
     without changing anything."""
-    assert lib.ssd_debug_knobs(-1, -1, -1, -1, -1) == 0
-    for bad in [(0, -1, -1, -1, -1), (9, -1, -1, -1, -1), (-1, 2, -1, -1, -1), (-1, -1, -2, -1, -1),
-                (-1, -1, -1, 5, -1), (-1, -1, -1, -1, -2)]:
+    assert lib.ssd_debug_knobs(-1, -1, -1, -1, -1, -1) == 0
+    for bad in [(0, -1, -1, -1, -1, -1), (9, -1, -1, -1, -1, -1), (-1, 2, -1, -1, -1, -1), (-1, -1, -2, -1, -1, -1),
+                (-1, -1, -1, 5, -1, -1), (-1, -1, -1, -1, -2, -1), (-1, -1, -1, -1, -1, 2), (-1, -1, -1, -1, -1, -2)]:
         assert lib.ssd_debug_knobs(*bad) == 1, bad
-    assert lib.ssd_debug_knobs(8, 1, 0, 0, 4) == 0
+    assert lib.ssd_debug_knobs(8, 1, 0, 0, 4, 1) == 0
     m.debug_knobs()  # restore
     with pytest.raises(m.SsdError):
         m.debug_knobs(tc_heads_per_unit=0)
