@@ -375,7 +375,7 @@ def run_gpu(args, w):
             "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg, "roofline": roof,
             "e2e": {"value": world * w.tokens / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "path": "ssd_fwd_host: pinned host buffers streamed in 8 token pieces (copies overlap compute)"},
+                    "path": "ssd_fwd_host: pinned host buffers streamed in token pieces of about 256 MiB of copies, 8 to 32 (copies overlap compute)"},
             "gpu_launches": args.steps * plan["launches"], "clocks": clk.summary(wall0, wall1, load_end)}
     if world == 1 and not args.no_cpu_baseline:
         import oracle

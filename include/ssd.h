@@ -247,8 +247,9 @@ SSD_API ssd_status_t ssd_fwd_static_scratch(const ssd_problem_t *prob, const voi
  * pieces so that the host<->device copies overlap the computation (no
  * counterpart on the pages; a library convenience for batches that live in
  * host memory).
- *  pieces       number of pieces (0: the library's choice, 8; at most one
- *               per chunk). The batch is cut along its tokens at multiples of
+ *  pieces       number of pieces (0: the library's choice, about 256 MiB of
+ *               copies per piece and from 8 to 32 pieces; at most one per
+ *               chunk). The batch is cut along its tokens at multiples of
  *               chunk_size, each piece holding the same token range of every
  *               sequence; the states leaving one piece enter the next (the
  *               same chunks, in the same order and precision, as one call).
