@@ -144,7 +144,8 @@ ssd_status_t plan(const ssd_problem_t *pr, int64_t nseq, Plan *out, bool segment
         if (!varlen && segments) {
             // test hook: forced chunks per segment (0: off)
             const int forced = ssd::knobs().tc_segment_chunks;
-            pl.seg = ssd::choose_segments(pl.nseq, pl.nc, pr->nheads, pr->ngroups, std::max(1, sm_count()), forced);
+            pl.seg = ssd::choose_segments(pl.nseq, pl.nc, pr->nheads, pr->ngroups, std::max(1, sm_count()), forced,
+                                          pr->state_dtype == SSD_F32);
             chains *= pl.seg.nseg;  // one state chain per (sequence, segment, head)
         }
         // for a variable-length batch the chunk count is only bounded here (pairs <= nc + nseq); it sizes the units

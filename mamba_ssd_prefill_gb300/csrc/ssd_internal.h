@@ -61,7 +61,7 @@ struct SegChoice {
     int64_t blk, nblk;         // chunks per aggregate block, blocks per sequence with an aggregate
     int hs;                    // heads per block-kernel work unit
 };
-SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced);
+SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced, bool fp32_states);
 struct SegPlan {
     int64_t blk, nblk;
     int hs;

@@ -602,19 +602,21 @@ cudaError_t launch_blocks(const Params &p, const SegPlan &sp, int sms, cudaStrea
 // the larger of two times: its per-head cadence spread over the SMs (about 2.3 us per head and chunk) and the
 // serial state chain of a sequence (about 2.4 us per chunk to chunk hop). Two-level passing costs a block pass
 // over most of x (about 0.9 us per head and chunk on an SM) and two more launches, so it is taken only where the
-// launch is long (at least 256 heads x chunks per SM) and the chain is at least 1.5 times the cadence time;
+// launch is long (at least 256 heads x chunks per SM) and the chain is at least 1.5 times the cadence time, or,
+// on shorter launches with fp32 states (a hop of about 3 us: flag, then data), at least 2.2 times (the 8K-token
+// batch-1 layer: 4 segments of 16 chunks, 0.168 against 0.193 ms; the 130M-shaped batch, at 2.1 times, is 8 %
+// slower segmented, and the 16K-token layer with fp16 states, at 1.9 times, 7 %);
 // segments are then cut so that a segment's chain takes at most half the cadence time, rounded up to a multiple
 // of 8 chunks (measured on the 2.7B-shaped 256K-token sequence with fp32 states: 4
-// segments of 512 chunks 3.55 ms, 5 of 410 3.70, 6 of 342 3.64, 8 of 256 3.74, 2 of 1024 3.74; the 8K-token
-// batch-1 layer gains 16 % with 8 segments of 8 chunks but the 16K one loses 7 %, so short sequences keep one
-// chain). A segment with no block length in [min(segment, 8), 32] keeps one chain. A block holds at least
+// segments of 512 chunks 3.55 ms, 5 of 410 3.70, 6 of 342 3.64, 8 of 256 3.74, 2 of 1024 3.74). A segment with
+// no block length in [min(segment, 8), 32] keeps one chain. A block holds at least
 // min(segment, 8) chunks, so that its
 // aggregate (32 KB a head) costs at most a quarter of the x it reads; among such blocks and the head counts per
 // unit (2, 4 or 8 dividing the heads per group: a chunk's heads then fill consecutive ring slots and share MMAs
 // of up to N = 256, and each X' warpgroup owns half of them; groups of an odd number of heads keep one chain per
 // sequence), the first pair, by more heads then longer blocks, that gives every SM two block units, else the pair
 // with the most units.
-SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced) {
+SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sms, int64_t forced, bool fp32_states) {
     SegChoice r{1, nc, 0, 0, 1};
     if (nseq < 1 || nc < 2 || sms < 1) return r;
     int64_t seg;
@@ -623,7 +625,12 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
         seg = forced;
     } else {
         const double per_sm = (double)nseq * (double)nc * (double)H / sms, cadence_us = per_sm * 2.3;
-        if (per_sm < 256.0 || (double)nc * 2.4 < 1.5 * cadence_us) return r;
+        // long launches: a chain at least 1.5 x the cadence time; shorter ones (the block pass and two more
+        // launches weigh more) only with fp32 states, whose hop (flag, then data) costs about 3 us, and a chain at
+        // least 2.2 x the cadence time
+        const bool long_launch = per_sm >= 256.0 && (double)nc * 2.4 >= 1.5 * cadence_us;
+        const bool short_fp32 = per_sm < 256.0 && fp32_states && (double)nc * 3.0 >= 2.2 * cadence_us;
+        if (!long_launch && !short_fp32) return r;
         const int64_t seg_max = (int64_t)(cadence_us / (2.0 * 2.4));
         if (seg_max >= nc || seg_max < 8) return r;
         const int64_t nseg0 = (nc + seg_max - 1) / seg_max;
