@@ -209,10 +209,12 @@ SSD_API ssd_status_t ssd_debug_set(void *workspace, uint64_t timeout_ns, int64_t
  *                     when it cuts a sequence into two or more segments.
  *                     It changes the workspace size: set it before
  *                     ssd_fwd_workspace_size.
- *  tc_head_flags      tensor-core kernel, fp32 states: 0 = every state row
- *                     published behind its own release flag by its chain
- *                     thread, 1 = one release flag per head, stored by the C.S
- *                     warp once all rows are written
+ *  tc_head_flags      tensor-core kernel: 0 = states passed the default way
+ *                     (fp32: every row behind its own release flag, stored by
+ *                     its chain thread; fp16: tagged words), 1 = one release
+ *                     flag per head, stored by the C.S warp once all rows are
+ *                     written (fp16 states then as plain halves). The library
+ *                     chooses 1 only for fp32 states.
  * The values are read by later calls on any host thread (not by calls already
  * queued). The library reads no environment variable. */
 SSD_API ssd_status_t ssd_debug_knobs(int32_t tc_heads_per_unit, int32_t tc_late_ticket, int32_t simt_two_pass,

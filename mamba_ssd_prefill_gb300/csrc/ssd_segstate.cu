@@ -631,7 +631,8 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
         const bool long_launch = per_sm >= 256.0 && (double)nc * 2.4 >= 1.5 * cadence_us;
         const bool short_fp32 = per_sm < 256.0 && fp32_states && (double)nc * 3.0 >= 2.2 * cadence_us;
         if (!long_launch && !short_fp32) return r;
-        const int64_t seg_max = (int64_t)(cadence_us / (2.0 * 2.4));
+        // fp16 states: segments half as long (their chains run with per-head flags, which want many of them)
+        const int64_t seg_max = (int64_t)(cadence_us / ((fp32_states ? 2.0 : 4.0) * 2.4));
         if (seg_max >= nc || seg_max < 8) return r;
         const int64_t nseg0 = (nc + seg_max - 1) / seg_max;
         seg = (nc + nseg0 - 1) / nseg0;

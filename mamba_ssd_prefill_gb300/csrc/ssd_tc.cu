@@ -822,7 +822,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // never wait on a release fence (about half a microsecond a head), at the price of a later publish.
         {
             constexpr uint32_t idCS = idesc_f16_f32(128, 64, false, true);
-            static_assert(!HF || sizeof(ST) == 4, "per-head flags publish fp32 states");
             const bool leader = elect_one();
             const int64_t skip = hdr->skip_publish - 1;
             uint64_t *flags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]: row 0's place per head
@@ -1130,7 +1129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ST *init = static_cast<const ST *>(p.init);
         ST *fin = static_cast<ST *>(p.final_states);
         uint64_t *tags = reinterpret_cast<uint64_t *>(p.flags);  // [chain][slot][row]
-        constexpr bool kTagged = sizeof(ST) == 2;
+        constexpr bool kTagged = sizeof(ST) == 2 && !HF;  // fp16 states in tagged words
+        constexpr bool kPlain16 = sizeof(ST) == 2 && HF;  // fp16 states as plain halves behind the head's flag
         ulonglong2 *ringv = static_cast<ulonglong2 *>(p.ring);  // fp16: [chain][slot][P / 4 vectors][row]
         const int64_t nvec = p.ring_bytes / 16, nstate = p.nseq * p.H * kP * kN;  // extents (bounds-checked builds)
         // row nrow of a slot: 16 vectors kN apart (checked as one span)
@@ -1201,16 +1201,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (ld_acquire_u64(tag_of(rchain, c)) == want_of(c) ||
                        (!aborted(hdr, epoch) && wait_tag(tag_of(rchain, c), want_of(c), epoch, hdr, limit, (uint32_t)c))) {
-                const float4 *src = chk(reinterpret_cast<const float4 *>(p.ring),
-                                        (rchain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
-                                        nvec, hdr, SITE_TC_RING);
+                if constexpr (kPlain16) {  // 8 vectors of 8 halves, kN apart
+                    const uint4 *src = chk(reinterpret_cast<const uint4 *>(p.ring),
+                                           (rchain * 2 + (c & 1)) * (int64_t)(kP / 8 * kN) + nrow,
+                                           (kP / 8 - 1) * kN + 1, nvec, hdr, SITE_TC_RING);
 #pragma unroll
-                for (int m = 0; m < kP / 4; ++m) {
-                    const float4 f = __ldcg(src + m * kN);
-                    S[4 * m] = f.x;
-                    S[4 * m + 1] = f.y;
-                    S[4 * m + 2] = f.z;
-                    S[4 * m + 3] = f.w;
+                    for (int m = 0; m < kP / 8; ++m) {
+                        const uint4 v = __ldcg(src + m * kN);
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_f16(w4[e]);
+                            S[8 * m + 2 * e] = f.x;
+                            S[8 * m + 2 * e + 1] = f.y;
+                        }
+                    }
+                } else {
+                    const float4 *src = chk(reinterpret_cast<const float4 *>(p.ring),
+                                            (rchain * 2 + (c & 1)) * (int64_t)(kP / 4 * kN) + nrow,
+                                            (kP / 4 - 1) * kN + 1, nvec, hdr, SITE_TC_RING);
+#pragma unroll
+                    for (int m = 0; m < kP / 4; ++m) {
+                        const float4 f = __ldcg(src + m * kN);
+                        S[4 * m] = f.x;
+                        S[4 * m + 1] = f.y;
+                        S[4 * m + 2] = f.z;
+                        S[4 * m + 3] = f.w;
+                    }
                 }
             } else {  // the error is recorded; carry on with zeros so the CTA drains
 #pragma unroll
@@ -1229,9 +1246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *srow = sm.x[hc % 3] + nrow * 128;  // the x tile is dead once MMA1 has read it
             float4 *dst32 = nullptr;
             ulonglong2 *dst16 = nullptr;
+            uint4 *dsth = nullptr;
             if (publish) {
                 if (kTagged)
                     dst16 = vrow_of(rchain, c + 1);
+                else if (kPlain16)
+                    dsth = chk(reinterpret_cast<uint4 *>(p.ring),
+                               (rchain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 8 * kN) + nrow, (kP / 8 - 1) * kN + 1,
+                               nvec, hdr, SITE_TC_RING);
                 else
                     dst32 = chk(reinterpret_cast<float4 *>(p.ring),
                                 (rchain * 2 + ((c + 1) & 1)) * (int64_t)(kP / 4 * kN) + nrow, (kP / 4 - 1) * kN + 1,
@@ -1258,6 +1280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 4; ++j)
                             st_ring(dst16 + (4 * m + j) * kN, tg | pack_f16(o[4 * j], o[4 * j + 1]),
                                     tg | pack_f16(o[4 * j + 2], o[4 * j + 3]));
+                    } else if (kPlain16) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+                            __stcg(dsth + (2 * m + j) * kN,
+                                   make_uint4(pack_f16(o[8 * j], o[8 * j + 1]), pack_f16(o[8 * j + 2], o[8 * j + 3]),
+                                              pack_f16(o[8 * j + 4], o[8 * j + 5]), pack_f16(o[8 * j + 6], o[8 * j + 7])));
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
@@ -1361,11 +1389,12 @@ size_t tc_ring_bytes(int64_t chains, int64_t P, int64_t N, int state_dtype) {
 // units share one, the loads then exposed at every unit boundary cost more than the chain.
 bool tc_late_ticket(int64_t units_per_chunk, int sms) { return units_per_chunk * 4 <= sms; }
 
-// fp32 states: one release flag per head, stored by the C.S warp after all rows, frees the chain threads of a
-// release fence every head but publishes a head's state later (once its C.S is issued). That pays only where a
-// chunk's successor starts well after it: early tickets and many head chains per chunk position (the 2.7B layer
-// at batch 8 and 32: -8 % and -4 %); the 256K-token layer in 4 segments (320 chains) lost 14 %, late-ticket
-// launches 10-15 % (same-box A/B).
+// One release flag per head, stored by the C.S warp after all rows, frees the chain threads of a release fence
+// every head (fp32 states) or of tagged ring words (fp16 states, then plain halves), but publishes a head's state
+// later (once its C.S is issued). That pays only where a chunk's successor starts well after it: early tickets and
+// many head chains per chunk position (the 2.7B layer at batch 8: fp32 -12 %, fp16 -20 %; batch 32 fp32 -5 %; the
+// 256K-token layer with fp16 states in 8 segments, 640 chains, -4 %); with fp32 states in 4 segments (320 chains)
+// that layer lost 12 %, late-ticket launches 10-30 % (same-box A/B).
 bool tc_head_flags(int64_t chains_per_position, bool late_ticket, int sms) {
     return !late_ticket && chains_per_position >= 3 * (int64_t)sms;
 }
@@ -1394,13 +1423,21 @@ cudaError_t launch_f32(const Params &p, int hs, int sms, cudaStream_t stream) {
     return launch_t<IO, float, CONV, false>(p, hs, sms, stream);
 }
 
+// fp16 states: plain halves behind per-head flags where asked (not with the fused convolution), else tagged words
+template <typename IO, bool CONV>
+cudaError_t launch_f16(const Params &p, int hs, int sms, cudaStream_t stream) {
+    if constexpr (!CONV) {
+        if (p.tc_head_flags) return launch_t<IO, __half, CONV, true>(p, hs, sms, stream);
+    }
+    return launch_t<IO, __half, CONV, false>(p, hs, sms, stream);
+}
+
 template <bool CONV>
 cudaError_t launch_any(const Params &p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {
     if (io_dtype == 1)
         return state_dtype == 0 ? launch_f32<__nv_bfloat16, CONV>(p, hs, sms, stream)
-                                : launch_t<__nv_bfloat16, __half, CONV, false>(p, hs, sms, stream);
-    return state_dtype == 0 ? launch_f32<__half, CONV>(p, hs, sms, stream)
-                            : launch_t<__half, __half, CONV, false>(p, hs, sms, stream);
+                                : launch_f16<__nv_bfloat16, CONV>(p, hs, sms, stream);
+    return state_dtype == 0 ? launch_f32<__half, CONV>(p, hs, sms, stream) : launch_f16<__half, CONV>(p, hs, sms, stream);
 }
 
 cudaError_t launch_tc(Params p, int io_dtype, int state_dtype, int hs, int sms, cudaStream_t stream) {

@@ -57,6 +57,8 @@ WORKLOADS = {
     "m2p7-L8k-b1": Workload("m2p7-L8k-b1", 1, 8192, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal", seed=1004),
     "m2p7-L8k-b8": Workload("m2p7-L8k-b8", 8, 8192, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal", seed=1004),
     "m2p7-L8k-b32": Workload("m2p7-L8k-b32", 32, 8192, 80, 64, 128, 1, 128, io="bf16", state="f32", init="normal", seed=1004),
+    "m2p7-L8k-b8-f16": Workload("m2p7-L8k-b8-f16", 8, 8192, 80, 64, 128, 1, 128, io="bf16", state="f16", init="normal",
+                                seed=1004),
     "long-L256k-g8": Workload("long-L256k-g8", 1, 262144, 80, 64, 128, 8, 128, io="bf16", state="f32", init="none",
                               dt_lo=1e-4, seed=1005),
     # the long-context layer at 1/8 of its length (profiling captures: 0.8 GB of inputs and outputs)

@@ -284,18 +284,20 @@ def test_tc_segments_with_tickets_and_heads(late, hs, knobs):
     assert torch.equal(y, y2) and torch.equal(fin, f2)
 
 
+@pytest.mark.parametrize("state", ["f32", "f16"])
 @pytest.mark.parametrize("late", [0, 1], ids=["early-tickets", "late-tickets"])
 @pytest.mark.parametrize("seg", [0, 4], ids=["one-chain", "segments"])
-def test_tc_head_flags(late, seg, knobs):
-    """fp32 states published behind one release flag per head (stored by the C.S warp once every row is written)
-    or behind one flag per row (each row's thread): the oracle's values, and the same bits either way, under both
-    ticket orders, with and without segments."""
-    w = WORKLOADS["m130-bf16"].with_(batch=3, seqlen=2200, nheads=8, ngroups=2, seed=97)
+def test_tc_head_flags(state, late, seg, knobs):
+    """States published behind one release flag per head (stored by the C.S warp once every row is written; fp16
+    states then as plain halves) or the default way (fp32: a flag per row, by each row's thread; fp16: tagged
+    words): the oracle's values, and the same bits either way, under both ticket orders, with and without
+    segments."""
+    w = WORKLOADS["m130-bf16"].with_(batch=3, seqlen=2200, nheads=8, ngroups=2, seed=97, state=state)
     inp = make_inputs(w, device="cuda")
     yr, fr = oracle.ssd_reference(**cpu(inp))
     knobs(tc_late_ticket=late, tc_segment_chunks=seg, tc_head_flags=1)
     y, fin = run_gpu(w, inp, kernel="tc")
-    assert_parity(w, y, fin, yr, fr, f"tc head flags late={late} seg={seg}", kernel="tc")
+    assert_parity(w, y, fin, yr, fr, f"tc head flags {state} late={late} seg={seg}", kernel="tc")
     knobs(tc_head_flags=0)
     y2, f2 = run_gpu(w, inp, kernel="tc")
     assert torch.equal(y, y2) and torch.equal(fin, f2)
