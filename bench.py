@@ -368,6 +368,7 @@ def run_gpu(args, w):
         del dtv
     cfg.update({"kernel": kernel, "segments": plan["segments"], "segment_chunks": plan["segment_chunks"],
                 "launches_per_step": plan["launches"],
+                "state_flags": "one release flag per head" if plan["head_flags"] else "per state row (fp32) or tagged words (fp16)",
                 "l2": f"{FLUSH_BYTES >> 20} MiB buffer written before every step, outside the events",
                 "wall_s_timed_region": round(wall, 3)})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -294,13 +294,19 @@ SSD_API int ssd_fwd_kernel_for(const ssd_problem_t *prob);
  * Fusion", state passing step, regrouped): a block kernel and a combine kernel
  * compute the states entering the segments before the fused kernel, whose
  * chunk-to-chunk state chain then restarts at every segment. segments == 1:
- * one chain per sequence. */
+ * one chain per sequence. head_flags == 1: the tensor-core kernel publishes
+ * each head's passed state behind one release flag, stored by the warp that
+ * issues the head's C.S once every state row is written (fp16 states then as
+ * plain halves); 0: fp32 rows each behind their own flag, fp16 states in tagged
+ * words. The struct grew head_flags in ABI 1.1 (ssd_version() >= 10100). */
 typedef struct {
     int32_t kernel;          /* ssd_kernel_t (SSD_KERNEL_SIMT, _TC or _STEP)  */
     int32_t launches;        /* kernel launches per ssd_fwd call              */
     int64_t segments;        /* per sequence (1: no two-level state passing)  */
     int64_t segment_chunks;  /* chunks per segment                             */
     size_t workspace_bytes;  /* = ssd_fwd_workspace_size                       */
+    int32_t head_flags;      /* tensor-core kernel: one release flag per head */
+    int32_t reserved;        /* 0                                              */
 } ssd_plan_t;
 SSD_API ssd_status_t ssd_fwd_plan(const ssd_problem_t *prob, ssd_plan_t *plan);
 

@@ -36,7 +36,8 @@ class SsdProblem(ctypes.Structure):
 
 class SsdPlan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("launches", ctypes.c_int32), ("segments", ctypes.c_int64),
-                ("segment_chunks", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t)]
+                ("segment_chunks", ctypes.c_int64), ("workspace_bytes", ctypes.c_size_t),
+                ("head_flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class SsdError(RuntimeError):
@@ -109,13 +110,15 @@ def workspace_size(prob: SsdProblem) -> int:
 
 
 def plan_info(prob: SsdProblem) -> dict:
-    """What ssd_fwd plans for a regular batch: kernel, launches per call, segments, chunks per segment, workspace."""
+    """What ssd_fwd plans for a regular batch: kernel, launches per call, segments, chunks per segment, workspace,
+    and whether the tensor-core kernel passes states behind one release flag per head."""
     pl = SsdPlan()
     st = lib().ssd_fwd_plan(ctypes.byref(prob), ctypes.byref(pl))
     if st:
         raise SsdError(st, "ssd_fwd_plan")
     return {"kernel": {1: "simt", 2: "tc", 3: "step"}[pl.kernel], "launches": pl.launches, "segments": pl.segments,
-            "segment_chunks": pl.segment_chunks, "workspace_bytes": pl.workspace_bytes}
+            "segment_chunks": pl.segment_chunks, "workspace_bytes": pl.workspace_bytes,
+            "head_flags": bool(pl.head_flags)}
 
 
 def kernel_for(prob: SsdProblem) -> str:

@@ -338,6 +338,8 @@ SSD_API ssd_status_t ssd_fwd_plan(const ssd_problem_t *prob, ssd_plan_t *out) {
     out->segment_chunks = pl.seg.nseg > 1 ? pl.seg.seg_chunks : pl.nc;
     out->launches = !tokens ? 0 : (pl.seg.nseg > 1 ? 3 : 1);
     out->workspace_bytes = pl.bytes;
+    out->head_flags = pl.kernel == SSD_KERNEL_TC && pl.head_flags ? 1 : 0;
+    out->reserved = 0;
     return SSD_OK;
 }
 
@@ -488,6 +490,6 @@ SSD_API const char *ssd_status_string(ssd_status_t status) {
     return "unknown status";
 }
 
-SSD_API int ssd_version(void) { return 10000; }
+SSD_API int ssd_version(void) { return 10100; }
 
 }  // extern "C"

@@ -247,6 +247,22 @@ def test_segment_length_without_a_block_length_keeps_one_chain(lib):
         m.debug_knobs()
 
 
+def test_host_pieces_sized_by_bytes(lib):
+    """ssd_fwd_host's own piece count: about 256 MiB of copies a piece, from 8 to 32 pieces. The scratch of the
+    library's choice equals that of the piece count it picks: 8 for a 2 GB batch, 25 for the 256K-token layer
+    (6.5 GB of copies), 32 at most."""
+    def scratch(p, pieces):
+        n = ctypes.c_size_t(0)
+        assert lib.ssd_fwd_host_scratch_size(ctypes.byref(p), pieces, ctypes.byref(n)) == 0
+        return n.value
+    small = prob(batch=8, seqlen=8192, nheads=80)  # 1.4 GB of copies
+    assert scratch(small, 0) == scratch(small, 8) != scratch(small, 16)
+    long = prob(batch=1, seqlen=262144, nheads=80, ngroups=8)  # 6.5 GB of copies
+    assert scratch(long, 0) == scratch(long, 25) != scratch(long, 24)
+    huge = prob(batch=8, seqlen=262144, nheads=80, ngroups=8)  # 52 GB of copies
+    assert scratch(huge, 0) == scratch(huge, 32)
+
+
 def test_plan_query_reports_kernel_launches_and_segments(lib):
     """ssd_fwd_plan: the kernel, the launches of one call (three with two-level state passing: block aggregates,
     their combination, the fused kernel) and the segments, consistent with ssd_fwd_workspace_size."""
@@ -254,6 +270,13 @@ def test_plan_query_reports_kernel_launches_and_segments(lib):
     info = m.plan_info(p)
     assert info["kernel"] == "tc" and info["segments"] == 1 and info["launches"] == 1
     assert info["segment_chunks"] == 32 and info["workspace_bytes"] == m.workspace_size(p)
+    try:  # the per-head flag choice is reported as planned (forced both ways through the test hook)
+        for forced in (0, 1):
+            m.debug_knobs(tc_head_flags=forced)
+            assert m.plan_info(p)["head_flags"] == bool(forced)
+    finally:
+        m.debug_knobs()
+    assert not m.plan_info(prob(io_dtype=torch.float32, dstate=64))["head_flags"]  # SIMT kernel: no such flags
     try:
         m.debug_knobs(tc_segment_chunks=5)  # 32 chunks: 7 segments, the last of 2 chunks
         info = m.plan_info(p)
