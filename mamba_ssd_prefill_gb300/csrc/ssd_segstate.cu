@@ -605,7 +605,8 @@ cudaError_t launch_blocks(const Params &p, const SegPlan &sp, int sms, cudaStrea
 // launch is long (at least 256 heads x chunks per SM) and the chain is at least 1.5 times the cadence time, or,
 // on shorter launches with fp32 states (a hop of about 3 us: flag, then data), at least 2.2 times (the 8K-token
 // batch-1 layer: 4 segments of 16 chunks, 0.168 against 0.193 ms; the 130M-shaped batch, at 2.1 times, is 8 %
-// slower segmented, and the 16K-token layer with fp16 states, at 1.9 times, 7 %);
+// slower segmented), and with fp16 states at least 1.8 times (the 16K-token layer, at 1.98: 8 segments of 16
+// chunks with per-head flags, 0.279 against 0.293 ms; the 130M-shaped batch, at 1.67, 6-22 % slower);
 // segments are then cut so that a segment's chain takes at most half the cadence time, rounded up to a multiple
 // of 8 chunks (measured on the 2.7B-shaped 256K-token sequence with fp32 states: 4
 // segments of 512 chunks 3.55 ms, 5 of 410 3.70, 6 of 342 3.64, 8 of 256 3.74, 2 of 1024 3.74). A segment with
@@ -630,7 +631,9 @@ SegChoice choose_segments(int64_t nseq, int64_t nc, int64_t H, int64_t G, int sm
         // least 2.2 x the cadence time
         const bool long_launch = per_sm >= 256.0 && (double)nc * 2.4 >= 1.5 * cadence_us;
         const bool short_fp32 = per_sm < 256.0 && fp32_states && (double)nc * 3.0 >= 2.2 * cadence_us;
-        if (!long_launch && !short_fp32) return r;
+        // shorter fp16 launches: their segmented chains take per-head flags (plain halves, no tagged words)
+        const bool short_fp16 = per_sm < 256.0 && !fp32_states && (double)nc * 2.4 >= 1.8 * cadence_us;
+        if (!long_launch && !short_fp32 && !short_fp16) return r;
         // fp16 states: segments half as long (their chains run with per-head flags, which want many of them)
         const int64_t seg_max = (int64_t)(cadence_us / ((fp32_states ? 2.0 : 4.0) * 2.4));
         if (seg_max >= nc || seg_max < 8) return r;
