@@ -284,6 +284,34 @@ def test_tc_segments_with_tickets_and_heads(late, hs, knobs):
     assert torch.equal(y, y2) and torch.equal(fin, f2)
 
 
+PLANS = [
+    # workload: (segments, chunks per segment, per-head flags, launches) the library plans on a 152-SM GB300
+    ("m130-bf16", (1, 32, False, 1)),
+    ("m130-bf16-f16", (1, 32, False, 1)),
+    ("m2p7-L16k-q128", (8, 16, True, 3)),
+    ("m2p7-L8k-b1", (4, 16, False, 3)),
+    ("m2p7-L8k-b8", (1, 64, True, 1)),
+    ("m2p7-L8k-b8-f16", (1, 64, True, 1)),
+    ("m2p7-L8k-b32", (1, 64, True, 1)),
+    ("long-L256k-g8", (4, 512, False, 3)),
+    ("long-L256k-g8-f16", (8, 256, True, 3)),
+]
+
+
+@pytest.mark.parametrize("name,want", PLANS, ids=[n for n, _ in PLANS])
+def test_plans_of_the_measured_layers(name, want):
+    """The launch plan of every measured layer on this GPU: two-level state passing where the chain outweighs
+    the cadence (segments and their length), per-head state flags where many chains share a chunk position, and
+    the launches a call makes. Pins the planning constants against the shapes they were measured on."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("plans measured on a 152-SM GB300")
+    w = WORKLOADS[name]
+    p = m.make_problem(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk, DTYPES[w.io],
+                       DTYPES[w.state])
+    info = m.plan_info(p)
+    assert (info["segments"], info["segment_chunks"], info["head_flags"], info["launches"]) == want, info
+
+
 @pytest.mark.parametrize("state", ["f32", "f16"])
 @pytest.mark.parametrize("late", [0, 1], ids=["early-tickets", "late-tickets"])
 @pytest.mark.parametrize("seg", [0, 4], ids=["one-chain", "segments"])
